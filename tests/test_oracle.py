@@ -1,0 +1,453 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks one oracle function against something fixed independently:
+a library routine (scipy's Hadamard matrix, numpy int64 matmul), a closed
+form, a hand-derived worked example under tests/golden/, or an error bound
+that follows from the arithmetic.  Method source: page "Karpathy's Trick for
+Faster Local LLMs Finally Has Proper Tooling", section "How Uzu optimizes
+bytes and tokens per pass".
+"""
+import os
+import struct
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+from quantized_speculative_verify_gb300 import synth
+
+C_BITS = 0x3E3504F3
+C = np.float32(struct.unpack("<f", struct.pack("<I", C_BITS))[0])
+EPS32 = 2.0 ** -24
+
+
+def f32_bits(x) -> int:
+    return struct.unpack("<I", struct.pack("<f", float(x)))[0]
+
+
+def sylvester(n=32):
+    i = np.arange(n)
+    pc = np.vectorize(lambda v: bin(int(v)).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1, -1).astype(np.int64)
+
+
+# ---------------------------------------------------------------- signs ---
+def test_splitmix64_published_vector(golden_dir):
+    lines = [l.split() for l in open(os.path.join(golden_dir, "splitmix64.txt")) if l.strip() and l[0] != "#"]
+    seed = int(lines[0][1])
+    expect = [int(l[0]) for l in lines[1:]]
+    got = [int(v) for v in oracle.splitmix64(seed, len(expect))]
+    assert got == expect
+
+
+def test_sign_packing_follows_top_bits():
+    K = 256
+    raw = oracle.splitmix64(77, K)
+    signs = oracle.make_signs(77, K)
+    for i in range(K):
+        bit = (int(signs[i // 32]) >> (i % 32)) & 1
+        assert bit == int(raw[i]) >> 63
+    # roughly half the signs are negative
+    assert 0.35 < np.mean(oracle.signs_to_pm1(signs, K) < 0) < 0.65
+
+
+def test_make_signs_rejects_bad_K():
+    with pytest.raises(ValueError):
+        oracle.make_signs(1, 48)
+
+
+# ------------------------------------------------------------- Hadamard ---
+def oracle_hadamard_matrix():
+    """Column j of the butterfly applied to unit vector e_j, as an int matrix."""
+    H = np.zeros((32, 32), dtype=np.int64)
+    for j in range(32):
+        e = np.zeros(32, dtype=np.float32)
+        e[j] = 1.0
+        H[j] = oracle.fwht32(e).astype(np.int64)
+    return H
+
+
+def test_butterfly_is_sylvester_hadamard():
+    H = oracle_hadamard_matrix()
+    assert np.array_equal(H, scipy.linalg.hadamard(32).astype(np.int64))
+    assert np.array_equal(H, sylvester(32))
+    assert set(np.unique(H)) == {-1, 1}
+
+
+def test_hadamard_orthogonal():
+    H = oracle_hadamard_matrix()
+    assert np.array_equal(H @ H.T, 32 * np.eye(32, dtype=np.int64))
+
+
+def test_butterfly_equals_matrix_product_on_integers():
+    rng = np.random.default_rng(5)
+    H = scipy.linalg.hadamard(32).astype(np.int64)
+    for _ in range(50):
+        v = rng.integers(-(2 ** 18), 2 ** 18, size=32)
+        got = oracle.fwht32(v.astype(np.float32))
+        assert np.array_equal(got.astype(np.int64), v @ H)
+
+
+def test_butterfly_twice_is_32_identity():
+    rng = np.random.default_rng(6)
+    for _ in range(20):
+        v = rng.integers(-(2 ** 12), 2 ** 12, size=32).astype(np.float32)
+        assert np.array_equal(oracle.fwht32(oracle.fwht32(v)), 32 * v)
+
+
+def fp64_rotation(V, signs):
+    """(V o s) blockdiag(H) / sqrt(32) in fp64 with scipy's Hadamard matrix."""
+    V = np.atleast_2d(np.asarray(V, dtype=np.float64))
+    R_, K = V.shape
+    s = oracle.signs_to_pm1(signs, K)
+    H = scipy.linalg.hadamard(32).astype(np.float64)
+    return ((V * s).reshape(R_, K // 32, 32) @ H / np.sqrt(32.0)).reshape(R_, K)
+
+
+def test_rotation_matches_fp64_definition():
+    K = 512
+    signs = oracle.make_signs(11, K)
+    X = synth.activations(8, K, seed=3, outlier_channels=2).numpy()
+    got = oracle.rotate(X, signs).astype(np.float64)
+    ref = fp64_rotation(X, signs)
+    l1 = np.abs(X.astype(np.float64)).reshape(8, K // 32, 32).sum(-1)
+    bound = (6 * EPS32 * l1 + 1e-30)[:, :, None] * np.ones((1, 1, 32))
+    assert np.all(np.abs(got - ref).reshape(8, K // 32, 32) <= bound)
+
+
+def test_rotation_inverse_roundtrip():
+    K = 1024
+    signs = oracle.make_signs(12, K)
+    W = synth.weights(16, K, seed=4).numpy()
+    back = oracle.rotate_inverse(oracle.rotate(W, signs), signs).astype(np.float64)
+    l1 = np.abs(W.astype(np.float64)).reshape(16, K // 32, 32).sum(-1)[:, :, None]
+    err = np.abs(back - W).reshape(16, K // 32, 32)
+    assert np.all(err <= 14 * EPS32 * l1)
+    # the inverse undoes the signs too: without them it would not round-trip
+    assert np.max(err) < 1e-6
+
+
+def test_rotation_preserves_product():
+    K = 2048
+    signs = oracle.make_signs(13, K)
+    X = synth.activations(16, K, seed=5, outlier_channels=2).numpy()
+    W = synth.weights(64, K, seed=6).numpy()
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    rot = oracle.rotate(X, signs).astype(np.float64) @ oracle.rotate(W, signs).astype(np.float64).T
+    assert np.linalg.norm(rot - ref) / np.linalg.norm(ref) <= 1e-5
+
+
+def test_outlier_spreading_golden(golden_dir):
+    cases = [l.split() for l in open(os.path.join(golden_dir, "outlier_spread.txt")) if l.startswith("case")]
+    assert len(cases) == 3
+    for _, K, j, t, sbit, mag_hex, pattern in cases:
+        K, j, t, sbit, mag = int(K), int(j), float(t), int(sbit), int(mag_hex, 16)
+        signs = np.zeros(K // 32, dtype=np.uint32)
+        if sbit:
+            signs[j // 32] |= np.uint32(1 << (j % 32))
+        v = np.zeros(K, dtype=np.float32)
+        v[j] = t
+        u = oracle.rotate(v, signs)[0]
+        b = j // 32
+        block = u[b * 32:(b + 1) * 32]
+        for i in range(32):
+            assert f32_bits(abs(block[i])) == mag
+            assert (block[i] > 0) == (pattern[i] == "+")
+        rest = np.concatenate([u[: b * 32], u[(b + 1) * 32:]])
+        assert np.all(rest == 0.0)
+        # the outlier's magnitude is spread: every entry is |t| / sqrt(32)
+        assert np.allclose(np.abs(block), abs(t) / np.sqrt(32.0), rtol=1e-7)
+
+
+# ----------------------------------------------------------- quantizers ---
+def parse_quant_golden(golden_dir):
+    out = []
+    for line in open(os.path.join(golden_dir, "quant_groups.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        kind, rest = line.split(None, 1)
+        parts = [p.split() for p in rest.split("|")]
+        out.append((kind, parts))
+    return out
+
+
+def test_quantizers_golden(golden_dir):
+    cases = parse_quant_golden(golden_dir)
+    kinds = {k for k, _ in cases}
+    assert kinds == {"asym4", "sym8", "act"}
+    for kind, parts in cases:
+        w = np.array([float(v) for v in parts[0]], dtype=np.float32)
+        if kind == "asym4":
+            q, s, z = oracle.quant_group_asym4(w)
+            assert f32_bits(s) == f32_bits(np.float32(parts[1][0])), (w, s)
+            assert z == int(parts[1][1]), (w, z)
+            assert q.tolist() == [int(v) for v in parts[2]], (w, q)
+        elif kind == "sym8":
+            q, s = oracle.quant_group_sym8(w)
+            assert f32_bits(s) == f32_bits(np.float32(parts[1][0])), (w, s)
+            assert q.tolist() == [int(v) for v in parts[2]], (w, q)
+        else:
+            q, s = oracle.quant_row_act(w)
+            assert f32_bits(s) == f32_bits(np.float32(parts[1][0])), (w, s)
+            assert q.tolist() == [int(v) for v in parts[2]], (w, q)
+
+
+def test_act_quant_error_bound_and_extremes():
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        K = 32 * int(rng.integers(1, 20))
+        u = (rng.standard_normal(K) * 10.0 ** rng.uniform(-6, 3)).astype(np.float32)
+        if trial % 5 == 0:
+            u[rng.integers(K)] *= 50
+        q, s = oracle.quant_row_act(u)
+        assert s > 0 and np.all(np.abs(q.astype(int)) <= 127)
+        err = np.abs(u.astype(np.float64) - q.astype(np.float64) * np.float64(s))
+        assert np.all(err <= np.float64(s) * (0.5 + 2.0 ** -16))
+        amax = int(np.argmax(np.abs(u)))
+        assert abs(int(q[amax])) == 127 and np.sign(q[amax]) == np.sign(u[amax])
+        assert np.float64(s) == pytest.approx(np.max(np.abs(u)) / 127.0, rel=1e-7)
+
+
+def test_w4_group_error_bound():
+    rng = np.random.default_rng(8)
+    for trial in range(200):
+        n = int(rng.choice([16, 32, 64, 128, 256]))
+        w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        if trial % 3 == 0:
+            w[rng.integers(n)] *= 20
+        if trial % 7 == 0:
+            w = np.abs(w)
+        if trial % 11 == 0:
+            w = -np.abs(w)
+        q, s, z = oracle.quant_group_asym4(w)
+        assert 0 <= z <= 15 and np.all(q <= 15)
+        deq = np.float64(s) * (q.astype(np.float64) - z)
+        assert np.all(np.abs(w - deq) <= np.float64(s) * (0.5 + 2.0 ** -16))
+        # zero is represented exactly by the code z
+        q0, _, _ = oracle.quant_group_asym4(np.concatenate([w, [0.0]]).astype(np.float32))
+        assert q0[-1] == oracle.quant_group_asym4(np.concatenate([w, [0.0]]).astype(np.float32))[2]
+
+
+def test_w8_group_error_bound():
+    rng = np.random.default_rng(9)
+    for trial in range(200):
+        n = int(rng.choice([32, 64, 128]))
+        w = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        if trial % 3 == 0:
+            w[rng.integers(n)] *= 20
+        q, s = oracle.quant_group_sym8(w)
+        assert np.all(np.abs(q.astype(int)) <= 127)
+        err = np.abs(w.astype(np.float64) - np.float64(s) * q.astype(np.float64))
+        assert np.all(err <= np.float64(s) * (0.5 + 2.0 ** -16))
+        amax = int(np.argmax(np.abs(w)))
+        assert abs(int(q[amax])) == 127
+
+
+def test_quant_act_composes_rotation_row_quant_and_group_sums():
+    K, G, M = 256, 64, 5
+    signs = oracle.make_signs(21, K)
+    X = synth.activations(M, K, seed=8, outlier_channels=2).numpy()
+    X[3] = 0.0
+    qx, sx, gsum = oracle.quant_act(X, G, signs)
+    U = oracle.rotate(X, signs)
+    for m in range(M):
+        q, s = oracle.quant_row_act(U[m])
+        assert np.array_equal(q, qx[m]) and f32_bits(s) == f32_bits(sx[m])
+    assert np.array_equal(gsum, qx.astype(np.int64).reshape(M, K // G, G).sum(-1))
+    assert sx[3] == 0.0 and not qx[3].any() and not gsum[3].any()
+
+
+def test_quant_weights_compose_rotation_and_group_quant():
+    K, G, N = 256, 32, 6
+    signs = oracle.make_signs(22, K)
+    W = synth.weights(N, K, seed=9).numpy()
+    W[2, 64:96] = 0.0
+    codes, scales, zeros = oracle.quant_w4(W, G, signs)
+    c8, s8 = oracle.quant_w8(W, G, signs)
+    U = oracle.rotate(W, signs)
+    for n in range(N):
+        for g in range(K // G):
+            q, s, z = oracle.quant_group_asym4(U[n, g * G:(g + 1) * G])
+            assert np.array_equal(q, codes[n, g * G:(g + 1) * G]) and s == scales[n, g] and z == zeros[n, g]
+            q8, s_8 = oracle.quant_group_sym8(U[n, g * G:(g + 1) * G])
+            assert np.array_equal(q8, c8[n, g * G:(g + 1) * G]) and s_8 == s8[n, g]
+    # rotating a zero block gives zeros: that group quantizes to scale 0
+    assert scales[2, 2] == 0.0 and zeros[2, 2] == 0 and not codes[2, 64:96].any()
+
+
+# ------------------------------------------------------- integer GEMM ---
+def brute_partials(qx, codes, zeros, G):
+    M, K = qx.shape
+    N = codes.shape[0]
+    a = qx.astype(np.int64).reshape(M, K // G, G)
+    w = codes.astype(np.int64).reshape(N, K // G, G)
+    if zeros is not None:
+        w = w - zeros.astype(np.int64)[:, :, None]
+    return np.einsum("mgk,ngk->mng", a, w)
+
+
+@pytest.mark.parametrize("fmt,G,K,N,M", [("w4", 32, 32, 3, 2), ("w4", 16, 64, 8, 4), ("w4", 64, 128, 5, 3),
+                                         ("w8", 32, 64, 8, 4), ("w8", 128, 256, 4, 1), ("w4", 128, 256, 7, 3)])
+def test_partials_brute_force(fmt, G, K, N, M):
+    rng = np.random.default_rng(K + N + M)
+    qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    if fmt == "w4":
+        codes = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+        zeros = rng.integers(0, 16, size=(N, K // G)).astype(np.uint8)
+    else:
+        codes = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+        zeros = None
+    P = oracle.partials(qx, codes, zeros, G)
+    assert np.array_equal(P.astype(np.int64), brute_partials(qx, codes, zeros, G))
+
+
+def test_partials_zero_point_identity():
+    K, G, N, M = 256, 64, 6, 3
+    signs = oracle.make_signs(31, K)
+    r = oracle.verify_linear(synth.activations(M, K, seed=10).numpy(), synth.weights(N, K, seed=11).numpy(), G,
+                             "w4", signs)
+    raw = np.einsum("mgk,ngk->mng", r["qx"].astype(np.int64).reshape(M, K // G, G),
+                    r["codes"].astype(np.int64).reshape(N, K // G, G))
+    corr = r["zeros"].astype(np.int64)[None, :, :] * r["gsum"].astype(np.int64)[:, None, :]
+    assert np.array_equal(r["P"].astype(np.int64), raw - corr)
+
+
+def test_partials_int32_headroom_extremes():
+    for fmt, G in (("w4", 256), ("w8", 256), ("w4", 128), ("w8", 128)):
+        K, N, M = 2 * G, 2, 2
+        qx = np.full((M, K), 127, dtype=np.int8)
+        qx[1] = -127
+        if fmt == "w4":
+            codes = np.full((N, K), 15, dtype=np.uint8)
+            zeros = np.zeros((N, K // G), dtype=np.uint8)
+            codes[1] = 0
+            zeros[1] = 15
+            top = 127 * 15 * G
+        else:
+            codes = np.full((N, K), 127, dtype=np.int8)
+            codes[1] = -127
+            zeros = None
+            top = 127 * 127 * G
+        P = oracle.partials(qx, codes, zeros, G)
+        assert P[0, 0, 0] == top and P[1, 0, 0] == -top and P[0, 1, 0] == -top and P[1, 1, 0] == top
+
+
+def test_epilogue_matches_fp64_within_rounding():
+    rng = np.random.default_rng(14)
+    M, N, NG = 4, 9, 64
+    P = rng.integers(-(2 ** 20), 2 ** 20, size=(M, N, NG)).astype(np.int32)
+    sx = (rng.random(M) * 0.1).astype(np.float32)
+    scales = (rng.random((N, NG)) * 0.01).astype(np.float32)
+    Y = oracle.output(P, sx, scales).astype(np.float64)
+    terms = scales.astype(np.float64)[None] * P.astype(np.float64)
+    exact = sx.astype(np.float64)[:, None] * terms.sum(-1)
+    bound = (NG + 2) * EPS32 * sx.astype(np.float64)[:, None] * np.abs(terms).sum(-1)
+    assert np.all(np.abs(Y - exact) <= bound)
+    # the order is g ascending: recompute sequentially in fp32 and match bit for bit
+    for m in range(M):
+        for n in range(N):
+            acc = np.float32(0.0)
+            for g in range(NG):
+                acc = np.float32(acc + np.float32(scales[n, g] * np.float32(P[m, n, g])))
+            assert np.float32(sx[m] * acc) == np.float32(Y[m, n])
+
+
+def layer_error_bound(X, W, G, fmt, signs, r):
+    """|Y - x' w'^T| bound from the quantization steps and the fp32 epilogue (fp64)."""
+    Xr = oracle.rotate(X, signs).astype(np.float64)
+    Wr = oracle.rotate(W, signs).astype(np.float64)
+    M, K = Xr.shape
+    N = Wr.shape[0]
+    ex = r["sx"].astype(np.float64) * (0.5 + 2.0 ** -16)                  # [M]
+    ew = np.repeat(r["scales"].astype(np.float64), G, axis=1) * (0.5 + 2.0 ** -16)  # [N][K]
+    bound = np.abs(Xr) @ ew.T + ex[:, None] * np.abs(Wr).sum(1)[None, :] + ex[:, None] * ew.sum(1)[None, :]
+    terms = np.abs(r["scales"].astype(np.float64)[None] * r["P"].astype(np.float64)).sum(-1)
+    bound += (K // G + 2) * EPS32 * r["sx"].astype(np.float64)[:, None] * terms
+    return Xr @ Wr.T, bound
+
+
+@pytest.mark.parametrize("fmt,G", [("w4", 32), ("w4", 64), ("w4", 16), ("w8", 128), ("w8", 32)])
+def test_layer_output_within_quantization_error_bound(fmt, G):
+    K, N, M = 512, 48, 5
+    signs = oracle.make_signs(40 + G, K)
+    X = synth.activations(M, K, seed=12, outlier_channels=2).numpy()
+    W = synth.weights(N, K, seed=13).numpy()
+    r = oracle.verify_linear(X, W, G, fmt, signs)
+    exact, bound = layer_error_bound(X, W, G, fmt, signs, r)
+    err = r["Y"].astype(np.float64) - exact
+    assert np.all(np.abs(err) <= bound)
+    # The bound above is worst case (all rounding errors aligned).  Rounding to
+    # nearest makes each error roughly uniform on +-step/2, so the output error
+    # variance is about sum_k (x'_k^2 sw_k^2 + w'_k^2 sx^2) / 12: a wrong sign,
+    # a dropped zero point or a misplaced scale shows up as far more than that.
+    Xr = oracle.rotate(X, signs).astype(np.float64)
+    Wr = oracle.rotate(W, signs).astype(np.float64)
+    sw2 = np.repeat(r["scales"].astype(np.float64), G, axis=1) ** 2
+    var = (Xr ** 2) @ sw2.T / 12 + (r["sx"].astype(np.float64) ** 2)[:, None] * (Wr ** 2).sum(1)[None, :] / 12
+    assert np.mean(err ** 2) <= 4.0 * np.mean(var)
+    assert np.mean(err ** 2) >= 0.05 * np.mean(var)
+
+
+def test_layer_plausible_against_unquantized_product():
+    K, N, M = 1024, 64, 16
+    signs = oracle.make_signs(50, K)
+    X = synth.activations(M, K, seed=14, outlier_channels=2).numpy()
+    W = synth.weights(N, K, seed=15).numpy()
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    for fmt, G, tol in (("w4", 64, 0.15), ("w8", 128, 0.02)):
+        Y = oracle.verify_linear(X, W, G, fmt, signs)["Y"].astype(np.float64)
+        assert np.linalg.norm(Y - ref) / np.linalg.norm(ref) < tol
+
+
+def test_rotation_lowers_4bit_error_on_outlier_weights():
+    K, N, G = 256, 256, 32
+    W = synth.weights(N, K, seed=0, outlier_frac=0.005).numpy()
+    signs = oracle.make_signs(0, K)
+    no_rot = np.zeros(K // 32, dtype=np.uint32)
+
+    def mse(rotated: bool):
+        s = signs if rotated else no_rot
+        Wr = oracle.rotate(W, s) if rotated else W
+        codes, scales, zeros = oracle.quant_w4(W, G, s) if rotated else _quant_w4_unrotated(W, G)
+        deq = np.repeat(scales, G, 1) * (codes.astype(np.float32) - np.repeat(zeros, G, 1).astype(np.float32))
+        return float(np.mean((deq - Wr) ** 2))
+
+    assert mse(True) < 0.8 * mse(False)
+
+
+def _quant_w4_unrotated(W, G):
+    N, K = W.shape
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty((N, K // G), np.float32)
+    zeros = np.empty((N, K // G), np.uint8)
+    for n in range(N):
+        for g in range(K // G):
+            codes[n, g * G:(g + 1) * G], scales[n, g], zeros[n, g] = oracle.quant_group_asym4(W[n, g * G:(g + 1) * G])
+    return codes, scales, zeros
+
+
+def test_fused_gemm_equals_partials_then_output():
+    K, N, M, G = 256, 40, 7, 64
+    signs = oracle.make_signs(60, K)
+    for fmt in ("w4", "w8"):
+        r = oracle.verify_linear(synth.activations(M, K, seed=16).numpy(), synth.weights(N, K, seed=17).numpy(), G,
+                                 fmt, signs)
+        Y2 = oracle.verify_gemm(r["qx"], r["sx"], r["codes"], r["scales"], r["zeros"], G)
+        assert np.array_equal(Y2.view(np.uint32), r["Y"].view(np.uint32))
+
+
+def test_openmp_build_matches_single_thread():
+    K, N, M, G = 256, 64, 4, 32
+    signs = oracle.make_signs(61, K)
+    X = synth.activations(M, K, seed=18).numpy()
+    W = synth.weights(N, K, seed=19).numpy()
+    a = oracle.quant_w4(W, G, signs)
+    b = oracle.quant_w4(W, G, signs, openmp=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    qx, sx, _ = oracle.quant_act(X, G, signs)
+    y1 = oracle.verify_gemm(qx, sx, a[0], a[1], a[2], G)
+    y2 = oracle.verify_gemm(qx, sx, a[0], a[1], a[2], G, openmp=True)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    assert oracle.num_threads(False) == 1 and oracle.num_threads(True) >= 1

@@ -1,0 +1,60 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle/hq_oracle.c (on the CPU),
+builds the copy, and runs tests/test_oracle.py against it in a subprocess:
+at least one pin has to fail.  A mistake that changes only the rounding order
+(not the exact arithmetic) is not a mistake the pins are meant to see and is
+not listed.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "hq_oracle.c")
+
+MUTANTS = {
+    "butterfly_difference_sign": ("float d = a - b;", "float d = b - a;"),
+    "hadamard_scale_off_by_one_ulp": ("0x3E3504F3u", "0x3E3504F4u"),
+    "signs_ignored": ("return ((signs[k / 32] >> (k % 32)) & 1u) ? -1.0f : 1.0f;", "return 1.0f;"),
+    "missing_overall_scale": ("out[b * OR_BLOCK + j] = u[j] * c;", "out[b * OR_BLOCK + j] = u[j];"),
+    "round_half_away": ("float r = rintf(x);", "float r = roundf(x);"),
+    "zero_point_sign_in_gemm": ("- (int64_t)zeros[(size_t)n * NG + g];", "+ (int64_t)zeros[(size_t)n * NG + g];"),
+    "range_not_widened_to_zero": ("float lo = 0.0f, hi = 0.0f, scale, z;", "float lo = w[0], hi = w[0], scale, z;"),
+    "zero_point_from_wrong_sign": ("z = or_round_clamp(-lo / scale, 0.0f, 15.0f);",
+                                   "z = or_round_clamp(lo / scale, 0.0f, 15.0f);"),
+    "asym_divisor_16": ("scale = (hi - lo) / 15.0f;", "scale = (hi - lo) / 16.0f;"),
+    "sym_divisor_128": ("scale = a / 127.0f;", "scale = a / 128.0f;"),
+    "act_absmax_signed": ("float t = fabsf(u[k]);", "float t = u[k];"),
+    "group_sum_drops_last": ("for (k = g * G; k < (g + 1) * G; ++k) t += q[k];",
+                             "for (k = g * G; k < (g + 1) * G - 1; ++k) t += q[k];"),
+    "activation_transposed": ("int64_t a = qx[(size_t)m * K + k];", "int64_t a = qx[(size_t)k * M + m];"),
+    "epilogue_drops_terms": ("acc = acc + t;", "acc = t;"),
+    "epilogue_wrong_group_scale": ("float t = scales[(size_t)n * NG + g] * p;",
+                                   "float t = scales[(size_t)n * NG + (g + 1) % NG] * p;"),
+    "epilogue_drops_row_scale": ("Y[(size_t)m * N + n] = sx[m] * acc;", "Y[(size_t)m * N + n] = acc;"),
+    "splitmix_gamma": ("0x9E3779B97F4A7C15ULL", "0x9E3779B97F4A7C16ULL"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "m.c")
+        so = os.path.join(d, "m.so")
+        open(c, "w").write(mutated)
+        subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", c, "-o", so, "-lm"],
+                       check=True)
+        env = dict(os.environ, HQ_ORACLE_TEST_LIB=so)
+        r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"), "-x",
+                            "-q", "-p", "no:cacheprovider", "-k", "not openmp"],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 1, f"{name}: pins did not fail (rc={r.returncode})\n{r.stdout[-2000:]}"
+        assert "failed" in r.stdout
