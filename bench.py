@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Throughput of the verify-pass quantized linear layers on GB300.
+
+One step = one verify pass of a 9B-class decoder over M = 16 draft-tree
+tokens: for each of 32 layers the q, k, v, o, fused gate+up and down
+projections, then the LM head -- every linear runs the activation rotation +
+int8 quantization kernel and the W4A8 GEMM kernel of libhq.so (4-bit
+asymmetric weights, group 64).  The pass streams 3.875 GB of packed weights,
+far more than the 129 MB L2, so every pass reads its weights from HBM.
+
+Reported (one JSON line on rank 0):
+  value        weight GB/s of the whole pass (packed weight bytes / time)
+  e2e          the same through host buffers: per step the activations are
+               copied host->device and the logits device->host
+  roofline     the GEMM kernel's weight bytes / its own time, vs measured HBM
+  cpu_baseline the CPU oracle on a bounded sample (a 4096x4096 layer)
+With torchrun (N > 1) every rank runs its own pass (independent verify
+batches, weak scaling, no collective on the data path).
+`--impl reference` times the CPU oracle instead (the slow reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A8 verify-GEMM weight GB/s (% of HBM peak) and passes/s at M=16 rows"
+WORKLOAD = "decoder_9b_verify_pass"
+TAUS = (1.0, 8.39, 16.0)  # tokens per pass: plain decoding, the pages' measured 8.39, the 16-token tree budget
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    p.add_argument("--fuse-qkv", action="store_true", help="pack q, k, v of a layer as one [6144][4096] weight")
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- ranks ---
+class Ranks:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            import torch
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.dist:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.dist:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(device_index), "-lms", str(period_ms)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.proc or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        win = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        if not win:  # a very short timed region: take the samples nearest to it
+            win = [s for _, s in self.samples][-3:]
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in win:
+            f = [x.strip() for x in s.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- CPU side ---
+def cpu_oracle_sample(target_s: float = 10.0):
+    """Time the oracle (OpenMP build, as it stands) on one 4096x4096 W4 G64 layer at M = 16:
+    activation rotation + quantization and the integer GEMM with its epilogue."""
+    import oracle
+    from quantized_speculative_verify_gb300 import synth
+    K = N = 4096
+    G, M, seed = 64, 16, 7
+    W = synth.weights(N, K, seed=seed).numpy()
+    X = synth.activations(M, K, seed=seed + 1, outlier_channels=2).numpy()
+    signs = oracle.make_signs(seed, K)
+    codes, scales, zeros = oracle.quant_w4(W, G, signs, openmp=True)
+    wbytes = N * K * (0.5 + 4.5 / G)
+
+    def one():
+        qx, sx, _ = oracle.quant_act(X, G, signs)
+        oracle.verify_gemm(qx, sx, codes, scales, zeros, G, openmp=True)
+
+    t = time.perf_counter()
+    one()
+    first = time.perf_counter() - t
+    reps = max(1, int(target_s / max(first, 1e-3)))
+    t = time.perf_counter()
+    for _ in range(reps):
+        one()
+    dt = time.perf_counter() - t
+    return dict(value=wbytes * reps / dt / 1e9, unit="GB/s", cores=oracle.num_threads(True), kind="oracle",
+                sample=f"one 4096x4096 W4 G64 layer (q-projection shape of the pass), M=16, act-quant + GEMM, "
+                       f"{reps} repetitions in {dt:.1f} s"), dt / reps, wbytes
+
+
+def run_reference(args, ranks: Ranks):
+    """The reference arm: the CPU oracle, one bounded sample per step."""
+    if ranks.rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    from quantized_speculative_verify_gb300 import synth
+    K = N = 4096
+    G, M, seed = 64, 16, 7
+    W = synth.weights(N, K, seed=seed).numpy()
+    X = synth.activations(M, K, seed=seed + 1, outlier_channels=2).numpy()
+    signs = oracle.make_signs(seed, K)
+    codes, scales, zeros = oracle.quant_w4(W, G, signs, openmp=True)
+    wbytes = N * K * (0.5 + 4.5 / G)
+
+    def step():
+        qx, sx, _ = oracle.quant_act(X, G, signs)
+        oracle.verify_gemm(qx, sx, codes, scales, zeros, G, openmp=True)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    value = wbytes * args.steps / dt / 1e9
+    sample = "one 4096x4096 W4 G64 layer (q-projection shape of the pass) per step, M=16, act-quant + GEMM"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": 16, "format": "w4_asym", "group": 64,
+                                            "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(True), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# -------------------------------------------------------------- GPU side ---
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("k_gemm.cuh", "hq_internal.cuh", "hq_api.cu"):
+        with open(os.path.join(ROOT, "quantized_speculative_verify_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic_record():
+    """ncu DRAM bytes of the GEMM for this workload, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "k_verify_gemm_decoder_9b_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d
+
+
+class VerifyPass:
+    """All packed weights, inputs and outputs of one decoder verify pass, resident on the device.
+
+    Each activation input (a layer's attention input, read by q, k and v; the
+    o input; the MLP input, read by the fused gate+up; the down input; the LM
+    head input) has its own sign vector, X, and quantized buffers; the
+    layers that read an input are packed with that input's signs."""
+
+    def __init__(self, torch, hq, synth, device, fuse_qkv: bool, pdl: bool):
+        cfg = synth.DECODER_9B
+        self.torch, self.hq = torch, hq
+        self.M, self.G, self.fmt = cfg["M"], cfg["G"], cfg["fmt"]
+        self.flags = hq.HQ_LAUNCH_PDL if pdl else hq.HQ_LAUNCH_DEFAULT
+        self.linears = synth.decoder_linears(cfg, fuse_qkv=fuse_qkv)
+        self.layers, self.ys, self.inputs, self.plan = [], [], [], []
+        seed = cfg["seed"]
+        ws_need = 0
+        s_host = None
+        for li, (name, K, N) in enumerate(self.linears):
+            if not name.endswith((".k", ".v")):  # a new activation input
+                s_host = hq.hq_make_signs(synth.layer_seed(seed, 500 + li), K)
+                X = synth.activations(self.M, K, seed=synth.layer_seed(seed, 2000 + li), device=device, **cfg["x"])
+                qx, sx, gsum = hq.act_buffers(self.M, K, self.G, device)
+                self.inputs.append([name, K, X, qx, sx, gsum, None])
+            W = synth.weights(N, K, seed=synth.layer_seed(seed, li), device=device, **cfg["w"])
+            layer = hq.pack_layer(W, self.G, self.fmt, s_host)
+            del W
+            if self.inputs[-1][6] is None:
+                self.inputs[-1][6] = layer.signs
+            self.layers.append(layer)
+            self.ys.append(torch.empty((self.M, N), dtype=torch.float32, device=device))
+            self.plan.append((len(self.inputs) - 1, li))
+            ws_need = max(ws_need, hq.hq_workspace_bytes(layer.desc, self.M))
+        self.ws = torch.zeros(ws_need, dtype=torch.uint8, device=device)
+        self.weight_bytes = sum(int(l.blob.numel()) for l in self.layers)
+        self.algo_weight_bytes = sum(K * N * (0.5 + 4.5 / self.G) for _, K, N in self.linears)
+        self.n_act = len(self.inputs)
+        self.n_gemm = len(self.layers)
+
+    def launch(self, act=True, gemm=True):
+        hq = self.hq
+        done = set()
+        for ii, li in self.plan:
+            name, K, X, qx, sx, gsum, signs = self.inputs[ii]
+            if act and ii not in done:
+                hq.hq_rotate_quant_act(X, self.M, K, self.G, signs, qx, sx, gsum, self.flags)
+                done.add(ii)
+            if gemm:
+                layer = self.layers[li]
+                hq.hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, self.M, self.ys[li], None, self.ws,
+                                  self.flags)
+
+    def h2d_bytes(self):
+        return sum(inp[2].numel() * 4 for inp in self.inputs)
+
+
+def run_gpu(args, ranks: Ranks):
+    import torch
+    from quantized_speculative_verify_gb300 import hq, synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(ranks.local)
+    device = torch.device("cuda", ranks.local)
+    hq.load()
+    peak, peak_kind = measured_peaks()
+
+    vp = VerifyPass(torch, hq, synth, device, fuse_qkv=args.fuse_qkv, pdl=not args.no_pdl)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=device)
+    torch.cuda.set_stream(stream)
+    # correctness of the run itself: one eager pass, no device-side time-out
+    vp.launch()
+    if hq.hq_workspace_status(vp.ws) != hq.HQ_OK:
+        raise SystemExit("device-side wait timed out")
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        vp.launch()
+    gemm_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gemm_graph, stream=stream):
+        vp.launch(act=False)
+
+    # ---- the timed region: K whole passes
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks = ClockSampler(ranks.local)
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks.mark_start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    clocks.mark_end()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = ranks.max(ms)
+    if hq.hq_workspace_status(vp.ws) != hq.HQ_OK:
+        raise SystemExit("device-side wait timed out during the timed region")
+    total_bytes = ranks.sum(vp.algo_weight_bytes * args.steps)
+    value = total_bytes / (ms_max / 1e3) / 1e9
+    passes_per_s = args.steps * ranks.world / (ms_max / 1e3)
+
+    # ---- the dominant kernel alone: the same GEMM launches without the activation kernels
+    for _ in range(3):
+        gemm_graph.replay()
+    reps = max(10, args.steps // 2)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(reps):
+        gemm_graph.replay()
+    g1.record(stream)
+    g1.synchronize()
+    gemm_ms_per_pass = g0.elapsed_time(g1) / reps
+    gemm_achieved = vp.algo_weight_bytes / (gemm_ms_per_pass / 1e3) / 1e9
+    traffic = gemm_traffic_record()
+    roofline = {"bound": "hbm", "achieved": gemm_achieved, "peak": peak, "unit": "GB/s",
+                "frac": gemm_achieved / peak, "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
+                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                "kernel": "k_verify_gemm", "launches_per_pass": vp.n_gemm,
+                "avg_launch_us": gemm_ms_per_pass * 1e3 / vp.n_gemm,
+                "algorithmic_bytes_per_launch": vp.algo_weight_bytes / vp.n_gemm}
+
+    # ---- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        hosts = [torch.empty_like(inp[2], device="cpu").pin_memory() for inp in vp.inputs]
+        for h, inp in zip(hosts, vp.inputs):
+            h.copy_(inp[2].cpu())
+        logits_dev = vp.ys[-1]
+        logits_host = torch.empty_like(logits_dev, device="cpu").pin_memory()
+        e_steps = max(3, args.steps // 4)
+
+        def e2e_step():
+            for h, inp in zip(hosts, vp.inputs):
+                inp[2].copy_(h, non_blocking=True)
+            graph.replay()
+            logits_host.copy_(logits_dev, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ranks.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms = ranks.max(e0.elapsed_time(e1))
+        e2e = {"value": ranks.sum(vp.algo_weight_bytes * e_steps) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_host.numel() * 4,
+               "ms_per_step": e_ms / e_steps, "steps": e_steps}
+
+    cpu = None
+    if not args.no_cpu_baseline and ranks.rank == 0:
+        cpu, _, _ = cpu_oracle_sample()
+
+    if ranks.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ranks.world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": vp.M, "format": "w4_asym", "group": vp.G, "layers": 32,
+                       "linears_per_pass": vp.n_gemm, "activation_inputs_per_pass": vp.n_act,
+                       "qkv_fused": bool(args.fuse_qkv), "pdl": not args.no_pdl,
+                       "weight_bytes_per_pass": vp.weight_bytes,
+                       "l2": "inputs larger than L2: 3.875 GB of packed weights streamed per pass, L2 129 MB",
+                       "parallelism": f"replicas x{ranks.world} (independent verify batches)"},
+            "passes_per_s": passes_per_s,
+            "pct_of_hbm_peak": 100.0 * value / (peak * ranks.world),
+            "tokens_per_s_ceiling": {f"tau={t:g}": passes_per_s * t for t in TAUS},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks.summary(),
+            "gpu_launches": args.steps * (vp.n_act + vp.n_gemm),
+        }
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    ranks = Ranks()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ranks)
+        return run_gpu(args, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * hq.h -- C ABI of the quantized speculative-verify linear layer for GB300
+ * (sm_103a).
+ *
+ * The layer is the target model's linear layer in the verification pass of
+ * speculative decoding: M drafted tree tokens (M = 1..128 rows) go through
+ *   1. a block-diagonal randomized Hadamard rotation (blocks of 32, seeded
+ *      +-1 sign flips, one overall scale 1/sqrt(32)) and per-row int8
+ *      quantization of the activations, computed on the fly;
+ *   2. an integer GEMM against weights that were rotated with the same
+ *      transform and quantized offline, either to 4-bit asymmetric grouped
+ *      integers ("Medium") or to 8-bit symmetric grouped integers ("Large");
+ *   3. a per-group fp32 dequantization epilogue.
+ * Source: page "Karpathy's Trick for Faster Local LLMs Finally Has Proper
+ * Tooling" (blog.dailydoseofds.com): section "How Uzu optimizes bytes and
+ * tokens per pass" (the two weight formats, 8-bit activations on the fly,
+ * int8 matrix path, 32-block randomized Hadamard transform, transform block
+ * independent of the quantization group) and section "Producing several
+ * tokens from one model pass" (the verify batch is the 16-32 token draft
+ * tree, "16 rows of work instead of 1").
+ *
+ * Conventions
+ *   - Row-major everywhere.  X is [M][K], W is [N][K], Y = X W^T is [M][N].
+ *   - Pointers are DEVICE pointers unless their name ends in _host.  The
+ *     caller owns and allocates every buffer; the library allocates no
+ *     memory and keeps no per-call state.
+ *   - Every call that takes a `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) only enqueues work and returns without synchronizing.
+ *   - Arguments are validated before anything is launched.  A call that
+ *     returns an error launched nothing, except HQ_ERR_CUDA, which reports
+ *     that the launch itself failed.  Faults of kernels that did launch show
+ *     up, as always with CUDA, at the caller's next synchronization.
+ *   - Calls are reentrant.  Two calls that share a workspace must not run
+ *     concurrently (use one workspace per stream).
+ */
+#ifndef HQ_H
+#define HQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HQ_OK = 0,
+    HQ_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer   */
+    HQ_ERR_UNSUPPORTED = 2, /* valid request this build does not implement  */
+    HQ_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+    HQ_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up            */
+} hq_status;
+
+typedef enum {
+    HQ_W4_ASYM = 0, /* "Medium": uint4 codes, fp32 scale + uint4 zero point per group */
+    HQ_W8_SYM = 1   /* "Large":  int8 codes, fp32 scale per group                     */
+} hq_format;
+
+/* One linear layer.  K = input features (multiple of 32 and of `group`),
+ * N = output features (>= 1), group = quantization group along K, one of
+ * 16, 32, 64, 128, 256 (independent of the 32-element transform block),
+ * format = hq_format. */
+typedef struct {
+    int32_t K;
+    int32_t N;
+    int32_t group;
+    int32_t format;
+} hq_layer_desc;
+
+/* Launch flags. */
+#define HQ_LAUNCH_DEFAULT 0u
+/* Launch with programmatic dependent launch: the kernel may start while the
+ * previous kernel of the stream is still running and waits for it (and for
+ * its memory) before reading anything that kernel could have produced.
+ * hq_verify_gemm additionally starts streaming the packed weights before
+ * that wait, so with this flag the blob must not be written by the
+ * operation launched immediately before it in the same stream. */
+#define HQ_LAUNCH_PDL 1u
+
+/* Maximum number of token rows per call. */
+#define HQ_MAX_M 128
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *hq_status_string(int status);
+
+/* ABI version of this library: (major << 16) | minor. */
+int32_t hq_version(void);
+
+/* Size in bytes of the packed weight blob of `desc` (0 if desc is invalid).
+ * The blob layout is private to the library; hq_unpack_codes gives the
+ * canonical view. */
+size_t hq_packed_bytes(const hq_layer_desc *desc);
+
+/* Size in bytes of the workspace hq_verify_gemm needs for `desc` and M rows
+ * (0 if the arguments are invalid).  The workspace holds the device error
+ * word, the split-K arrival counters and the split-K partial sums.  It must
+ * be zero-filled once after allocation; every call leaves it zero-filled
+ * again (except for the error word after a timeout, see
+ * hq_workspace_status). */
+size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M);
+
+/* Sign vector of the randomized Hadamard transform ("random sign flips
+ * applied before the mixing", section "How Uzu optimizes bytes and tokens
+ * per pass").  Host-only.  Feature k is negated when the top bit of the k-th
+ * output of SplitMix64 (Steele, Lea & Flood 2014) seeded with `seed` is set;
+ * the result is bit-packed: bit (k % 32) of signs_host[k / 32].
+ * K must be a positive multiple of 32; signs_host has K/32 words.  The same
+ * vector must be used for the weights and for the activations of a layer. */
+int hq_make_signs(uint64_t seed, int32_t K, uint32_t *signs_host);
+
+/* Offline: rotate, quantize and pack the weights of one layer (section "How
+ * Uzu optimizes bytes and tokens per pass": Medium = 4-bit asymmetric,
+ * Large = 8-bit symmetric, transform before quantization).
+ *   W      fp32 [N][K], 16-byte aligned
+ *   signs  uint32 [K/32] (device copy of hq_make_signs' output)
+ *   blob   hq_packed_bytes(desc) bytes, 16-byte aligned, written in full
+ * Per (output channel n, group g): Medium: lo = min(0, min w), hi = max(0,
+ * max w), scale = (hi - lo) / 15, zero = rint(-lo / scale), code =
+ * clamp(rint(w / scale) + zero, 0, 15); Large: scale = max|w| / 127, code =
+ * clamp(rint(w / scale), -127, 127); an all-zero group has scale 0 and
+ * codes 0.  rint rounds half to even; divisions are IEEE. */
+int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *signs, void *blob,
+                    void *stream);
+
+/* Verify pass, step 1: rotate and quantize the activations of M rows
+ * (section "How Uzu optimizes bytes and tokens per pass": activations
+ * quantized to 8 bits on the fly, after the same randomized Hadamard
+ * transform as the weights).
+ *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op)
+ *   signs uint32 [K/32]
+ *   qx    int8 [M][K] (8-byte aligned):  clamp(rint(x' / sx), -127, 127)
+ *   sx    fp32 [M]:  max_k |x'[m][k]| / 127  (0 for an all-zero row)
+ *   gsum  int32 [M][K/group]: sum of qx over each group (the zero-point
+ *         correction term of the Medium format; may be NULL for Large)
+ * x' is the rotated row: per 32-block, sign flip, unnormalized Walsh-
+ * Hadamard butterfly at strides 1, 2, 4, 8, 16 in fp32 without fused
+ * multiply-add, then multiplication by fp32(1/sqrt(32)).  flags:
+ * HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL. */
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+                        float *sx, int32_t *gsum, uint32_t flags, void *stream);
+
+/* Verify pass, step 2: integer GEMM of the quantized activations against the
+ * packed weights with the per-group dequantization epilogue (section "How
+ * Uzu optimizes bytes and tokens per pass": both matmul operands integers,
+ * int8 matrix path).
+ *   blob      packed by hq_pack_weights for the same desc (16-byte aligned)
+ *   qx, sx, gsum  from hq_rotate_quant_act with the same K, group, signs
+ *             (gsum may be NULL for the Large format)
+ *   M         0..HQ_MAX_M (0: no-op)
+ *   Y         fp32 [M][N]:
+ *               Y[m][n] = sx[m] * sum_g ( scale[n][g] * P[m][n][g] )
+ *             with P[m][n][g] = sum_{k in g} qx[m][k] * (code[n][k] - zero[n][g])
+ *             (zero = 0 for Large), the sum over g in fp32.
+ *   partials  check mode: NULL, or int32 [M][N][K/group] that receives P
+ *             exactly (slower; for verification)
+ *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
+ *             before its first use
+ * The fp32 sum over groups is taken in ascending group order; an output
+ * whose K range is split across thread blocks sums the blocks' partial sums
+ * in ascending K order, so results are deterministic.  flags:
+ * HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL (see above). */
+int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
+                   const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
+                   void *stream);
+
+/* Canonical view of a blob (for verification and for saving in a portable
+ * form): codes uint8 [N][K] (Medium: 0..15; Large: the int8 code's byte),
+ * scales fp32 [N][K/group], zeros uint8 [N][K/group] (Medium only; may be
+ * NULL for Large). */
+int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
+                    void *stream);
+
+/* Synchronizes `stream`, then reads and clears the error word of a
+ * workspace.  Returns HQ_ERR_TIMEOUT if a bounded wait inside
+ * hq_verify_gemm gave up since the word was last cleared (the outputs of
+ * that call are then incomplete), HQ_OK otherwise. */
+int hq_workspace_status(void *workspace, void *stream);
+
+/* Self-test of the bounded-wait path: launches one block that waits on a
+ * shared-memory barrier nothing will ever complete, giving up after
+ * `limit_ns` nanoseconds (1000..100000000) and setting the error word of
+ * `workspace` (>= 16 bytes, zero-filled).  hq_workspace_status then
+ * returns HQ_ERR_TIMEOUT.  No fault and no hang: the kernel returns. */
+int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HQ_H */

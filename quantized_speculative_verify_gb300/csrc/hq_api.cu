@@ -1,0 +1,213 @@
+// hq_api.cu -- the C ABI declared in include/hq.h: argument validation (done
+// before anything is launched), blob/workspace geometry and kernel dispatch.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "hq_internal.cuh"
+#include "k_gemm.cuh"
+
+namespace hq {
+
+int device_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+namespace {
+
+__global__ void k_wait_selftest(int *err, long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    // Nothing arrives on this barrier: the bounded wait must give up.
+    mbar_wait_bounded(b, 0u, err, (unsigned long long)limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s) {
+    k_wait_selftest<<<1, 1, 0, s>>>(static_cast<int *>(workspace), limit_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const int8_t *qx, const float *sx,
+                               const int32_t *gsum, int M, float *Y, int32_t *partials, void *workspace, bool pdl,
+                               cudaStream_t s) {
+    GemmArgs a;
+    a.blob = static_cast<const uint8_t *>(blob);
+    a.qx = qx;
+    a.sx = sx;
+    a.gsum = gsum;
+    a.Y = Y;
+    a.partials = partials;
+    a.ws = static_cast<uint8_t *>(workspace);
+    a.ws_partial_off = ws_partial_offset(g);
+    a.M = M;
+    a.N = g.N;
+    a.K = g.K;
+    a.NGK = g.NGK;
+    a.KTILES = g.KTILES;
+    a.T = g.NB * g.KTILES;
+    int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    int grid = sms;
+    if (grid > a.T) grid = a.T;
+    if (grid > MAX_CTAS) grid = MAX_CTAS;
+    a.grid = grid;
+    // Stage ring of about 96 KB: two blocks of consecutive launches fit on an
+    // SM together, so the next layer's weights stream while this one ends.
+    int stages = (96 * 1024) / g.tile_bytes;
+    if (stages < 2) stages = 2;
+    if (stages > 16) stages = 16;
+    a.stages = stages;
+    a.tile_bytes = g.tile_bytes;
+    a.code_bytes = g.code_bytes;
+    a.scale_bytes = g.scale_bytes;
+    return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, g.G, pdl, s) : launch_gemm_w8(a, g.G, pdl, s);
+}
+
+}  // namespace hq
+
+using hq::Geom;
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool desc_ok(const hq_layer_desc *d) { return d && hq::desc_valid(d->K, d->N, d->group, d->format); }
+
+Geom geom_of(const hq_layer_desc *d) { return hq::make_geom(d->K, d->N, d->group, d->format); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA; }
+
+// SplitMix64 (Steele, Lea & Flood 2014): state += golden gamma, then the
+// two xor-shift-multiply finalizer rounds.
+uint64_t splitmix64_next(uint64_t &state) {
+    state += 0x9E3779B97F4A7C15ull;
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hq_status_string(int status) {
+    switch (status) {
+        case HQ_OK: return "HQ_OK";
+        case HQ_ERR_INVALID_ARG: return "HQ_ERR_INVALID_ARG";
+        case HQ_ERR_UNSUPPORTED: return "HQ_ERR_UNSUPPORTED";
+        case HQ_ERR_CUDA: return "HQ_ERR_CUDA";
+        case HQ_ERR_TIMEOUT: return "HQ_ERR_TIMEOUT";
+        default: return "HQ_ERR_UNKNOWN";
+    }
+}
+
+int32_t hq_version(void) { return (1 << 16) | 0; }
+
+size_t hq_packed_bytes(const hq_layer_desc *desc) {
+    if (!desc_ok(desc)) return 0;
+    return hq::blob_bytes(geom_of(desc));
+}
+
+size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M) {
+    if (!desc_ok(desc) || M < 0 || M > HQ_MAX_M) return 0;
+    return hq::ws_bytes(geom_of(desc), M);
+}
+
+int hq_make_signs(uint64_t seed, int32_t K, uint32_t *signs_host) {
+    if (!signs_host || K <= 0 || K % 32 != 0) return HQ_ERR_INVALID_ARG;
+    uint64_t st = seed;
+    for (int32_t w = 0; w < K / 32; ++w) {
+        uint32_t bits = 0;
+        for (int j = 0; j < 32; ++j)
+            if (splitmix64_next(st) >> 63) bits |= 1u << j;
+        signs_host[w] = bits;
+    }
+    return HQ_OK;
+}
+
+int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *signs, void *blob, void *stream) {
+    if (!desc_ok(desc) || !W || !signs || !blob) return HQ_ERR_INVALID_ARG;
+    if (!aligned(W, 4) || !aligned(signs, 4) || !aligned(blob, 16)) return HQ_ERR_INVALID_ARG;
+    const Geom g = geom_of(desc);
+    return cuda_status(hq::launch_pack(g, W, signs, blob, static_cast<cudaStream_t>(stream)));
+}
+
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+                        float *sx, int32_t *gsum, uint32_t flags, void *stream) {
+    if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
+    if (K <= 0 || K % 32 != 0) return HQ_ERR_INVALID_ARG;
+    if (!(group == 16 || group == 32 || group == 64 || group == 128 || group == 256) || K % group != 0)
+        return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (M == 0) return HQ_OK;
+    if (!X || !signs || !qx || !sx) return HQ_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(qx, 8) || !aligned(sx, 4) || !aligned(signs, 4) || (gsum && !aligned(gsum, 4)))
+        return HQ_ERR_INVALID_ARG;
+    if (K > 65536) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, group, signs, qx, sx, gsum, (flags & HQ_LAUNCH_PDL) != 0,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
+                   const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
+                   void *stream) {
+    if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
+    if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (M == 0) return HQ_OK;
+    if (!blob || !qx || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
+    if (desc->format == HQ_W4_ASYM && !gsum) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(qx, 8) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
+        (gsum && !aligned(gsum, 4)) || (partials && !aligned(partials, 4)))
+        return HQ_ERR_INVALID_ARG;
+    const Geom g = geom_of(desc);
+    return cuda_status(hq::launch_verify_gemm(g, blob, qx, sx, gsum, M, Y, partials, workspace,
+                                              (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
+                    void *stream) {
+    if (!desc_ok(desc) || !blob || !codes || !scales) return HQ_ERR_INVALID_ARG;
+    if (desc->format == HQ_W4_ASYM && !zeros) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(scales, 4)) return HQ_ERR_INVALID_ARG;
+    const Geom g = geom_of(desc);
+    return cuda_status(hq::launch_unpack(g, blob, codes, scales, desc->format == HQ_W4_ASYM ? zeros : nullptr,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int hq_workspace_status(void *workspace, void *stream) {
+    if (!workspace || !aligned(workspace, 16)) return HQ_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return HQ_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return HQ_ERR_CUDA;
+    if (v == 0) return HQ_OK;
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return HQ_ERR_CUDA;
+    return HQ_ERR_TIMEOUT;
+}
+
+int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream) {
+    if (!workspace || !aligned(workspace, 16)) return HQ_ERR_INVALID_ARG;
+    if (limit_ns < 1000 || limit_ns > 100000000) return HQ_ERR_INVALID_ARG;
+    return cuda_status(hq::launch_wait_selftest(workspace, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

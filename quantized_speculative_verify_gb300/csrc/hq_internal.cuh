@@ -1,0 +1,209 @@
+// hq_internal.cuh -- blob geometry and device helpers shared by the kernels
+// of the quantized speculative-verify linear layer (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/hq.h"
+
+namespace hq {
+
+// ---------------------------------------------------------------------------
+// Packed weight blob.
+//
+// The weights of a layer are cut into tiles of BN = 128 output channels by
+// KT input features (KT = max(128, group)).  Tiles are stored n-block major,
+// K minor, so the tiles one thread block streams are one contiguous byte
+// range and one bulk copy fetches a whole tile.  Inside a tile:
+//
+//   codes   [chunk][ntile 0..7][lane 0..31][16 bytes]
+//           ntile = 16 consecutive channels; a lane's 16 bytes are exactly
+//           the A operand it feeds to mma.m16n8k32 (two k32 steps for the
+//           4-bit format, one for the 8-bit format) -- see pack kernel.
+//   scales  [group in tile][ntile][16 floats, rows ordered 0,8,1,9,...,7,15]
+//   zeros   [group in tile][ntile][8 bytes, byte r = z[r] | z[r+8] << 4]
+//           (4-bit format only)
+//
+// Every region and every tile is a multiple of 16 bytes, and the byte count
+// of a tile equals its algorithmic size: BN*KT*(bits/8) for the codes plus
+// 4 bytes (and half a byte for the zero point) per (channel, group).
+// N and K are padded up to whole tiles with zero codes and zero scales.
+// ---------------------------------------------------------------------------
+constexpr int BN = 128;           // output channels per tile (8 mma row tiles)
+constexpr int NTILES = BN / 16;   // mma row tiles per tile
+constexpr int MAX_CTAS = 512;     // upper bound on GEMM thread blocks (workspace sizing)
+constexpr int MAX_M = HQ_MAX_M;
+
+struct Geom {
+    int K, N, G, fmt;
+    int KT;          // features per tile
+    int Kp;          // K rounded up to KT
+    int NB;          // n-blocks (tiles along N)
+    int KTILES;      // tiles along K
+    int GPT;         // groups per tile
+    int NGK;         // real groups along K (K / G)
+    int code_bytes;  // per tile
+    int scale_bytes; // per tile
+    int zero_bytes;  // per tile
+    int tile_bytes;
+    int chunk_k;     // features covered by one 16-byte lane chunk: 64 (4-bit) or 32 (8-bit)
+};
+
+__host__ __device__ inline bool desc_valid(int K, int N, int G, int fmt) {
+    if (K <= 0 || N <= 0) return false;
+    if (K % 32 != 0) return false;
+    if (!(G == 16 || G == 32 || G == 64 || G == 128 || G == 256)) return false;
+    if (K % G != 0) return false;
+    if (fmt != HQ_W4_ASYM && fmt != HQ_W8_SYM) return false;
+    return true;
+}
+
+__host__ __device__ inline Geom make_geom(int K, int N, int G, int fmt) {
+    Geom g;
+    g.K = K;
+    g.N = N;
+    g.G = G;
+    g.fmt = fmt;
+    g.KT = G > 128 ? G : 128;
+    g.Kp = (K + g.KT - 1) / g.KT * g.KT;
+    g.NB = (N + BN - 1) / BN;
+    g.KTILES = g.Kp / g.KT;
+    g.GPT = g.KT / G;
+    g.NGK = K / G;
+    g.code_bytes = fmt == HQ_W4_ASYM ? BN * g.KT / 2 : BN * g.KT;
+    g.scale_bytes = g.GPT * BN * 4;
+    g.zero_bytes = fmt == HQ_W4_ASYM ? g.GPT * BN / 2 : 0;
+    g.tile_bytes = g.code_bytes + g.scale_bytes + g.zero_bytes;
+    g.chunk_k = fmt == HQ_W4_ASYM ? 64 : 32;
+    return g;
+}
+
+__host__ __device__ inline size_t blob_bytes(const Geom &g) {
+    return (size_t)g.NB * (size_t)g.KTILES * (size_t)g.tile_bytes;
+}
+
+// Workspace: [0, 16) error word; [16, 16 + ctr) arrival counters (one per
+// n-block); then partial-sum slots, two per thread block, BN x M floats each.
+__host__ __device__ inline size_t ws_counter_offset() { return 16; }
+__host__ __device__ inline size_t ws_counter_bytes(const Geom &g) { return ((size_t)g.NB * 4 + 15) / 16 * 16; }
+__host__ __device__ inline size_t ws_partial_offset(const Geom &g) { return ws_counter_offset() + ws_counter_bytes(g); }
+__host__ __device__ inline size_t ws_slot_floats(int M) { return (size_t)BN * (size_t)M; }
+__host__ __device__ inline size_t ws_bytes(const Geom &g, int M) {
+    return ws_partial_offset(g) + (size_t)MAX_CTAS * 2 * ws_slot_floats(M) * 4;
+}
+
+// Device error codes written to the workspace error word.
+constexpr int DEV_ERR_TIMEOUT = 1;
+// Bounded waits give up after this long (normal waits last microseconds).
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+// fp32 nearest to 1/sqrt(32): the overall scale of the Hadamard transform.
+constexpr uint32_t HADAMARD_SCALE_BITS = 0x3E3504F3u;
+
+// ---------------------------------------------------------------------------
+// Device helpers (inline PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with parity `parity` of barrier `bar` to complete, for
+// at most `limit_ns`.  On time-out, records DEV_ERR_TIMEOUT in *err (if not
+// NULL) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int *err,
+                                                  unsigned long long limit_ns = WAIT_LIMIT_NS) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    uint32_t it = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++it & 255u) == 0u && global_timer_ns() - t0 > limit_ns) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// One-dimensional bulk copy global -> shared, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// D = A(16x32, int8) * B(32x8, int8) + D, int32 accumulate.
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace hq
+
+// Launchers (defined in the kernel translation units).
+namespace hq {
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
+                                    int32_t *gsum, bool pdl, cudaStream_t s);
+cudaError_t launch_pack(const Geom &g, const float *W, const uint32_t *signs, void *blob, cudaStream_t s);
+cudaError_t launch_unpack(const Geom &g, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
+                          cudaStream_t s);
+cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const int8_t *qx, const float *sx,
+                               const int32_t *gsum, int M, float *Y, int32_t *partials, void *workspace, bool pdl,
+                               cudaStream_t s);
+cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s);
+int device_sm_count();
+}  // namespace hq

@@ -1,0 +1,176 @@
+// k_act.cu -- rotate + quantize the activations of the verify batch.
+//
+// Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling",
+// section "How Uzu optimizes bytes and tokens per pass": activations are
+// quantized to 8 bits on the fly, after the block-diagonal randomized
+// Hadamard transform (32-element blocks, random sign flips before the
+// mixing, one overall scale) that the weights went through offline.
+//
+// One thread block per row.  Thread i holds float4s i, i + T, i + 2T, ...
+// of the row, so 8 consecutive lanes hold one 32-element block: butterfly
+// strides 1 and 2 are inside a lane's float4, strides 4, 8 and 16 are lane
+// exchanges (xor 1, 2, 4).  Every add, subtract and multiply is a separate
+// IEEE-rounded fp32 operation in the order 1, 2, 4, 8, 16, so the rotated
+// values are bit-identical to a scalar implementation of the same order.
+#include <cuda_runtime.h>
+
+#include "hq_internal.cuh"
+
+namespace hq {
+namespace {
+
+__device__ __forceinline__ float flip(float x, uint32_t bit) {
+    return __int_as_float(__float_as_int(x) ^ (int)(bit << 31));
+}
+
+// Stage h in {4, 8, 16}: lane partner = lane ^ (h / 4).  The lane holding the
+// lower index keeps a + b, the other keeps a - b (a = lower, b = upper).
+__device__ __forceinline__ float bfly_x(float v, int lane_bit, bool upper) {
+    float p = __shfl_xor_sync(0xffffffffu, v, lane_bit);
+    return upper ? __fsub_rn(p, v) : __fadd_rn(v, p);
+}
+
+template <int V, int T>
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G,
+                                                        const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
+                                                        float *__restrict__ sx, int32_t *__restrict__ gsum) {
+    __shared__ float s_red[T / 32];
+    extern __shared__ __align__(16) int8_t s_q[];  // the row's codes, for the group sums
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int n4 = K >> 2;  // float4s per row
+    const float c = __int_as_float((int)HADAMARD_SCALE_BITS);
+    const float4 *xr = reinterpret_cast<const float4 *>(X + (size_t)row * K);
+    const int NG = K / G;
+
+    float4 v[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = tid + j * T;
+        v[j] = idx < n4 ? __ldg(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = tid + j * T;
+        // signs of features 4*idx .. 4*idx+3
+        uint32_t sw = 0;
+        if (idx < n4) sw = __ldg(signs + (idx >> 3)) >> ((idx & 7) * 4);
+        float a0 = flip(v[j].x, sw & 1u), a1 = flip(v[j].y, (sw >> 1) & 1u);
+        float a2 = flip(v[j].z, (sw >> 2) & 1u), a3 = flip(v[j].w, (sw >> 3) & 1u);
+        // stride 1
+        float t0 = __fadd_rn(a0, a1), t1 = __fsub_rn(a0, a1);
+        float t2 = __fadd_rn(a2, a3), t3 = __fsub_rn(a2, a3);
+        // stride 2
+        a0 = __fadd_rn(t0, t2);
+        a2 = __fsub_rn(t0, t2);
+        a1 = __fadd_rn(t1, t3);
+        a3 = __fsub_rn(t1, t3);
+        // strides 4, 8, 16 across lanes
+#pragma unroll
+        for (int lb = 1; lb <= 4; lb <<= 1) {
+            const bool up = (lane & lb) != 0;
+            a0 = bfly_x(a0, lb, up);
+            a1 = bfly_x(a1, lb, up);
+            a2 = bfly_x(a2, lb, up);
+            a3 = bfly_x(a3, lb, up);
+        }
+        a0 = __fmul_rn(a0, c);
+        a1 = __fmul_rn(a1, c);
+        a2 = __fmul_rn(a2, c);
+        a3 = __fmul_rn(a3, c);
+        v[j] = make_float4(a0, a1, a2, a3);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
+    }
+
+    // row absmax: warp, then block
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_red[tid >> 5] = amax;
+    __syncthreads();
+    if (tid < 32) {
+        float a = tid < T / 32 ? s_red[tid] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (tid == 0) s_red[0] = a;
+    }
+    __syncthreads();
+    const float a = s_red[0];
+    const float s = a == 0.0f ? 0.0f : __fdiv_rn(a, 127.0f);
+    if (tid == 0) sx[row] = s;
+
+    char4 *qr = reinterpret_cast<char4 *>(qx + (size_t)row * K);
+    char4 *sq = reinterpret_cast<char4 *>(s_q);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int idx = tid + j * T;
+        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+        if (s != 0.0f) {
+            q0 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].x, s))));
+            q1 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].y, s))));
+            q2 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].z, s))));
+            q3 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].w, s))));
+        }
+        if (idx < n4) {
+            const char4 q4 = make_char4((signed char)q0, (signed char)q1, (signed char)q2, (signed char)q3);
+            qr[idx] = q4;
+            if (gsum) sq[idx] = q4;
+        }
+    }
+    if (gsum) {
+        // one thread per group: sum its G codes (exact integer arithmetic)
+        __syncthreads();
+        for (int gi = tid; gi < NG; gi += T) {
+            const char4 *p = sq + (size_t)gi * (G / 4);
+            int t = 0;
+            for (int w = 0; w < G / 4; ++w) {
+                const char4 c4 = p[w];
+                t += (int)c4.x + (int)c4.y + (int)c4.z + (int)c4.w;
+            }
+            gsum[(size_t)row * NG + gi] = t;
+        }
+    }
+}
+
+template <int V, int T>
+cudaError_t launch_act_t(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
+                         int32_t *gsum, bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M);
+    cfg.blockDim = dim3(T);
+    cfg.dynamicSmemBytes = gsum ? (size_t)K : 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (cfg.dynamicSmemBytes > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_rotate_quant_act<V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, signs, qx, sx, gsum);
+}
+
+}  // namespace
+
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
+                                    int32_t *gsum, bool pdl, cudaStream_t s) {
+    const int n4 = K / 4;
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 256 * 2) return launch_act_t<2, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 256 * 4) return launch_act_t<4, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 512 * 4) return launch_act_t<4, 512>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hq

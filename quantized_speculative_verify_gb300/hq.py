@@ -1,0 +1,242 @@
+"""Python binding of libhq.so (include/hq.h): argument marshalling only.
+
+Every step of the verify-pass linear layer runs in the library's CUDA kernels.
+This module converts torch tensors to raw device pointers, passes the current
+CUDA stream, and turns status codes into exceptions.  There is no fallback: if
+libhq.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+HQ_OK = 0
+HQ_ERR_INVALID_ARG = 1
+HQ_ERR_UNSUPPORTED = 2
+HQ_ERR_CUDA = 3
+HQ_ERR_TIMEOUT = 4
+HQ_W4_ASYM = 0
+HQ_W8_SYM = 1
+HQ_LAUNCH_DEFAULT = 0
+HQ_LAUNCH_PDL = 1
+HQ_MAX_M = 128
+
+FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
+
+# Every symbol include/hq.h declares.
+EXPORTS = ("hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_make_signs",
+           "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
+           "hq_selftest_wait_timeout")
+
+
+class HQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class hq_layer_desc(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_int32), ("N", ctypes.c_int32), ("group", ctypes.c_int32), ("format", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libhq.so (building it first if the sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise HQError(HQ_ERR_CUDA, f"libhq.so not found at {_build.LIB}")
+    lib = ctypes.CDLL(_build.LIB)
+    P, I32, U32, U64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t
+    D = ctypes.POINTER(hq_layer_desc)
+    sig = {
+        "hq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "hq_version": (I32, []),
+        "hq_packed_bytes": (SZ, [D]),
+        "hq_workspace_bytes": (SZ, [D, I32]),
+        "hq_make_signs": (ctypes.c_int, [U64, I32, P]),
+        "hq_pack_weights": (ctypes.c_int, [D, P, P, P, P]),
+        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, I32, P, P, P, P, U32, P]),
+        "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, P, I32, P, P, P, U32, P]),
+        "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
+        "hq_workspace_status": (ctypes.c_int, [P, P]),
+        "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().hq_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != HQ_OK:
+        raise HQError(rc, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr()
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    raise TypeError(f"cannot pass {type(t)} as a pointer")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def make_desc(K: int, N: int, group: int, fmt) -> hq_layer_desc:
+    return hq_layer_desc(int(K), int(N), int(group), FORMATS.get(fmt, fmt) if isinstance(fmt, str) else int(fmt))
+
+
+# ------------------------------------------------------------ C-ABI calls ---
+def hq_version() -> int:
+    return int(load().hq_version())
+
+
+def hq_packed_bytes(desc: hq_layer_desc) -> int:
+    return int(load().hq_packed_bytes(ctypes.byref(desc)))
+
+
+def hq_workspace_bytes(desc: hq_layer_desc, M: int) -> int:
+    return int(load().hq_workspace_bytes(ctypes.byref(desc), int(M)))
+
+
+def hq_make_signs(seed: int, K: int) -> np.ndarray:
+    out = np.zeros(max(K // 32, 1), dtype=np.uint32)
+    _check(load().hq_make_signs(ctypes.c_uint64(seed & (2 ** 64 - 1)), int(K), out.ctypes.data), "hq_make_signs")
+    return out[: K // 32]
+
+
+def hq_pack_weights(desc, W, signs, blob, stream=None) -> None:
+    _check(load().hq_pack_weights(ctypes.byref(desc), _ptr(W), _ptr(signs), _ptr(blob), _stream(stream)),
+           "hq_pack_weights")
+
+
+def hq_rotate_quant_act(X, M: int, K: int, group: int, signs, qx, sx, gsum, flags: int = 0, stream=None) -> None:
+    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), int(group), _ptr(signs), _ptr(qx), _ptr(sx),
+                                      _ptr(gsum), int(flags), _stream(stream)), "hq_rotate_quant_act")
+
+
+def hq_verify_gemm(desc, blob, qx, sx, gsum, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
+    _check(load().hq_verify_gemm(ctypes.byref(desc), _ptr(blob), _ptr(qx), _ptr(sx), _ptr(gsum), int(M), _ptr(Y),
+                                 _ptr(partials), _ptr(workspace), int(flags), _stream(stream)), "hq_verify_gemm")
+
+
+def hq_unpack_codes(desc, blob, codes, scales, zeros, stream=None) -> None:
+    _check(load().hq_unpack_codes(ctypes.byref(desc), _ptr(blob), _ptr(codes), _ptr(scales), _ptr(zeros),
+                                  _stream(stream)), "hq_unpack_codes")
+
+
+def hq_workspace_status(workspace, stream=None) -> int:
+    return int(load().hq_workspace_status(_ptr(workspace), _stream(stream)))
+
+
+def hq_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
+    _check(load().hq_selftest_wait_timeout(_ptr(workspace), int(limit_ns), _stream(stream)),
+           "hq_selftest_wait_timeout")
+
+
+# ------------------------------------------------------- tensor helpers ---
+@dataclass
+class PackedLayer:
+    """A packed layer on the device: its descriptor, blob and device signs."""
+    desc: hq_layer_desc
+    blob: torch.Tensor
+    signs: torch.Tensor
+
+    @property
+    def K(self) -> int:
+        return self.desc.K
+
+    @property
+    def N(self) -> int:
+        return self.desc.N
+
+    @property
+    def group(self) -> int:
+        return self.desc.group
+
+    @property
+    def fmt(self) -> int:
+        return self.desc.format
+
+
+def pack_layer(W: torch.Tensor, group: int, fmt, signs_host: np.ndarray, stream=None) -> PackedLayer:
+    """Rotate + quantize + pack W [N][K] (fp32, on the device)."""
+    N, K = W.shape
+    desc = make_desc(K, N, group, fmt)
+    nbytes = hq_packed_bytes(desc)
+    if nbytes == 0:
+        raise HQError(HQ_ERR_INVALID_ARG, "hq_packed_bytes")
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    signs = torch.from_numpy(signs_host.astype(np.int32, copy=False).view(np.int32)).to(W.device)
+    hq_pack_weights(desc, W.contiguous(), signs, blob, stream)
+    return PackedLayer(desc, blob, signs)
+
+
+def act_buffers(M: int, K: int, group: int, device) -> tuple:
+    qx = torch.empty((M, K), dtype=torch.int8, device=device)
+    sx = torch.empty(M, dtype=torch.float32, device=device)
+    gsum = torch.empty((M, K // group), dtype=torch.int32, device=device)
+    return qx, sx, gsum
+
+
+def workspace(desc: hq_layer_desc, M: int, device) -> torch.Tensor:
+    n = hq_workspace_bytes(desc, M)
+    if n == 0:
+        raise HQError(HQ_ERR_INVALID_ARG, "hq_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def unpack(layer: PackedLayer, stream=None):
+    N, K, G = layer.N, layer.K, layer.group
+    dev = layer.blob.device
+    codes = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, K // G), dtype=torch.float32, device=dev)
+    zeros = torch.empty((N, K // G), dtype=torch.uint8, device=dev) if layer.fmt == HQ_W4_ASYM else None
+    hq_unpack_codes(layer.desc, layer.blob, codes, scales, zeros, stream)
+    return codes, scales, zeros
+
+
+def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torch.Tensor | None = None,
+                  bufs=None, flags: int = 0, partials: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = dequant(int GEMM(quant(rotate(X)), packed W)): the two kernels in sequence."""
+    M, K = X.shape
+    if bufs is None:
+        bufs = act_buffers(M, K, layer.group, X.device)
+    qx, sx, gsum = bufs
+    if Y is None:
+        Y = torch.empty((M, layer.N), dtype=torch.float32, device=X.device)
+    hq_rotate_quant_act(X, M, K, layer.group, layer.signs, qx, sx, gsum, flags, stream)
+    hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, M, Y, partials, ws, flags, stream)
+    return Y

@@ -1,0 +1,139 @@
+"""The C-ABI library on the host, without a GPU: it loads, exports every
+symbol include/hq.h declares, computes sizes, draws the same signs as the
+oracle, and rejects invalid arguments before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_speculative_verify_gb300 import hq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hq.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(hq.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = hq.load()
+    out = subprocess.run(["nm", "-D", "--defined-only", hq.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings_and_version():
+    assert hq.status_string(hq.HQ_OK) == "HQ_OK"
+    assert hq.status_string(hq.HQ_ERR_TIMEOUT) == "HQ_ERR_TIMEOUT"
+    assert hq.status_string(99) == "HQ_ERR_UNKNOWN"
+    assert hq.hq_version() >> 16 == 1
+
+
+@pytest.mark.parametrize("seed,K", [(0, 32), (1, 4096), (2, 12288), (1234567, 256), (2 ** 63 + 5, 8192)])
+def test_make_signs_matches_oracle(seed, K):
+    assert np.array_equal(hq.hq_make_signs(seed, K), oracle.make_signs(seed, K))
+
+
+def test_make_signs_rejects_bad_K():
+    lib = hq.load()
+    buf = np.zeros(4, dtype=np.uint32)
+    for K in (0, -32, 48):
+        assert lib.hq_make_signs(1, K, buf.ctypes.data) == hq.HQ_ERR_INVALID_ARG
+    assert lib.hq_make_signs(1, 64, None) == hq.HQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("K,N,G,fmt", [(256, 256, 32, "w4"), (4096, 4096, 64, "w4"), (4096, 24576, 128, "w8"),
+                                       (8192, 8192, 64, "w4"), (8192, 8192, 128, "w8"), (12288, 4096, 64, "w4"),
+                                       (4096, 151552, 64, "w4"), (4096, 1024, 256, "w4"), (4096, 1024, 16, "w8")])
+def test_packed_bytes_equal_algorithmic_bytes(K, N, G, fmt):
+    d = hq.make_desc(K, N, G, fmt)
+    per_weight = (0.5 + 4.5 / G) if fmt == "w4" else (1.0 + 4.0 / G)
+    assert hq.hq_packed_bytes(d) == int(round(N * K * per_weight))
+    assert hq.hq_packed_bytes(d) % 16 == 0
+
+
+def test_packed_bytes_pad_ragged_shapes():
+    # N and K are padded to whole 128 x 128 tiles
+    d = hq.make_desc(96, 200, 32, "w4")
+    assert hq.hq_packed_bytes(d) == 2 * 1 * (128 * 128 // 2 + 4 * 128 * 4 + 4 * 64)
+
+
+@pytest.mark.parametrize("K,N,G,fmt", [(0, 8, 32, 0), (48, 8, 16, 0), (64, 8, 48, 0), (96, 8, 64, 0), (64, 0, 32, 0),
+                                       (64, 8, 32, 2), (64, 8, 512, 1), (64, -1, 32, 1)])
+def test_invalid_desc_has_no_size(K, N, G, fmt):
+    d = hq.hq_layer_desc(K, N, G, fmt)
+    assert hq.hq_packed_bytes(d) == 0
+    assert hq.hq_workspace_bytes(d, 16) == 0
+
+
+def test_workspace_bytes():
+    d = hq.make_desc(4096, 4096, 64, "w4")
+    assert hq.hq_workspace_bytes(d, 16) > hq.hq_workspace_bytes(d, 1) > 0
+    assert hq.hq_workspace_bytes(d, 129) == 0 and hq.hq_workspace_bytes(d, -1) == 0
+    assert hq.hq_workspace_bytes(d, 16) % 16 == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-NULL value; never dereferenced: every call below fails validation
+
+
+def test_invalid_arguments_are_rejected_before_launch():
+    lib = hq.load()
+    d = hq.make_desc(256, 256, 32, "w4")
+    D = ctypes.byref(d)
+    bad = hq.hq_layer_desc(100, 256, 32, 0)
+    E = hq.HQ_ERR_INVALID_ARG
+    # pack
+    assert lib.hq_pack_weights(None, FAKE, FAKE, FAKE, None) == E
+    assert lib.hq_pack_weights(ctypes.byref(bad), FAKE, FAKE, FAKE, None) == E
+    assert lib.hq_pack_weights(D, None, FAKE, FAKE, None) == E
+    assert lib.hq_pack_weights(D, FAKE, FAKE, FAKE + 8, None) == E  # blob must be 16-byte aligned
+    # activations
+    assert lib.hq_rotate_quant_act(FAKE, 129, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, -1, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 100, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 96, 64, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 48, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(None, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 2, None) == E
+    # gemm
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 129, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, None, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, None, 4, FAKE, None, FAKE, 0, None) == E  # W4 needs gsum
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, None, 0, None) == E  # workspace
+    assert lib.hq_verify_gemm(D, FAKE + 8, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 8, None) == E
+    assert lib.hq_verify_gemm(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    # unpack / status / self-test
+    assert lib.hq_unpack_codes(D, FAKE, FAKE, FAKE, None, None) == E  # W4 needs zeros
+    assert lib.hq_workspace_status(None, None) == E
+    assert lib.hq_selftest_wait_timeout(FAKE, 10, None) == E
+    assert lib.hq_selftest_wait_timeout(None, 10 ** 6, None) == E
+
+
+def test_empty_batch_is_a_no_op():
+    lib = hq.load()
+    d = hq.make_desc(256, 256, 32, "w4")
+    # M = 0: nothing to do, nothing launched, pointers never touched
+    assert lib.hq_rotate_quant_act(None, 0, 256, 32, None, None, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK

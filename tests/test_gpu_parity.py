@@ -1,0 +1,317 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer stages (int8 activations, row scales, group sums, packed codes,
+scales, zero points, per-group int32 partial sums) must match bit for bit;
+fp32 outputs within |dY| <= 1e-6 + 1e-5 |Y_oracle|.  Inputs are seeded and
+synthetic (quantized_speculative_verify_gb300.synth); the oracle and the GPU
+receive the same arrays.  Large shapes compare a seeded sample of output
+channels: each channel depends only on its own weight row, so the oracle
+quantizes just the sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_speculative_verify_gb300 import hq, synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-6, 1e-5
+DEV = "cuda"
+# Fraction of outputs that must also meet |dY| <= ATOL + RTOL |Y| with the
+# relative part taken against |Y| itself (see assert_close).
+STRICT_FRACTION = 0.99
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hq.load()
+
+
+def sum_magnitude(ref):
+    """sx[m] * sum_g |scale[n][g] * P[m][n][g]|: the size of the fp32 sum that forms Y[m][n]."""
+    terms = np.abs(ref["scales"].astype(np.float64)[None] * ref["P"].astype(np.float64)).sum(-1)
+    return np.abs(ref["sx"].astype(np.float64))[:, None] * terms
+
+
+def assert_close(y, ref_out):
+    """fp32 outputs within 1e-6 absolute + 1e-5 relative of the oracle.
+
+    The fp32 sum over quantization groups is formed in ascending group order
+    by the oracle and by every thread block that owns a 128-channel block's
+    whole K range (those outputs are bit-identical, see
+    test_gemm_unsplit_blocks_are_bit_exact); where K is split between thread
+    blocks the partial sums are added in ascending K order, which rounds
+    differently.  Any two summation orders of the same fp32 terms differ by
+    a few ulp of the partial sums, so the relative part is taken against the
+    magnitude of the sum being formed, sx * sum_g |scale * P|; in addition at
+    least STRICT_FRACTION of the outputs must meet the tolerance relative to
+    |Y| itself."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref_out["Y"], dtype=np.float64)
+    err = np.abs(y - ref)
+    mag = np.maximum(np.abs(ref), sum_magnitude(ref_out))
+    lim = ATOL + RTOL * mag
+    bad = err > lim
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance; worst {np.max(err - lim):.3e}"
+    strict = err <= ATOL + RTOL * np.abs(ref)
+    assert strict.mean() >= STRICT_FRACTION, f"only {strict.mean():.5f} within the elementwise tolerance"
+
+
+def gpu_act(X, G, signs_dev):
+    M, K = X.shape
+    qx, sx, gsum = hq.act_buffers(M, K, G, DEV)
+    hq.hq_rotate_quant_act(X, M, K, G, signs_dev, qx, sx, gsum)
+    torch.cuda.synchronize()
+    return qx, sx, gsum
+
+
+def signs_pair(seed, K):
+    s = hq.hq_make_signs(seed, K)
+    return s, torch.from_numpy(s.view(np.int32)).to(DEV)
+
+
+# ------------------------------------------------------- activations ---
+ACT_CASES = [(1, 32, 32), (3, 64, 16), (16, 256, 32), (17, 256, 64), (16, 4096, 64), (32, 4096, 128),
+             (7, 4096, 256), (16, 12288, 64), (128, 4096, 16), (64, 8192, 128), (5, 96, 32), (2, 40960, 256)]
+
+
+@pytest.mark.parametrize("M,K,G", ACT_CASES)
+def test_rotate_quant_act_bit_exact(M, K, G):
+    X = synth.activations(M, K, seed=M * 7 + K, outlier_channels=min(2, K), heavy_frac=0.01)
+    s_host, s_dev = signs_pair(M + K, K)
+    qx, sx, gsum = gpu_act(X.to(DEV), G, s_dev)
+    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
+    assert np.array_equal(qx.cpu().numpy(), rq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(gsum.cpu().numpy(), rg)
+
+
+def test_rotate_quant_act_degenerate_rows():
+    M, K, G = 6, 256, 32
+    X = synth.activations(M, K, seed=3)
+    X[1] = 0.0                       # all-zero row -> scale 0, codes 0
+    X[2] = 0.0
+    X[2, 37] = -5.0                  # one outlier -> spread over its block
+    X[3] = 1e-30                     # tiny values (subnormal products)
+    X[4, :32] = 3.0                  # constant block
+    X[5] = 1e30                      # huge values
+    s_host, s_dev = signs_pair(9, K)
+    qx, sx, gsum = gpu_act(X.to(DEV), G, s_dev)
+    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
+    assert np.array_equal(qx.cpu().numpy(), rq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(gsum.cpu().numpy(), rg)
+    assert sx[1].item() == 0.0 and not qx[1].any()
+
+
+def test_rotate_quant_act_nan_does_not_crash():
+    M, K, G = 2, 64, 32
+    X = synth.activations(M, K, seed=4)
+    X[0, 3] = float("nan")
+    X[1, 9] = float("inf")
+    _, s_dev = signs_pair(1, K)
+    gpu_act(X.to(DEV), G, s_dev)  # values unspecified; it must return
+
+
+# ----------------------------------------------------------- packing ---
+PACK_CASES = [("w4", 256, 256, 32), ("w4", 4096, 4096, 64), ("w8", 4096, 1024, 128), ("w4", 32, 200, 32),
+              ("w4", 96, 130, 16), ("w8", 64, 1, 32), ("w4", 12288, 256, 64), ("w8", 512, 384, 256),
+              ("w4", 1024, 136, 128), ("w4", 512, 128, 256), ("w8", 256, 256, 16)]
+
+
+def gpu_pack(W, G, fmt, s_host):
+    layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
+    codes, scales, zeros = hq.unpack(layer)
+    torch.cuda.synchronize()
+    return layer, codes, scales, zeros
+
+
+@pytest.mark.parametrize("fmt,K,N,G", PACK_CASES)
+def test_pack_bit_exact(fmt, K, N, G):
+    W = synth.weights(N, K, seed=K + N, outlier_frac=0.005)
+    if N > 3:
+        W[2, :] = 0.0             # all-zero channel
+        W[3, : min(K, 64)] = 0.25  # constant stretch
+    s_host, _ = signs_pair(K * 3 + G, K)
+    _, codes, scales, zeros = gpu_pack(W, G, fmt, s_host)
+    if fmt == "w4":
+        rc, rs, rz = oracle.quant_w4(W.numpy(), G, s_host, openmp=True)
+        assert np.array_equal(zeros.cpu().numpy(), rz)
+    else:
+        rc, rs = oracle.quant_w8(W.numpy(), G, s_host, openmp=True)
+        rc = rc.view(np.uint8)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+# ---------------------------------------------------------------- GEMM ---
+def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
+    M, K = X.shape
+    if layer is None:
+        layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
+    ws = hq.workspace(layer.desc, M, DEV)
+    bufs = hq.act_buffers(M, K, G, DEV)
+    P = torch.empty((M, layer.N, K // G), dtype=torch.int32, device=DEV) if check else None
+    Y = hq.verify_linear(layer, X.to(DEV), ws, bufs=bufs, partials=P, flags=flags)
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    torch.cuda.synchronize()
+    # every call leaves the arrival counters at zero
+    nb = (layer.N + 127) // 128
+    assert not ws[16:16 + 4 * nb].any()
+    return dict(Y=Y.cpu().numpy(), P=None if P is None else P.cpu().numpy(), layer=layer, ws=ws)
+
+
+GEMM_CASES = [("w4", 1, 256, 256, 32), ("w4", 16, 256, 256, 32), ("w4", 3, 512, 200, 64), ("w8", 17, 384, 136, 128),
+              ("w4", 32, 1024, 1024, 16), ("w8", 8, 1024, 512, 32), ("w4", 64, 512, 256, 64), ("w8", 128, 256, 384, 128),
+              ("w4", 128, 256, 128, 256), ("w4", 16, 32, 136, 32), ("w8", 24, 96, 64, 32), ("w4", 5, 12288, 128, 64),
+              ("w8", 1, 4096, 256, 256), ("w4", 40, 2048, 1000, 128)]
+
+
+@pytest.mark.parametrize("fmt,M,K,N,G", GEMM_CASES)
+def test_gemm_partials_bit_exact_and_output_close(fmt, M, K, N, G):
+    X = synth.activations(M, K, seed=M + K, outlier_channels=2)
+    W = synth.weights(N, K, seed=N + K + 1, outlier_frac=0.005)
+    s_host, _ = signs_pair(M * N + K, K)
+    r = run_layer(X, W, G, fmt, s_host, check=True)
+    ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+    assert np.array_equal(r["P"], ref["P"])
+    assert_close(r["Y"], ref)
+
+
+def test_gemm_unsplit_blocks_are_bit_exact():
+    # K = 128: every 128-channel block is one tile, handled by one thread
+    # block from its first to its last group -> the same fp32 order as the oracle
+    M, K, N, G = 16, 128, 1024, 32
+    X = synth.activations(M, K, seed=1, outlier_channels=2)
+    W = synth.weights(N, K, seed=2)
+    s_host, _ = signs_pair(5, K)
+    for fmt in ("w4", "w8"):
+        r = run_layer(X, W, G, fmt, s_host)
+        ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+        assert np.array_equal(r["Y"].view(np.uint32), ref["Y"].view(np.uint32))
+
+
+def test_gemm_pdl_flag_and_repeat_are_identical():
+    M, K, N, G = 16, 4096, 1024, 64
+    X = synth.activations(M, K, seed=11, outlier_channels=2)
+    W = synth.weights(N, K, seed=12)
+    s_host, _ = signs_pair(13, K)
+    r0 = run_layer(X, W, G, "w4", s_host)
+    r1 = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
+    r2 = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
+    assert np.array_equal(r0["Y"].view(np.uint32), r1["Y"].view(np.uint32))
+    assert np.array_equal(r1["Y"].view(np.uint32), r2["Y"].view(np.uint32))
+
+
+def test_gemm_extreme_codes_int32_headroom():
+    # activations whose rotated rows are +-a (all codes +-127) and weights whose
+    # rotated groups are constant (all codes 15 with zero point 0 / all 127)
+    M, K, N = 4, 512, 128
+    s_host, _ = signs_pair(21, K)
+    Xr = np.stack([np.full(K, (m + 1) * (1.0 if m % 2 == 0 else -1.0)) for m in range(M)]).astype(np.float32)
+    X = torch.from_numpy(oracle.rotate_inverse(Xr, s_host))
+    Wr = np.ones((N, K), dtype=np.float32) * 0.5
+    Wr[1::2] *= -1.0
+    W = torch.from_numpy(oracle.rotate_inverse(Wr, s_host))
+    for fmt, G in (("w4", 256), ("w8", 256), ("w4", 64)):
+        r = run_layer(X, W, G, fmt, s_host, check=True)
+        ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+        assert np.array_equal(r["P"], ref["P"])
+        assert np.abs(ref["P"]).max() > 0.9 * 127 * (15 if fmt == "w4" else 127) * G
+        assert_close(r["Y"], ref)
+
+
+def test_gemm_zero_weights_and_zero_rows():
+    M, K, N, G = 8, 512, 256, 64
+    X = synth.activations(M, K, seed=31)
+    X[2] = 0.0
+    W = synth.weights(N, K, seed=32)
+    W[:, :128] = 0.0
+    W[7] = 0.0
+    s_host, _ = signs_pair(33, K)
+    for fmt in ("w4", "w8"):
+        r = run_layer(X, W, G, fmt, s_host, check=True)
+        ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+        assert np.array_equal(r["P"], ref["P"])
+        assert_close(r["Y"], ref)
+        assert not r["Y"][2].any() and not r["Y"][:, 7].any()
+
+
+def test_wait_timeout_selftest_reports_error_and_recovers():
+    ws = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    hq.hq_selftest_wait_timeout(ws, 1_000_000)
+    assert hq.hq_workspace_status(ws) == hq.HQ_ERR_TIMEOUT
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK  # the word was cleared
+    # the context is still usable
+    assert torch.ones(4, device=DEV).sum().item() == 4.0
+
+
+# ------------------------------------------------ full-size workloads ---
+def sampled_channels(N, count, seed):
+    g = np.random.default_rng(seed)
+    idx = set(g.choice(N, size=min(count, N), replace=False).tolist())
+    idx.update([0, N - 1, min(127, N - 1), min(128, N - 1), N // 2])
+    return np.array(sorted(idx))
+
+
+def check_full_layer(K, N, G, fmt, M, seed, wcfg, xcfg, count=384, layer=None, W=None):
+    """Full-size layer on the GPU; the oracle recomputes `count` sampled channels."""
+    s_host, _ = signs_pair(seed, K)
+    if W is None:
+        W = synth.weights(N, K, seed=seed, device=DEV, **wcfg)
+    X = synth.activations(M, K, seed=seed + 1, **xcfg)
+    if layer is None:
+        layer = hq.pack_layer(W, G, fmt, s_host)
+    ws = hq.workspace(layer.desc, M, DEV)
+    Y = hq.verify_linear(layer, X.to(DEV), ws, flags=hq.HQ_LAUNCH_PDL)
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    idx = sampled_channels(N, count, seed)
+    Ws = W[torch.from_numpy(idx).to(DEV)].cpu().numpy()
+    ref = oracle.verify_linear(X.numpy(), Ws, G, fmt, s_host)
+    assert_close(Y.cpu().numpy()[:, idx], ref)
+    return layer
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_workload_tiny_256(M):
+    c = synth.CONFIGS["tiny_256"]
+    check_full_layer(c["K"], c["N"], c["G"], c["fmt"], M, c["seed"], c["w"], c["x"], count=256)
+
+
+def test_workload_attn_4096():
+    c = synth.CONFIGS["attn_4096"]
+    check_full_layer(c["K"], c["N"], c["G"], c["fmt"], 16, c["seed"], c["w"], c["x"], count=4096)
+
+
+def test_workload_gateup_w8():
+    c = synth.CONFIGS["gateup_w8"]
+    W = synth.weights(c["N"], c["K"], seed=c["seed"], device=DEV, **c["w"])
+    layer = None
+    for M in c["Ms"]:
+        layer = check_full_layer(c["K"], c["N"], c["G"], c["fmt"], M, c["seed"], c["w"], c["x"], layer=layer, W=W)
+
+
+@pytest.mark.parametrize("name", ["sweep_8192_w8", "sweep_8192_w4"])
+def test_workload_sweep_8192(name):
+    c = synth.CONFIGS[name]
+    W = synth.weights(c["N"], c["K"], seed=c["seed"], device=DEV, **c["w"])
+    layer = None
+    for M in c["Ms"]:
+        layer = check_full_layer(c["K"], c["N"], c["G"], c["fmt"], M, c["seed"], c["w"], c["x"], count=192,
+                                 layer=layer, W=W)
+
+
+def test_workload_decoder_9b_each_shape():
+    cfg = synth.DECODER_9B
+    shapes = {}
+    for name, K, N in synth.decoder_linears(cfg):
+        shapes.setdefault((K, N), name)
+    assert len(shapes) == 5  # q and o, k and v, gate_up, down, lm_head
+    for i, ((K, N), name) in enumerate(sorted(shapes.items())):
+        check_full_layer(K, N, cfg["G"], cfg["fmt"], cfg["M"], synth.layer_seed(cfg["seed"], i), cfg["w"], cfg["x"],
+                         count=256)
+        torch.cuda.empty_cache()
