@@ -176,6 +176,32 @@ int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes,
  * that call are then incomplete), HQ_OK otherwise. */
 int hq_workspace_status(void *workspace, void *stream);
 
+/* hq_verify_gemm without a caller-supplied workspace, for callers that
+ * cannot allocate device memory at the point of the call: code that runs
+ * under an allocator that forbids new allocations (for example inside a
+ * memory-capped serving process, or a plugin whose host owns all device
+ * memory), or code that must not call cudaMalloc because it would
+ * synchronize the device.  The pages have no counterpart of this call.
+ *
+ * The scratch lives in one file-scope device array of
+ * HQ_NOALLOC_SCRATCH_BYTES (16 MiB + 64 KiB) that every GPU which loads the
+ * library holds until the process exits.  A call is accepted when
+ * hq_workspace_bytes(desc, M) fits in it (M <= 32 for any N up to about two
+ * million outputs); larger calls return HQ_ERR_UNSUPPORTED and launch
+ * nothing.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Each call clears the
+ * array's control words (error word and arrival counters) on `stream`
+ * before the kernel.  All calls on a device share the one array, so calls
+ * that may overlap on the GPU (different streams, or graphs replayed
+ * concurrently) race and must be serialized by the caller.  Arguments,
+ * outputs and flags are those of hq_verify_gemm. */
+#define HQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 64u * 1024u)
+int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
+                           const int32_t *gsum, int32_t M, float *Y, int32_t *partials, uint32_t flags,
+                           void *stream);
+
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing will ever complete, giving up after
  * `limit_ns` nanoseconds (1000..100000000) and setting the error word of

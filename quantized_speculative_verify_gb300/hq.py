@@ -32,7 +32,7 @@ FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 # Every symbol include/hq.h declares.
 EXPORTS = ("hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_make_signs",
            "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
-           "hq_selftest_wait_timeout")
+           "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc")
 
 
 class HQError(RuntimeError):
@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
         "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
         "hq_workspace_status": (ctypes.c_int, [P, P]),
         "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
+        "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, P, I32, P, P, U32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -164,6 +165,20 @@ def hq_workspace_status(workspace, stream=None) -> int:
 def hq_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
     _check(load().hq_selftest_wait_timeout(_ptr(workspace), int(limit_ns), _stream(stream)),
            "hq_selftest_wait_timeout")
+
+
+HQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 64 * 1024
+
+
+def hq_verify_gemm_noalloc(desc, blob, qx, sx, gsum, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:
+    """hq_verify_gemm with the library's fixed device scratch array instead of a workspace."""
+    rc = load().hq_verify_gemm_noalloc(ctypes.byref(desc), _ptr(blob), _ptr(qx), _ptr(sx), _ptr(gsum), int(M), _ptr(Y),
+                                       _ptr(partials), int(flags), _stream(stream))
+    if rc == HQ_ERR_UNSUPPORTED:
+        need = hq_workspace_bytes(desc, M)
+        raise HQError(rc, f"hq_verify_gemm_noalloc: this call needs {need} bytes of scratch, more than the "
+                          f"library's fixed {HQ_NOALLOC_SCRATCH_BYTES}-byte array")
+    _check(rc, "hq_verify_gemm_noalloc")
 
 
 # ------------------------------------------------------- tensor helpers ---

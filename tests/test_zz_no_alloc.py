@@ -1,0 +1,62 @@
+"""hq_verify_gemm_noalloc: the verify GEMM for callers that cannot allocate.
+
+Some callers cannot call cudaMalloc where they run the verify GEMM: a plugin
+whose host process owns every device allocation, a memory-capped serving
+process whose allocator refuses new blocks, or code on a latency-critical
+path where an allocation would synchronize the device.  For them the library
+exports one more entry point that takes no workspace and allocates nothing:
+its scratch is a fixed file-scope device array inside the library.  These
+tests check that it gives the same outputs as hq_verify_gemm with a caller
+workspace, on two calls in a row (the array keeps the previous call's
+contents), and that calls needing more scratch than the array are refused.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_speculative_verify_gb300 import hq, synth
+
+ATOL, RTOL = 1e-6, 1e-5
+
+
+def test_noalloc_refuses_calls_larger_than_its_array():
+    lib = hq.load()
+    d = hq.make_desc(4096, 4096, 64, "w4")
+    fake = 0x10000  # never dereferenced: the size check comes first
+    assert hq.hq_workspace_bytes(d, 33) > hq.HQ_NOALLOC_SCRATCH_BYTES
+    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(d), fake, fake, fake, fake, 33, fake, None, 0, None)
+    assert rc == hq.HQ_ERR_UNSUPPORTED
+    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, fake, fake, fake, 16, fake, None, 0, None)
+    assert rc == hq.HQ_ERR_INVALID_ARG
+    assert lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, None, None, None, 0, None, None, 0, None) == hq.HQ_OK
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt,M,K,N,G", [("w4", 16, 4096, 1024, 64), ("w8", 32, 4096, 384, 128),
+                                         ("w4", 5, 512, 200, 32)])
+def test_noalloc_matches_workspace_entry_point_twice(fmt, M, K, N, G):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = "cuda"
+    X = synth.activations(M, K, seed=M + 3, outlier_channels=2).to(dev)
+    W = synth.weights(N, K, seed=N + 5).to(dev)
+    signs = hq.hq_make_signs(17, K)
+    layer = hq.pack_layer(W, G, fmt, signs)
+    qx, sx, gsum = hq.act_buffers(M, K, G, dev)
+    hq.hq_rotate_quant_act(X, M, K, G, layer.signs, qx, sx, gsum)
+    ws = hq.workspace(layer.desc, M, dev)
+    y_ref = torch.empty((M, N), dtype=torch.float32, device=dev)
+    hq.hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, M, y_ref, None, ws)
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    ref = y_ref.cpu().numpy().astype(np.float64)
+    for call in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        hq.hq_verify_gemm_noalloc(layer.desc, layer.blob, qx, sx, gsum, M, y)
+        torch.cuda.synchronize()
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref)), f"call {call + 1} differs"
