@@ -284,13 +284,13 @@ class VerifyPass:
             if not name.endswith((".k", ".v")):  # a new activation input
                 s_host = hq.hq_make_signs(synth.layer_seed(seed, 500 + li), K)
                 X = synth.activations(self.M, K, seed=synth.layer_seed(seed, 2000 + li), device=device, **cfg["x"])
-                qx, sx, gsum = hq.act_buffers(self.M, K, self.G, device)
-                self.inputs.append([name, K, X, qx, sx, gsum, None])
+                _, qop, sx = hq.act_buffers(self.M, K, device, int8_codes=False)
+                self.inputs.append([name, K, X, qop, sx, None])
             W = synth.weights(N, K, seed=synth.layer_seed(seed, li), device=device, **cfg["w"])
             layer = hq.pack_layer(W, self.G, self.fmt, s_host)
             del W
-            if self.inputs[-1][6] is None:
-                self.inputs[-1][6] = layer.signs
+            if self.inputs[-1][5] is None:
+                self.inputs[-1][5] = layer.signs
             self.layers.append(layer)
             self.ys.append(torch.empty((self.M, N), dtype=torch.float32, device=device))
             self.plan.append((len(self.inputs) - 1, li))
@@ -305,14 +305,13 @@ class VerifyPass:
         hq = self.hq
         done = set()
         for ii, li in self.plan:
-            name, K, X, qx, sx, gsum, signs = self.inputs[ii]
+            name, K, X, qop, sx, signs = self.inputs[ii]
             if act and ii not in done:
-                hq.hq_rotate_quant_act(X, self.M, K, self.G, signs, qx, sx, gsum, self.flags)
+                hq.hq_rotate_quant_act(X, self.M, K, signs, None, qop, sx, self.flags)
                 done.add(ii)
             if gemm:
                 layer = self.layers[li]
-                hq.hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, self.M, self.ys[li], None, self.ws,
-                                  self.flags)
+                hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, self.M, self.ys[li], None, self.ws, self.flags)
 
     def h2d_bytes(self):
         return sum(inp[2].numel() * 4 for inp in self.inputs)

@@ -93,7 +93,8 @@ size_t hq_packed_bytes(const hq_layer_desc *desc);
 
 /* Size in bytes of the workspace hq_verify_gemm needs for `desc` and M rows
  * (0 if the arguments are invalid).  The workspace holds the device error
- * word, the split-K arrival counters and the split-K partial sums.  It must
+ * word, the split-K arrival counters and the split-K partial sums (sized for
+ * at most 32 rows: larger batches run as consecutive 32-row launches).  It must
  * be zero-filled once after allocation; every call leaves it zero-filled
  * again (except for the error word after a timeout, see
  * hq_workspace_status). */
@@ -122,30 +123,36 @@ int hq_make_signs(uint64_t seed, int32_t K, uint32_t *signs_host);
 int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *signs, void *blob,
                     void *stream);
 
+/* Size in bytes of the GEMM's activation operand for M rows and K features
+ * (0 if the arguments are invalid): M * ceil(K/128) * 256. */
+size_t hq_act_operand_bytes(int32_t M, int32_t K);
+
 /* Verify pass, step 1: rotate and quantize the activations of M rows
  * (section "How Uzu optimizes bytes and tokens per pass": activations
  * quantized to 8 bits on the fly, after the same randomized Hadamard
  * transform as the weights).
- *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op)
+ *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op),
+ *         K a positive multiple of 32, at most 65536
  *   signs uint32 [K/32]
- *   qx    int8 [M][K] (8-byte aligned):  clamp(rint(x' / sx), -127, 127)
+ *   qx    int8 [M][K] (4-byte aligned) or NULL: clamp(rint(x' / sx), -127, 127)
+ *   qop   the GEMM's activation operand (hq_act_operand_bytes(M, K) bytes,
+ *         16-byte aligned) or NULL: the same codes as IEEE fp16 in blocks of
+ *         128 features, [ceil(K/128)][M][128]; within a row of 128 codes the
+ *         16-byte chunk c of an odd row m is stored at chunk c ^ 4; codes past
+ *         K are zero
  *   sx    fp32 [M]:  max_k |x'[m][k]| / 127  (0 for an all-zero row)
- *   gsum  int32 [M][K/group]: sum of qx over each group (the zero-point
- *         correction term of the Medium format; may be NULL for Large)
- * x' is the rotated row: per 32-block, sign flip, unnormalized Walsh-
- * Hadamard butterfly at strides 1, 2, 4, 8, 16 in fp32 without fused
- * multiply-add, then multiplication by fp32(1/sqrt(32)).  flags:
- * HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL. */
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
-                        float *sx, int32_t *gsum, uint32_t flags, void *stream);
+ * At least one of qx, qop must be given.  x' is the rotated row: per
+ * 32-block, sign flip, unnormalized Walsh-Hadamard butterfly at strides 1, 2,
+ * 4, 8, 16 in fp32 without fused multiply-add, then multiplication by
+ * fp32(1/sqrt(32)).  flags: HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL. */
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *signs, int8_t *qx, void *qop,
+                        float *sx, uint32_t flags, void *stream);
 
 /* Verify pass, step 2: integer GEMM of the quantized activations against the
  * packed weights with the per-group dequantization epilogue (section "How
- * Uzu optimizes bytes and tokens per pass": both matmul operands integers,
- * int8 matrix path).
+ * Uzu optimizes bytes and tokens per pass": both matmul operands integers).
  *   blob      packed by hq_pack_weights for the same desc (16-byte aligned)
- *   qx, sx, gsum  from hq_rotate_quant_act with the same K, group, signs
- *             (gsum may be NULL for the Large format)
+ *   qop, sx   from hq_rotate_quant_act with the same M, K and signs
  *   M         0..HQ_MAX_M (0: no-op)
  *   Y         fp32 [M][N]:
  *               Y[m][n] = sx[m] * sum_g ( scale[n][g] * P[m][n][g] )
@@ -155,13 +162,14 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, con
  *             exactly (slower; for verification)
  *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
  *             before its first use
- * The fp32 sum over groups is taken in ascending group order; an output
- * whose K range is split across thread blocks sums the blocks' partial sums
- * in ascending K order, so results are deterministic.  flags:
- * HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL (see above). */
-int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
-                   const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
-                   void *stream);
+ * The integer sums P are exact (the codes are multiplied on fp16 tensor cores
+ * with fp32 accumulation, which is exact for these ranges).  The fp32 sum
+ * over groups is taken in ascending group order; an output whose K range is
+ * split across thread blocks sums the blocks' partial sums in ascending K
+ * order, so results are deterministic.  flags: HQ_LAUNCH_DEFAULT or
+ * HQ_LAUNCH_PDL (see above). */
+int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
+                   int32_t *partials, void *workspace, uint32_t flags, void *stream);
 
 /* Canonical view of a blob (for verification and for saving in a portable
  * form): codes uint8 [N][K] (Medium: 0..15; Large: the int8 code's byte),
@@ -186,7 +194,7 @@ int hq_workspace_status(void *workspace, void *stream);
  * The scratch lives in one file-scope device array of
  * HQ_NOALLOC_SCRATCH_BYTES (16 MiB + 64 KiB) that every GPU which loads the
  * library holds until the process exits.  A call is accepted when
- * hq_workspace_bytes(desc, M) fits in it (M <= 32 for any N up to about two
+ * hq_workspace_bytes(desc, M) fits in it (any M, for N up to about two
  * million outputs); larger calls return HQ_ERR_UNSUPPORTED and launch
  * nothing.  The call allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine.  The first call on a device looks up the
@@ -198,9 +206,8 @@ int hq_workspace_status(void *workspace, void *stream);
  * concurrently) race and must be serialized by the caller.  Arguments,
  * outputs and flags are those of hq_verify_gemm. */
 #define HQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 64u * 1024u)
-int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
-                           const int32_t *gsum, int32_t M, float *Y, int32_t *partials, uint32_t flags,
-                           void *stream);
+int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
+                           int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream);
 
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing will ever complete, giving up after

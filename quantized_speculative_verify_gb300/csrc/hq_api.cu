@@ -43,40 +43,53 @@ cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const int8_t *qx, const float *sx,
-                               const int32_t *gsum, int M, float *Y, int32_t *partials, void *workspace, bool pdl,
-                               cudaStream_t s) {
+cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
+                               int32_t *partials, void *workspace, bool pdl, cudaStream_t s) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
     GemmArgs a;
     a.blob = static_cast<const uint8_t *>(blob);
-    a.qx = qx;
+    a.qop = qop;
     a.sx = sx;
-    a.gsum = gsum;
     a.Y = Y;
     a.partials = partials;
     a.ws = static_cast<uint8_t *>(workspace);
     a.ws_partial_off = ws_partial_offset(g);
-    a.M = M;
+    a.M_total = M;
     a.N = g.N;
     a.K = g.K;
     a.NGK = g.NGK;
     a.KTILES = g.KTILES;
     a.T = g.NB * g.KTILES;
-    int sms = device_sm_count();
-    if (sms <= 0) return cudaErrorNoDevice;
-    int grid = sms;
-    if (grid > a.T) grid = a.T;
+    // Two thread blocks per SM (eight consumer warps) keep enough loads and
+    // tensor-core steps in flight; each block's stage ring is about 64 KB.
+    // Small layers get fewer blocks so that every block streams at least
+    // MIN_TILES tiles and an n-block is split between few blocks (the last
+    // one to finish sums the others' partial sums).
+    constexpr int MIN_TILES = 4;
+    int grid = 2 * sms;
+    if (grid > a.T / MIN_TILES) grid = a.T / MIN_TILES;
+    if (grid < 1) grid = 1;
     if (grid > MAX_CTAS) grid = MAX_CTAS;
     a.grid = grid;
-    // Stage ring of about 96 KB: two blocks of consecutive launches fit on an
-    // SM together, so the next layer's weights stream while this one ends.
-    int stages = (96 * 1024) / g.tile_bytes;
-    if (stages < 2) stages = 2;
-    if (stages > 16) stages = 16;
-    a.stages = stages;
     a.tile_bytes = g.tile_bytes;
     a.code_bytes = g.code_bytes;
     a.scale_bytes = g.scale_bytes;
-    return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, g.G, pdl, s) : launch_gemm_w8(a, g.G, pdl, s);
+    // Batches of more than MAX_M_LAUNCH rows run as consecutive launches over
+    // row slices; each streams the weights again and reuses the workspace.
+    for (int m0 = 0; m0 < M; m0 += MAX_M_LAUNCH) {
+        a.m0 = m0;
+        a.M = M - m0 < MAX_M_LAUNCH ? M - m0 : MAX_M_LAUNCH;
+        a.act_bytes = a.M * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
+        int stages = (64 * 1024) / (g.tile_bytes + a.act_bytes);
+        if (stages < 2) stages = 2;
+        if (stages > 16) stages = 16;
+        a.stages = stages;
+        const cudaError_t e =
+            g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, g.G, pdl, s) : launch_gemm_w8(a, g.G, pdl, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace hq
@@ -149,36 +162,38 @@ int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *s
     return cuda_status(hq::launch_pack(g, W, signs, blob, static_cast<cudaStream_t>(stream)));
 }
 
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
-                        float *sx, int32_t *gsum, uint32_t flags, void *stream) {
-    if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if (K <= 0 || K % 32 != 0) return HQ_ERR_INVALID_ARG;
-    if (!(group == 16 || group == 32 || group == 64 || group == 128 || group == 256) || K % group != 0)
-        return HQ_ERR_INVALID_ARG;
-    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
-    if (M == 0) return HQ_OK;
-    if (!X || !signs || !qx || !sx) return HQ_ERR_INVALID_ARG;
-    if (!aligned(X, 16) || !aligned(qx, 8) || !aligned(sx, 4) || !aligned(signs, 4) || (gsum && !aligned(gsum, 4)))
-        return HQ_ERR_INVALID_ARG;
-    if (K > 65536) return HQ_ERR_UNSUPPORTED;
-    return cuda_status(hq::launch_rotate_quant_act(X, M, K, group, signs, qx, sx, gsum, (flags & HQ_LAUNCH_PDL) != 0,
-                                                   static_cast<cudaStream_t>(stream)));
+size_t hq_act_operand_bytes(int32_t M, int32_t K) {
+    if (M < 0 || M > HQ_MAX_M || K <= 0 || K % 32 != 0) return 0;
+    return hq::act_operand_bytes(M, K);
 }
 
-int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
-                   const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
-                   void *stream) {
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *signs, int8_t *qx, void *qop,
+                        float *sx, uint32_t flags, void *stream) {
+    if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
+    if (K <= 0 || K % 32 != 0) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (M == 0) return HQ_OK;
+    if (!X || !signs || !sx || (!qx && !qop)) return HQ_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(sx, 4) || !aligned(signs, 4) || (qx && !aligned(qx, 4)) ||
+        (qop && !aligned(qop, 16)))
+        return HQ_ERR_INVALID_ARG;
+    if (K > 65536) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, signs, qx, static_cast<uint8_t *>(qop), sx,
+                                                   (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
+                   int32_t *partials, void *workspace, uint32_t flags, void *stream) {
     if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
     if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
-    if (!blob || !qx || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
-    if (desc->format == HQ_W4_ASYM && !gsum) return HQ_ERR_INVALID_ARG;
-    if (!aligned(blob, 16) || !aligned(qx, 8) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
-        (gsum && !aligned(gsum, 4)) || (partials && !aligned(partials, 4)))
+    if (!blob || !qop || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
+        (partials && !aligned(partials, 4)))
         return HQ_ERR_INVALID_ARG;
     const Geom g = geom_of(desc);
-    return cuda_status(hq::launch_verify_gemm(g, blob, qx, sx, gsum, M, Y, partials, workspace,
+    return cuda_status(hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, workspace,
                                               (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
 }
 

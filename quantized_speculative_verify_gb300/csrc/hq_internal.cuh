@@ -18,9 +18,14 @@ namespace hq {
 // range and one bulk copy fetches a whole tile.  Inside a tile:
 //
 //   codes   [chunk][ntile 0..7][lane 0..31][16 bytes]
-//           ntile = 16 consecutive channels; a lane's 16 bytes are exactly
-//           the A operand it feeds to mma.m16n8k32 (two k32 steps for the
-//           4-bit format, one for the 8-bit format) -- see pack kernel.
+//           ntile = 16 consecutive channels.  A lane (g = lane/4, t = lane%4)
+//           of the consumer warp that owns the ntile holds, for every 32
+//           features f0.., channels g and g+8 at features f0 + 8t .. f0 + 8t + 7:
+//           the operands of two mma.m16n8k16 steps.  A chunk covers 64
+//           features in the 4-bit format (four 32-bit words, one per 16-feature
+//           step, nibble layout in widen_w4 of k_gemm.cuh) and 32 features in
+//           the 8-bit format (four words: channel g features +0..3, channel
+//           g+8 +0..3, channel g +4..7, channel g+8 +4..7).
 //   scales  [group in tile][ntile][16 floats, rows ordered 0,8,1,9,...,7,15]
 //   zeros   [group in tile][ntile][8 bytes, byte r = z[r] | z[r+8] << 4]
 //           (4-bit format only)
@@ -89,8 +94,21 @@ __host__ __device__ inline size_t ws_counter_offset() { return 16; }
 __host__ __device__ inline size_t ws_counter_bytes(const Geom &g) { return ((size_t)g.NB * 4 + 15) / 16 * 16; }
 __host__ __device__ inline size_t ws_partial_offset(const Geom &g) { return ws_counter_offset() + ws_counter_bytes(g); }
 __host__ __device__ inline size_t ws_slot_floats(int M) { return (size_t)BN * (size_t)M; }
+// The GEMM handles at most MAX_M_LAUNCH rows per launch (larger batches are
+// run as consecutive launches that reuse the workspace).
+constexpr int MAX_M_LAUNCH = 32;
 __host__ __device__ inline size_t ws_bytes(const Geom &g, int M) {
-    return ws_partial_offset(g) + (size_t)MAX_CTAS * 2 * ws_slot_floats(M) * 4;
+    const int m = M < MAX_M_LAUNCH ? M : MAX_M_LAUNCH;
+    return ws_partial_offset(g) + (size_t)MAX_CTAS * 2 * ws_slot_floats(m) * 4;
+}
+
+// Activation operand of the GEMM: fp16 codes in blocks of 128 features,
+// [ceil(K/128)][M][128]; inside a 256-byte row the 16-byte chunk q of token
+// row t is stored at chunk q ^ (4 * (t & 1)) (bank-conflict-free reads of
+// the mma B operands); features past K are zero.
+constexpr int ACT_BLOCK = 128;
+__host__ __device__ inline size_t act_operand_bytes(int M, int K) {
+    return (size_t)M * (size_t)((K + ACT_BLOCK - 1) / ACT_BLOCK) * ACT_BLOCK * 2;
 }
 
 // Device error codes written to the workspace error word.
@@ -160,6 +178,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -182,28 +206,17 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// D = A(16x32, int8) * B(32x8, int8) + D, int32 accumulate.
-__device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 }  // namespace hq
 
 // Launchers (defined in the kernel translation units).
 namespace hq {
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
-                                    int32_t *gsum, bool pdl, cudaStream_t s);
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop,
+                                    float *sx, bool pdl, cudaStream_t s);
 cudaError_t launch_pack(const Geom &g, const float *W, const uint32_t *signs, void *blob, cudaStream_t s);
 cudaError_t launch_unpack(const Geom &g, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
                           cudaStream_t s);
-cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const int8_t *qx, const float *sx,
-                               const int32_t *gsum, int M, float *Y, int32_t *partials, void *workspace, bool pdl,
-                               cudaStream_t s);
+cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
+                               int32_t *partials, void *workspace, bool pdl, cudaStream_t s);
 cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s);
 int device_sm_count();
 }  // namespace hq

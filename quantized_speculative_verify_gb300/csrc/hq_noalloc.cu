@@ -36,16 +36,14 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
-extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
-                                      const int32_t *gsum, int32_t M, float *Y, int32_t *partials, uint32_t flags,
-                                      void *stream) {
+extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
+                                      int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream) {
     if (!desc || !hq::desc_valid(desc->K, desc->N, desc->group, desc->format)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
     if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
-    if (!blob || !qx || !sx || !Y) return HQ_ERR_INVALID_ARG;
-    if (desc->format == HQ_W4_ASYM && !gsum) return HQ_ERR_INVALID_ARG;
-    if (!aligned(blob, 16) || !aligned(qx, 8) || !aligned(sx, 4) || !aligned(Y, 4) || (gsum && !aligned(gsum, 4)) ||
+    if (!blob || !qop || !sx || !Y) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) ||
         (partials && !aligned(partials, 4)))
         return HQ_ERR_INVALID_ARG;
     const hq::Geom g = hq::make_geom(desc->K, desc->N, desc->group, desc->format);
@@ -58,7 +56,8 @@ extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blo
     // The previous call's contents stay in the array: clear the error word
     // and the arrival counters, which must start at zero.
     if (cudaMemsetAsync(scratch, 0, hq::ws_partial_offset(g), s) != cudaSuccess) return HQ_ERR_CUDA;
-    const cudaError_t e = hq::launch_verify_gemm(g, blob, qx, sx, gsum, M, Y, partials, scratch,
-                                                 (flags & HQ_LAUNCH_PDL) != 0, s);
+    const cudaError_t e =
+        hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, scratch,
+                               (flags & HQ_LAUNCH_PDL) != 0, s);
     return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }

@@ -12,6 +12,9 @@
 // exchanges (xor 1, 2, 4).  Every add, subtract and multiply is a separate
 // IEEE-rounded fp32 operation in the order 1, 2, 4, 8, 16, so the rotated
 // values are bit-identical to a scalar implementation of the same order.
+// The codes are written as int8 and/or as the GEMM's operand: fp16 (exact
+// for |q| <= 127) in 128-feature blocks, laid out for its tensor-core steps.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "hq_internal.cuh"
@@ -31,11 +34,10 @@ __device__ __forceinline__ float bfly_x(float v, int lane_bit, bool upper) {
 }
 
 template <int V, int T>
-__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G,
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K,
                                                         const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
-                                                        float *__restrict__ sx, int32_t *__restrict__ gsum) {
+                                                        uint8_t *__restrict__ qop, float *__restrict__ sx) {
     __shared__ float s_red[T / 32];
-    extern __shared__ __align__(16) int8_t s_q[];  // the row's codes, for the group sums
     pdl_launch_dependents();
     pdl_wait();
 
@@ -45,7 +47,6 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const int n4 = K >> 2;  // float4s per row
     const float c = __int_as_float((int)HADAMARD_SCALE_BITS);
     const float4 *xr = reinterpret_cast<const float4 *>(X + (size_t)row * K);
-    const int NG = K / G;
 
     float4 v[V];
 #pragma unroll
@@ -104,72 +105,62 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const float s = a == 0.0f ? 0.0f : __fdiv_rn(a, 127.0f);
     if (tid == 0) sx[row] = s;
 
-    char4 *qr = reinterpret_cast<char4 *>(qx + (size_t)row * K);
-    char4 *sq = reinterpret_cast<char4 *>(s_q);
+    // outputs: int8 codes and/or the GEMM operand (the same codes as fp16,
+    // exact), 4 features per thread; the operand's padding past K is zeroed
+    char4 *qr = qx ? reinterpret_cast<char4 *>(qx + (size_t)row * K) : nullptr;
+    const int n4pad = ((K + ACT_BLOCK - 1) / ACT_BLOCK) * (ACT_BLOCK / 4);
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int idx = tid + j * T;
         int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-        if (s != 0.0f) {
+        if (s != 0.0f && idx < n4) {
             q0 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].x, s))));
             q1 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].y, s))));
             q2 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].z, s))));
             q3 = min(127, max(-127, __float2int_rn(__fdiv_rn(v[j].w, s))));
         }
-        if (idx < n4) {
-            const char4 q4 = make_char4((signed char)q0, (signed char)q1, (signed char)q2, (signed char)q3);
-            qr[idx] = q4;
-            if (gsum) sq[idx] = q4;
-        }
-    }
-    if (gsum) {
-        // one thread per group: sum its G codes (exact integer arithmetic)
-        __syncthreads();
-        for (int gi = tid; gi < NG; gi += T) {
-            const char4 *p = sq + (size_t)gi * (G / 4);
-            int t = 0;
-            for (int w = 0; w < G / 4; ++w) {
-                const char4 c4 = p[w];
-                t += (int)c4.x + (int)c4.y + (int)c4.z + (int)c4.w;
-            }
-            gsum[(size_t)row * NG + gi] = t;
+        if (qr && idx < n4) qr[idx] = make_char4((signed char)q0, (signed char)q1, (signed char)q2, (signed char)q3);
+        if (qop && idx < n4pad) {
+            const uint32_t h0 = __half_as_ushort(__int2half_rn(q0)), h1 = __half_as_ushort(__int2half_rn(q1));
+            const uint32_t h2 = __half_as_ushort(__int2half_rn(q2)), h3 = __half_as_ushort(__int2half_rn(q3));
+            const int f = idx * 4;                      // first feature
+            const int kb = f / ACT_BLOCK;               // 128-feature block
+            const int q = (f % ACT_BLOCK) / 8;          // 16-byte chunk in the row
+            const int qs = q ^ ((row & 1) << 2);        // swizzled chunk
+            uint8_t *dst = qop + ((size_t)kb * M + row) * (ACT_BLOCK * 2) + qs * 16 + (f % 8) * 2;
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
         }
     }
 }
 
 template <int V, int T>
-cudaError_t launch_act_t(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
-                         int32_t *gsum, bool pdl, cudaStream_t s) {
+cudaError_t launch_act_t(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop, float *sx,
+                         bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)M);
     cfg.blockDim = dim3(T);
-    cfg.dynamicSmemBytes = gsum ? (size_t)K : 0;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (cfg.dynamicSmemBytes > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_rotate_quant_act<V, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)cfg.dynamicSmemBytes);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, signs, qx, sx, gsum);
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, signs, qx, qop, sx);
 }
 
 }  // namespace
 
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, float *sx,
-                                    int32_t *gsum, bool pdl, cudaStream_t s) {
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop,
+                                    float *sx, bool pdl, cudaStream_t s) {
     const int n4 = K / 4;
-    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 256 * 2) return launch_act_t<2, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 256 * 4) return launch_act_t<4, 256>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 512 * 4) return launch_act_t<4, 512>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
-    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, signs, qx, sx, gsum, pdl, s);
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 256 * 2) return launch_act_t<2, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 256 * 4) return launch_act_t<4, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 512 * 4) return launch_act_t<4, 512>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -1,12 +1,21 @@
-// k_gemm.cuh -- the verify GEMM: int8 activations x packed 4-/8-bit weights,
-// per-group int32 partial sums, fp32 dequantization epilogue.
+// k_gemm.cuh -- the verify GEMM: activation codes x packed 4-/8-bit weights,
+// per-group exact integer partial sums, fp32 dequantization epilogue.
 //
 // Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling":
 // section "How Uzu optimizes bytes and tokens per pass" (both operands of the
-// verify matmul are integers and run on the int8 matrix path; Medium weights
-// are 4-bit asymmetric, Large 8-bit symmetric, grouped along K) and section
-// "Why batch-one decoding is memory-bound" (the pass streams every weight
-// once, so the kernel is bound by memory bandwidth, not arithmetic).
+// verify matmul are integers; Medium weights are 4-bit asymmetric, Large 8-bit
+// symmetric, grouped along K) and section "Why batch-one decoding is
+// memory-bound" (the pass streams every weight once, so the kernel is bound by
+// memory bandwidth, not arithmetic).
+//
+// Integer arithmetic on fp16 tensor cores.  The int8 MMA rate of this GPU is
+// far below its fp16 rate, so the integer contraction runs as an exact fp16
+// MMA with fp32 accumulation: activation codes (|q| <= 127), weight codes
+// minus zero point (|q - z| <= 15) and 8-bit weight codes (|q| <= 127) are
+// exact in fp16, their products are exact in fp32, and a group's sum stays
+// below 127 * 127 * 256 < 2^24, so the fp32 accumulator holds the integer
+// partial sum P exactly.  The zero point is applied while widening the 4-bit
+// codes: (1024 + q) - (1024 + z) = q - z in fp16.
 //
 // Work decomposition (stream-K).  The blob is a sequence of T tiles
 // (n-block major, K minor).  Thread block c owns tiles [c*T/grid,
@@ -16,16 +25,17 @@
 // last (arrival counter, no waiting), which sums the contributors' fp32
 // partial sums in ascending K order.
 //
-// Inside a block: one producer warp issues one bulk copy per tile into a ring
-// of shared-memory stages (mbarrier transaction counts); NCW consumer warps
-// each own NW row tiles of 16 channels of the 128-channel n-block and walk the
-// tiles in K order.  Per k32 step a lane loads 8 bytes of int8 activations
-// per 8-token column tile (the B operand of mma.m16n8k32) and reads its
-// 16-byte weight fragment from shared memory (the A operand: 16 channels x
-// 32 features; 4-bit codes are widened to bytes with two masks).  After each
-// quantization group: P = acc - zero * gsum (int32, exact), then
-// y += scale * float(P) with separately rounded fp32 multiply and add, group
-// by group in ascending order.
+// Inside a block: one producer thread issues, per tile, a bulk copy of the
+// weight tile and one of the activation block for the tile's features into a
+// ring of shared-memory stages (mbarrier transaction counts).  The weight
+// copies of the first stages are issued before waiting for the previous
+// kernel of the stream (weights never depend on it); the activation copies
+// after.  Four consumer warps each own two row tiles of 16 channels of the
+// 128-channel n-block and walk the tiles in K order: per 32 features a lane
+// reads 16 bytes of fp16 activation codes per 8-token column tile (the B
+// operands of two mma.m16n8k16) and widens its 16-byte weight chunk into the
+// A operands.  After each quantization group: y += scale * P with separately
+// rounded fp32 multiply and add, group by group in ascending order.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -36,15 +46,15 @@ namespace hq {
 
 struct GemmArgs {
     const uint8_t *blob;
-    const int8_t *qx;
-    const float *sx;
-    const int32_t *gsum;
-    float *Y;
-    int32_t *partials;
+    const uint8_t *qop;  // activation operand: [K/128][M_total][128 fp16], odd rows swizzled
+    const float *sx;     // [M_total]
+    float *Y;            // [M_total][N]
+    int32_t *partials;   // check mode: [M_total][N][K/G] or NULL
     uint8_t *ws;
     size_t ws_partial_off;  // byte offset of the partial-sum slots in ws
-    int M, N, K, NGK, KTILES, T, grid, stages;
-    int tile_bytes, code_bytes, scale_bytes;
+    int M_total, m0, M;     // rows of the call, first row of this launch, rows of this launch (<= 32)
+    int N, K, NGK, KTILES, T, grid, stages;
+    int tile_bytes, code_bytes, scale_bytes, act_bytes;
 };
 
 __device__ __forceinline__ int tile_begin(int c, int T, int grid) { return (int)(((long long)c * T) / grid); }
@@ -53,72 +63,79 @@ __device__ __forceinline__ int cta_of_tile(int t, int T, int grid) {
     return (int)((((long long)t + 1) * grid - 1) / T);
 }
 
-// End of one quantization group: P = acc - zero * gsum (exact int32), then
-// y += scale * float(P), one IEEE-rounded multiply and one add per output.
-// gl = group within the tile, gg = group along the whole K.
-template <int FMT, int MT, int NW>
-__device__ __forceinline__ void group_epilogue(const GemmArgs &a, int (&iacc)[NW][MT][4], float (&facc)[NW][MT][4],
-                                               const float *tsc, const uint8_t *tzp, int gl, int gg, int b, int warp,
-                                               int g8, int tig) {
-    int gs[MT][2];
-#pragma unroll
-    for (int tt = 0; tt < MT; ++tt) {
-        const int tok0 = tt * 8 + tig * 2;
-        gs[tt][0] = (FMT == HQ_W4_ASYM && tok0 < a.M) ? __ldg(a.gsum + (size_t)tok0 * a.NGK + gg) : 0;
-        gs[tt][1] = (FMT == HQ_W4_ASYM && tok0 + 1 < a.M) ? __ldg(a.gsum + (size_t)(tok0 + 1) * a.NGK + gg) : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < NW; ++j) {
-        const int nt = warp * NW + j;
-        const float2 sc = *reinterpret_cast<const float2 *>(tsc + ((size_t)gl * NTILES + nt) * 16 + 2 * g8);
-        int zl = 0, zh = 0;
-        if (FMT == HQ_W4_ASYM) {
-            const int zb = tzp[((size_t)gl * NTILES + nt) * 8 + g8];
-            zl = zb & 15;
-            zh = zb >> 4;
-        }
-#pragma unroll
-        for (int tt = 0; tt < MT; ++tt) {
-            int p[4];
-            p[0] = iacc[j][tt][0] - zl * gs[tt][0];
-            p[1] = iacc[j][tt][1] - zl * gs[tt][1];
-            p[2] = iacc[j][tt][2] - zh * gs[tt][0];
-            p[3] = iacc[j][tt][3] - zh * gs[tt][1];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float s = (e >> 1) ? sc.y : sc.x;
-                facc[j][tt][e] = __fadd_rn(facc[j][tt][e], __fmul_rn(s, __int2float_rn(p[e])));
-                iacc[j][tt][e] = 0;
-            }
-            if (a.partials) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = tt * 8 + tig * 2 + (e & 1);
-                    const int n = b * BN + nt * 16 + g8 + 8 * (e >> 1);
-                    if (tok < a.M && n < a.N) a.partials[((size_t)tok * a.N + n) * a.NGK + gg] = p[e];
-                }
-            }
-        }
-    }
+// 4-bit codes -> fp16 (q - z).  Word layout (nibble i at bits 4i):
+// (n0, n4) row g features b, b+1; (n1, n5) row g+8 features b, b+1;
+// (n2, n6) row g features b+2, b+3; (n3, n7) row g+8 features b+2, b+3.
+// Low nibbles of a half become 1024 + q via the fp16 exponent bits 0x6400;
+// nibbles at bits 4..7 of a half become 1024 + 16 q and are scaled by 1/16.
+// kA = fp16x2(1024 + z_g), kB = fp16x2(-(64 + z_{g+8})).
+__device__ __forceinline__ void widen_w4(uint32_t w, uint32_t kA, uint32_t kB, uint32_t (&A)[4]) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t x0 = (w & 0x000F000Fu) | 0x64006400u;
+    const uint32_t x1 = (w & 0x00F000F0u) | 0x64006400u;
+    const uint32_t x2 = (w8 & 0x000F000Fu) | 0x64006400u;
+    const uint32_t x3 = (w8 & 0x00F000F0u) | 0x64006400u;
+    const uint32_t sixteenth = 0x2C002C00u;  // fp16x2(1/16)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(A[0]) : "r"(x0), "r"(kA));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(A[1]) : "r"(x1), "r"(sixteenth), "r"(kB));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(A[2]) : "r"(x2), "r"(kA));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(A[3]) : "r"(x3), "r"(sixteenth), "r"(kB));
 }
 
-template <int FMT, int G, int MT, int NW>
+// Four int8 codes -> two fp16x2: bias to unsigned, place under the fp16
+// exponent bits 0x64 (1024 + 128 + q), subtract 1152.
+__device__ __forceinline__ void widen_i8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t l, h;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(l) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(h) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
+}
+
+// D = A(16x16, fp16) * B(16x8, fp16) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&A)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(b0), "r"(b1));
+}
+// Same with a zero accumulator input (first step of a group).
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], const uint32_t (&A)[4], uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
+// (f0, f1) += s * (a0, a1): product rounded, then sum rounded (not fused).
+__device__ __forceinline__ void scale_add2(float &f0, float &f1, float a0, float a1, float s) {
+    f0 = __fadd_rn(f0, __fmul_rn(s, a0));
+    f1 = __fadd_rn(f1, __fmul_rn(s, a1));
+}
+
+template <int FMT, int G, int MT>
 struct GemmCfg {
-    static constexpr int KT = G > 128 ? G : 128;
-    static constexpr int STEPS = KT / 32;   // k32 steps per tile
-    static constexpr int GPT = KT / G;      // groups per tile
-    static constexpr int NCW = NTILES / NW; // consumer warps
+    static constexpr int NW = 2;                  // row tiles per consumer warp
+    static constexpr int KT = G > 128 ? G : 128;  // features per tile
+    static constexpr int STEPS = KT / 32;         // 32-feature steps per tile
+    static constexpr int GPT = KT / G;            // groups per tile
+    static constexpr int NCW = NTILES / NW;       // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
 };
 
-template <int FMT, int G, int MT, int NW>
-__global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gemm(const GemmArgs a) {
-    using C = GemmCfg<FMT, G, MT, NW>;
-    constexpr int KT = C::KT, STEPS = C::STEPS, NCW = C::NCW;
+template <int FMT, int G, int MT>
+__global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(const GemmArgs a) {
+    using C = GemmCfg<FMT, G, MT>;
+    constexpr int KT = C::KT, NCW = C::NCW, NW = C::NW, STEPS = C::STEPS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = a.stages;
+    const int stage_bytes = a.tile_bytes + a.act_bytes;
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * a.tile_bytes);  // full[S], empty[S]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);  // full[S], empty[S]
     int *s_flag = reinterpret_cast<int *>(bars + 2 * S);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,25 +157,40 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
     if (warp == NCW) {
         // ------------------------------------------------------ producer ---
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            const int KTILES = a.KTILES;
+            const int blocks = KT / 128;
+            const uint32_t row_bytes = (uint32_t)a.M * 256;  // one 128-feature activation block of this launch
+            // activation blocks of the i-th tile of this thread block -> its stage
+            auto copy_acts = [&](int i, int st) {
+                const int kb = ((t0 + i) % KTILES) * blocks;
+                const uint8_t *src = a.qop + ((size_t)kb * a.M_total + a.m0) * 256;
+                const uint32_t dst = smem_addr(ring + (size_t)st * stage_bytes + a.tile_bytes);
+                const uint32_t fb = smem_addr(&bars[st]);
+                for (int kk = 0; kk < blocks; ++kk)
+                    bulk_copy_g2s(dst + kk * row_bytes, src + (size_t)kk * a.M_total * 256, row_bytes, fb, pol_a);
+            };
             int i = 0;
-            // The weights never depend on earlier kernels of the stream: the
-            // first stages are requested before waiting for them.
+            // Weights never depend on earlier kernels of the stream: the first
+            // stages' weight copies go out before waiting for them.
             for (; i < ntl && i < S; ++i) {
                 const uint32_t fb = smem_addr(&bars[i]);
-                mbar_arrive_expect_tx(fb, (uint32_t)a.tile_bytes);
-                bulk_copy_g2s(smem_addr(ring + (size_t)i * a.tile_bytes),
-                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol);
+                mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+                bulk_copy_g2s(smem_addr(ring + (size_t)i * stage_bytes),
+                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
             }
             pdl_wait();
+            for (int j = 0; j < i; ++j) copy_acts(j, j);
             for (; i < ntl; ++i) {
                 const int st = i % S;
                 const uint32_t ph = (uint32_t)((i / S) & 1);
                 if (!mbar_wait_bounded(smem_addr(&bars[S + st]), ph ^ 1u, err)) break;
                 const uint32_t fb = smem_addr(&bars[st]);
-                mbar_arrive_expect_tx(fb, (uint32_t)a.tile_bytes);
-                bulk_copy_g2s(smem_addr(ring + (size_t)st * a.tile_bytes),
-                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol);
+                mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+                bulk_copy_g2s(smem_addr(ring + (size_t)st * stage_bytes),
+                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
+                copy_acts(i, st);
             }
             // No copy may still be landing in shared memory when the block exits.
             const int issued = i;
@@ -171,12 +203,13 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
     // ---------------------------------------------------------- consumers ---
     pdl_wait();
     const int g8 = lane >> 2, tig = lane & 3;
-    const int M = a.M, N = a.N, K = a.K, NGK = a.NGK;
-    const int KTILES = a.KTILES;
+    const int M = a.M, N = a.N, KTILES = a.KTILES;
     float *wsp = reinterpret_cast<float *>(a.ws + a.ws_partial_off);
     int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
+    const float *sxm = a.sx + a.m0;
+    float *Ym = a.Y + (size_t)a.m0 * N;
 
-    int iacc[NW][MT][4];
+    float acc[NW][MT][4], acc2[NW][MT][4];
     float facc[NW][MT][4];
     int seg_k0 = 0;
     bool ok = true;
@@ -198,94 +231,117 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
         }
         const int st = i % S;
         if (ok) ok = mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / S) & 1), err);
-        const uint8_t *tile = ring + (size_t)st * a.tile_bytes;
+        const uint8_t *tile = ring + (size_t)st * stage_bytes;
+        const uint8_t *acts = tile + a.tile_bytes;
         const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);
         const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;
 
-#pragma unroll
-        for (int j = 0; j < NW; ++j)
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) iacc[j][tt][e] = 0;
-
         uint4 wchunk[NW];
+        uint32_t kA[NW], kB[NW];  // zero-point constants of the lane's current group (4-bit format)
 #pragma unroll
-        for (int s = 0; s < STEPS; ++s) {
-            const int kg = kt * KT + s * 32;  // first feature of this k32 step
-            if (kg >= K) break;               // padding past the real K
-            // A operands (weights) from shared memory
-            if (FMT == HQ_W8_SYM || (s & 1) == 0) {
-                const int ch = FMT == HQ_W4_ASYM ? s >> 1 : s;
+        for (int c = 0; c < STEPS; ++c) {
+            // B operands: 8 fp16 activation codes of token tt*8 + g8, features c*32 + tig*8 .. +7
+            uint4 bq[MT];
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt) {
+                const int tok = tt * 8 + g8;
+                const int q = ((c & 3) * 4 + tig) ^ ((tok & 1) << 2);  // swizzled 16-byte chunk
+                bq[tt] = tok < M ? *reinterpret_cast<const uint4 *>(acts + ((size_t)((c >> 2) * M + tok) * 256 + q * 16))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // A operands: the lane's 16-byte weight chunk (64 features for 4-bit, 32 for 8-bit)
+            if (FMT == HQ_W8_SYM || (c & 1) == 0) {
+                const int ch = FMT == HQ_W4_ASYM ? c >> 1 : c;
 #pragma unroll
                 for (int j = 0; j < NW; ++j) {
                     const int nt = warp * NW + j;
                     wchunk[j] = *reinterpret_cast<const uint4 *>(tile + (((size_t)ch * NTILES + nt) * 32 + lane) * 16);
                 }
             }
-            uint32_t A[NW][4];
+            const bool group_start = G <= 32 || (c * 32) % G == 0;
+            if (FMT == HQ_W4_ASYM && group_start) {
+                const int gl = G == 16 ? 2 * c + (tig >> 1) : (c * 32) / G;  // group of the lane's features
 #pragma unroll
-            for (int j = 0; j < NW; ++j) {
-                if (FMT == HQ_W4_ASYM) {
-                    const uint32_t w0 = (s & 1) ? wchunk[j].z : wchunk[j].x;
-                    const uint32_t w1 = (s & 1) ? wchunk[j].w : wchunk[j].y;
-                    A[j][0] = w0 & 0x0F0F0F0Fu;
-                    A[j][1] = (w0 >> 4) & 0x0F0F0F0Fu;
-                    A[j][2] = w1 & 0x0F0F0F0Fu;
-                    A[j][3] = (w1 >> 4) & 0x0F0F0F0Fu;
-                } else {
-                    A[j][0] = wchunk[j].x;
-                    A[j][1] = wchunk[j].y;
-                    A[j][2] = wchunk[j].z;
-                    A[j][3] = wchunk[j].w;
+                for (int j = 0; j < NW; ++j) {
+                    const int nt = warp * NW + j;
+                    const uint32_t zb = tzp[((size_t)gl * NTILES + nt) * 8 + g8];
+                    kA[j] = (0x6400u | (zb & 15u)) * 0x10001u;
+                    kB[j] = (0xD400u | ((zb >> 4) << 4)) * 0x10001u;
                 }
             }
-            // B operands (activations): token column tile tt, token tt*8 + g8
-            uint32_t B[MT][2];
 #pragma unroll
-            for (int tt = 0; tt < MT; ++tt) {
-                const int tok = tt * 8 + g8;
-                if (tok < M) {
-                    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(a.qx + (size_t)tok * K + kg + tig * 8));
-                    B[tt][0] = v.x;
-                    B[tt][1] = v.y;
-                } else {
-                    B[tt][0] = 0u;
-                    B[tt][1] = 0u;
+            for (int s2 = 0; s2 < 2; ++s2) {  // the two 16-feature MMA steps
+                uint32_t A[NW][4];
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    if (FMT == HQ_W4_ASYM) {
+                        const uint32_t w = (c & 1) ? (s2 ? wchunk[j].w : wchunk[j].z) : (s2 ? wchunk[j].y : wchunk[j].x);
+                        widen_w4(w, kA[j], kB[j], A[j]);
+                    } else {
+                        widen_i8(s2 ? wchunk[j].z : wchunk[j].x, A[j][0], A[j][2]);
+                        widen_i8(s2 ? wchunk[j].w : wchunk[j].y, A[j][1], A[j][3]);
+                    }
+                }
+                const bool first = group_start && s2 == 0;
+#pragma unroll
+                for (int tt = 0; tt < MT; ++tt) {
+                    const uint32_t b0 = s2 ? bq[tt].z : bq[tt].x;
+                    const uint32_t b1 = s2 ? bq[tt].w : bq[tt].y;
+                    if (G == 16) {
+                        // two groups per step: lanes tig 0,1 hold the first 16 features
+                        const bool lowhalf = tig < 2;
+                        const uint32_t l0 = lowhalf ? b0 : 0u, l1 = lowhalf ? b1 : 0u;
+                        const uint32_t h0 = lowhalf ? 0u : b0, h1 = lowhalf ? 0u : b1;
+#pragma unroll
+                        for (int j = 0; j < NW; ++j) {
+                            if (first) {
+                                mma_f16_16816_z(acc[j][tt], A[j], l0, l1);
+                                mma_f16_16816_z(acc2[j][tt], A[j], h0, h1);
+                            } else {
+                                mma_f16_16816(acc[j][tt], A[j], l0, l1);
+                                mma_f16_16816(acc2[j][tt], A[j], h0, h1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NW; ++j) {
+                            if (first)
+                                mma_f16_16816_z(acc[j][tt], A[j], b0, b1);
+                            else
+                                mma_f16_16816(acc[j][tt], A[j], b0, b1);
+                        }
+                    }
                 }
             }
-            if (G == 16) {
-                // two groups per step: lanes tig 0,1 hold the first 16 features
-                int iacc2[NW][MT][4];
+            // end of a group: fold it into the fp32 sums
+            auto epilogue = [&](float(&ac)[NW][MT][4], int gl) {
+                const int gg = kt * C::GPT + gl;
 #pragma unroll
-                for (int j = 0; j < NW; ++j)
-#pragma unroll
-                    for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) iacc2[j][tt][e] = 0;
-                const bool lowhalf = tig < 2;
-#pragma unroll
-                for (int j = 0; j < NW; ++j)
+                for (int j = 0; j < NW; ++j) {
+                    const int nt = warp * NW + j;
+                    const float2 sc = *reinterpret_cast<const float2 *>(tsc + ((size_t)gl * NTILES + nt) * 16 + 2 * g8);
 #pragma unroll
                     for (int tt = 0; tt < MT; ++tt) {
-                        mma_s8_16832(iacc[j][tt], A[j][0], A[j][1], A[j][2], A[j][3], lowhalf ? B[tt][0] : 0u,
-                                     lowhalf ? B[tt][1] : 0u);
-                        mma_s8_16832(iacc2[j][tt], A[j][0], A[j][1], A[j][2], A[j][3], lowhalf ? 0u : B[tt][0],
-                                     lowhalf ? 0u : B[tt][1]);
+                        scale_add2(facc[j][tt][0], facc[j][tt][1], ac[j][tt][0], ac[j][tt][1], sc.x);
+                        scale_add2(facc[j][tt][2], facc[j][tt][3], ac[j][tt][2], ac[j][tt][3], sc.y);
+                        if (a.partials && gg < a.NGK) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int tok = tt * 8 + tig * 2 + (e & 1);
+                                const int n = b * BN + nt * 16 + g8 + 8 * (e >> 1);
+                                if (tok < M && n < N)
+                                    a.partials[((size_t)(a.m0 + tok) * N + n) * a.NGK + gg] =
+                                        __float2int_rn(ac[j][tt][e]);
+                            }
+                        }
                     }
-                group_epilogue<FMT, MT, NW>(a, iacc, facc, tsc, tzp, 2 * s, kt * C::GPT + 2 * s, b, warp, g8, tig);
-                group_epilogue<FMT, MT, NW>(a, iacc2, facc, tsc, tzp, 2 * s + 1, kt * C::GPT + 2 * s + 1, b, warp,
-                                            g8, tig);
-            } else {
-#pragma unroll
-                for (int j = 0; j < NW; ++j)
-#pragma unroll
-                    for (int tt = 0; tt < MT; ++tt)
-                        mma_s8_16832(iacc[j][tt], A[j][0], A[j][1], A[j][2], A[j][3], B[tt][0], B[tt][1]);
-                if (((s + 1) * 32) % G == 0) {
-                    const int gl = ((s + 1) * 32) / G - 1;
-                    group_epilogue<FMT, MT, NW>(a, iacc, facc, tsc, tzp, gl, kt * C::GPT + gl, b, warp, g8, tig);
                 }
+            };
+            if (G == 16) {
+                epilogue(acc, 2 * c);
+                epilogue(acc2, 2 * c + 1);
+            } else if (((c + 1) * 32) % G == 0) {
+                epilogue(acc, ((c + 1) * 32) / G - 1);
             }
         }
         // release the stage
@@ -305,7 +361,8 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
                             const int row = (warp * NW + j) * 16 + g8 + 8 * (e >> 1);
                             const int tok = tt * 8 + tig * 2 + (e & 1);
                             const int n = b * BN + row;
-                            if (tok < M && n < N) a.Y[(size_t)tok * N + n] = __fmul_rn(__ldg(a.sx + tok), facc[j][tt][e]);
+                            if (tok < M && n < N)
+                                Ym[(size_t)tok * N + n] = __fmul_rn(__ldg(sxm + tok), facc[j][tt][e]);
                         }
             } else {
                 // partial: publish, count arrivals, the last contributor finishes
@@ -331,17 +388,41 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
                 }
                 named_barrier(1, NCW * 32);
                 if (*s_flag) {
+                    // Sum the contributors' partials in ascending K order.  Each
+                    // thread owns 4 consecutive channels of one token and keeps
+                    // up to 8 contributors' 16-byte loads in flight at once.
                     __threadfence();
-                    for (int idx = threadIdx.x; idx < M * BN; idx += NCW * 32) {
-                        const int tok = idx / BN, row = idx - tok * BN;
-                        float sum = 0.0f;
-                        for (int cc = c_lo; cc <= c_hi; ++cc) {
-                            const int sl = (b == tile_begin(cc, a.T, a.grid) / KTILES) ? 0 : 1;
-                            sum = __fadd_rn(sum, __ldcg(wsp + ((size_t)cc * 2 + sl) * ws_slot_floats(M) +
-                                                        (size_t)tok * BN + row));
+                    for (int gi = threadIdx.x; gi < M * (BN / 4); gi += NCW * 32) {
+                        const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
+                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int cc = c_lo; cc <= c_hi; cc += 8) {
+                            float4 x[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const int c2 = cc + u;
+                                if (c2 <= c_hi) {
+                                    const int sl = (b == tile_begin(c2, a.T, a.grid) / KTILES) ? 0 : 1;
+                                    x[u] = __ldcg(reinterpret_cast<const float4 *>(
+                                        wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats(M) + (size_t)tok * BN + r4));
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                if (cc + u <= c_hi) {
+                                    sum.x = __fadd_rn(sum.x, x[u].x);
+                                    sum.y = __fadd_rn(sum.y, x[u].y);
+                                    sum.z = __fadd_rn(sum.z, x[u].z);
+                                    sum.w = __fadd_rn(sum.w, x[u].w);
+                                }
+                            }
                         }
-                        const int n = b * BN + row;
-                        if (n < N) a.Y[(size_t)tok * N + n] = __fmul_rn(__ldg(a.sx + tok), sum);
+                        const float sxt = __ldg(sxm + tok);
+                        const int n = b * BN + r4;
+                        float *yr = Ym + (size_t)tok * N;
+                        if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum.x);
+                        if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum.y);
+                        if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum.z);
+                        if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum.w);
                     }
                     if (threadIdx.x == 0) atomicExch(&ctr[b], 0);
                 }
@@ -349,16 +430,15 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT, NW>::THREADS) k_verify_gem
             }
         }
     }
-    (void)NGK;
 }
 
 // Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers
 // and a flag word.
-template <int FMT, int G, int MT, int NW>
+template <int FMT, int G, int MT>
 cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
-    using C = GemmCfg<FMT, G, MT, NW>;
-    auto kern = k_verify_gemm<FMT, G, MT, NW>;
-    const size_t smem = (size_t)a.stages * (size_t)a.tile_bytes + (size_t)a.stages * 16 + 16;
+    using C = GemmCfg<FMT, G, MT>;
+    auto kern = k_verify_gemm<FMT, G, MT>;
+    const size_t smem = (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16;
     static int configured_for = -1;  // device the attribute was last set for
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -381,14 +461,12 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Instances for one format: M buckets {<=8, <=16, <=32, <=64, <=128}.
+// Instances for one format: token buckets {<=8, <=16, <=32} per launch.
 template <int FMT, int G>
 cudaError_t launch_gemm_g(const GemmArgs &a, bool pdl, cudaStream_t s) {
-    if (a.M <= 8) return launch_gemm_instance<FMT, G, 1, 2>(a, pdl, s);
-    if (a.M <= 16) return launch_gemm_instance<FMT, G, 2, 2>(a, pdl, s);
-    if (a.M <= 32) return launch_gemm_instance<FMT, G, 4, 2>(a, pdl, s);
-    if (a.M <= 64) return launch_gemm_instance<FMT, G, 8, 1>(a, pdl, s);
-    return launch_gemm_instance<FMT, G, 16, 1>(a, pdl, s);
+    if (a.M <= 8) return launch_gemm_instance<FMT, G, 1>(a, pdl, s);
+    if (a.M <= 16) return launch_gemm_instance<FMT, G, 2>(a, pdl, s);
+    return launch_gemm_instance<FMT, G, 4>(a, pdl, s);
 }
 
 template <int FMT>

@@ -135,12 +135,19 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
         const int r0 = j * 16 + (t >> 2), r1 = r0 + 8, tig = t & 3;
         uint8_t out[16];
         if (w4) {
+            // word (c2, s2): features b = ch*64 + c2*32 + tig*8 + 4*s2 .. b+3;
+            // nibbles n0..n7 = (r0,b) (r1,b) (r0,b+2) (r1,b+2) (r0,b+1) (r1,b+1) (r0,b+3) (r1,b+3)
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const int kb = ch * 64 + s * 32 + tig * 8;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    out[8 * s + e] = (uint8_t)(codes_s[r0 * KT + kb + e] | (codes_s[r1 * KT + kb + e] << 4));
+            for (int wd = 0; wd < 4; ++wd) {
+                const int b = ch * 64 + (wd >> 1) * 32 + tig * 8 + 4 * (wd & 1);
+                const uint8_t *p0 = codes_s + r0 * KT + b, *p1 = codes_s + r1 * KT + b;
+                const uint32_t word = (uint32_t)p0[0] | ((uint32_t)p1[0] << 4) | ((uint32_t)p0[2] << 8) |
+                                      ((uint32_t)p1[2] << 12) | ((uint32_t)p0[1] << 16) | ((uint32_t)p1[1] << 20) |
+                                      ((uint32_t)p0[3] << 24) | ((uint32_t)p1[3] << 28);
+                out[4 * wd + 0] = (uint8_t)word;
+                out[4 * wd + 1] = (uint8_t)(word >> 8);
+                out[4 * wd + 2] = (uint8_t)(word >> 16);
+                out[4 * wd + 3] = (uint8_t)(word >> 24);
             }
         } else {
             const int kb = ch * 32 + tig * 8;
@@ -186,14 +193,20 @@ __global__ void __launch_bounds__(256) k_unpack(Geom g, const uint8_t *__restric
         const uint8_t *in = tile + (size_t)q * 16;
         const int n0 = b * BN + r0, n1 = b * BN + r1;
         for (int e = 0; e < 16; ++e) {
-            int k, cr0, cr1;
+            int k;
             if (w4) {
-                k = kt * g.KT + ch * 64 + (e / 8) * 32 + tig * 8 + (e % 8);
-                cr0 = in[e] & 15;
-                cr1 = in[e] >> 4;
-                if (k < g.K) {
-                    if (n0 < g.N) codes[(size_t)n0 * g.K + k] = (uint8_t)cr0;
-                    if (n1 < g.N) codes[(size_t)n1 * g.K + k] = (uint8_t)cr1;
+                if (e >= 4) continue;  // one 32-bit word per iteration
+                const int wd = e;
+                const uint32_t word = (uint32_t)in[4 * wd] | ((uint32_t)in[4 * wd + 1] << 8) |
+                                      ((uint32_t)in[4 * wd + 2] << 16) | ((uint32_t)in[4 * wd + 3] << 24);
+                const int b = kt * g.KT + ch * 64 + (wd >> 1) * 32 + tig * 8 + 4 * (wd & 1);
+                // nibble i -> (row, feature offset)
+                const int rowsel[8] = {0, 1, 0, 1, 0, 1, 0, 1};
+                const int foff[8] = {0, 0, 2, 2, 1, 1, 3, 3};
+                for (int nb = 0; nb < 8; ++nb) {
+                    const int kk = b + foff[nb];
+                    const int n = rowsel[nb] ? n1 : n0;
+                    if (kk < g.K && n < g.N) codes[(size_t)n * g.K + kk] = (uint8_t)((word >> (4 * nb)) & 15u);
                 }
             } else {
                 const int quarter = e / 4, off = e % 4;

@@ -30,7 +30,8 @@ HQ_MAX_M = 128
 FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 
 # Every symbol include/hq.h declares.
-EXPORTS = ("hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_make_signs",
+EXPORTS = ("hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
+           "hq_make_signs",
            "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
            "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc")
 
@@ -69,14 +70,15 @@ def load() -> ctypes.CDLL:
         "hq_version": (I32, []),
         "hq_packed_bytes": (SZ, [D]),
         "hq_workspace_bytes": (SZ, [D, I32]),
+        "hq_act_operand_bytes": (SZ, [I32, I32]),
         "hq_make_signs": (ctypes.c_int, [U64, I32, P]),
         "hq_pack_weights": (ctypes.c_int, [D, P, P, P, P]),
-        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, I32, P, P, P, P, U32, P]),
-        "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, P, I32, P, P, P, U32, P]),
+        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, P, P, P, P, U32, P]),
+        "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, I32, P, P, P, U32, P]),
         "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
         "hq_workspace_status": (ctypes.c_int, [P, P]),
         "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
-        "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, P, I32, P, P, U32, P]),
+        "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, I32, P, P, U32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -132,6 +134,10 @@ def hq_workspace_bytes(desc: hq_layer_desc, M: int) -> int:
     return int(load().hq_workspace_bytes(ctypes.byref(desc), int(M)))
 
 
+def hq_act_operand_bytes(M: int, K: int) -> int:
+    return int(load().hq_act_operand_bytes(int(M), int(K)))
+
+
 def hq_make_signs(seed: int, K: int) -> np.ndarray:
     out = np.zeros(max(K // 32, 1), dtype=np.uint32)
     _check(load().hq_make_signs(ctypes.c_uint64(seed & (2 ** 64 - 1)), int(K), out.ctypes.data), "hq_make_signs")
@@ -143,13 +149,13 @@ def hq_pack_weights(desc, W, signs, blob, stream=None) -> None:
            "hq_pack_weights")
 
 
-def hq_rotate_quant_act(X, M: int, K: int, group: int, signs, qx, sx, gsum, flags: int = 0, stream=None) -> None:
-    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), int(group), _ptr(signs), _ptr(qx), _ptr(sx),
-                                      _ptr(gsum), int(flags), _stream(stream)), "hq_rotate_quant_act")
+def hq_rotate_quant_act(X, M: int, K: int, signs, qx, qop, sx, flags: int = 0, stream=None) -> None:
+    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), _ptr(signs), _ptr(qx), _ptr(qop), _ptr(sx),
+                                      int(flags), _stream(stream)), "hq_rotate_quant_act")
 
 
-def hq_verify_gemm(desc, blob, qx, sx, gsum, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
-    _check(load().hq_verify_gemm(ctypes.byref(desc), _ptr(blob), _ptr(qx), _ptr(sx), _ptr(gsum), int(M), _ptr(Y),
+def hq_verify_gemm(desc, blob, qop, sx, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
+    _check(load().hq_verify_gemm(ctypes.byref(desc), _ptr(blob), _ptr(qop), _ptr(sx), int(M), _ptr(Y),
                                  _ptr(partials), _ptr(workspace), int(flags), _stream(stream)), "hq_verify_gemm")
 
 
@@ -170,9 +176,9 @@ def hq_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
 HQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 64 * 1024
 
 
-def hq_verify_gemm_noalloc(desc, blob, qx, sx, gsum, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:
+def hq_verify_gemm_noalloc(desc, blob, qop, sx, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:
     """hq_verify_gemm with the library's fixed device scratch array instead of a workspace."""
-    rc = load().hq_verify_gemm_noalloc(ctypes.byref(desc), _ptr(blob), _ptr(qx), _ptr(sx), _ptr(gsum), int(M), _ptr(Y),
+    rc = load().hq_verify_gemm_noalloc(ctypes.byref(desc), _ptr(blob), _ptr(qop), _ptr(sx), int(M), _ptr(Y),
                                        _ptr(partials), int(flags), _stream(stream))
     if rc == HQ_ERR_UNSUPPORTED:
         need = hq_workspace_bytes(desc, M)
@@ -219,11 +225,23 @@ def pack_layer(W: torch.Tensor, group: int, fmt, signs_host: np.ndarray, stream=
     return PackedLayer(desc, blob, signs)
 
 
-def act_buffers(M: int, K: int, group: int, device) -> tuple:
-    qx = torch.empty((M, K), dtype=torch.int8, device=device)
+def act_buffers(M: int, K: int, device, int8_codes: bool = True) -> tuple:
+    """(qx int8 [M][K] or None, GEMM activation operand (uint8 bytes), sx fp32 [M])."""
+    qx = torch.empty((M, K), dtype=torch.int8, device=device) if int8_codes else None
+    qop = torch.empty(hq_act_operand_bytes(M, K), dtype=torch.uint8, device=device)
     sx = torch.empty(M, dtype=torch.float32, device=device)
-    gsum = torch.empty((M, K // group), dtype=torch.int32, device=device)
-    return qx, sx, gsum
+    return qx, qop, sx
+
+
+def decode_act_operand(qop: np.ndarray, M: int, K: int) -> np.ndarray:
+    """The GEMM activation operand as fp16 codes [M][K] (layout in include/hq.h)."""
+    nb = (K + 127) // 128
+    a = np.asarray(qop, dtype=np.uint8).view(np.float16).reshape(nb, M, 16, 8)
+    out = np.empty((M, nb * 128), dtype=np.float16)
+    for m in range(M):
+        chunks = np.arange(16) ^ (4 * (m & 1))
+        out[m] = a[:, m, chunks, :].reshape(nb * 128)
+    return out[:, :K]
 
 
 def workspace(desc: hq_layer_desc, M: int, device) -> torch.Tensor:
@@ -248,10 +266,10 @@ def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torc
     """Y = dequant(int GEMM(quant(rotate(X)), packed W)): the two kernels in sequence."""
     M, K = X.shape
     if bufs is None:
-        bufs = act_buffers(M, K, layer.group, X.device)
-    qx, sx, gsum = bufs
+        bufs = act_buffers(M, K, X.device, int8_codes=False)
+    qx, qop, sx = bufs
     if Y is None:
         Y = torch.empty((M, layer.N), dtype=torch.float32, device=X.device)
-    hq_rotate_quant_act(X, M, K, layer.group, layer.signs, qx, sx, gsum, flags, stream)
-    hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, M, Y, partials, ws, flags, stream)
+    hq_rotate_quant_act(X, M, K, layer.signs, qx, qop, sx, flags, stream)
+    hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, partials, ws, flags, stream)
     return Y

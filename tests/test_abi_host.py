@@ -86,10 +86,18 @@ def test_invalid_desc_has_no_size(K, N, G, fmt):
     assert hq.hq_workspace_bytes(d, 16) == 0
 
 
+def test_act_operand_bytes():
+    assert hq.hq_act_operand_bytes(16, 4096) == 16 * 32 * 256
+    assert hq.hq_act_operand_bytes(3, 96) == 3 * 1 * 256  # padded to a 128-feature block
+    assert hq.hq_act_operand_bytes(0, 4096) == 0
+    assert hq.hq_act_operand_bytes(129, 4096) == 0 and hq.hq_act_operand_bytes(4, 100) == 0
+
+
 def test_workspace_bytes():
     d = hq.make_desc(4096, 4096, 64, "w4")
     assert hq.hq_workspace_bytes(d, 16) > hq.hq_workspace_bytes(d, 1) > 0
     assert hq.hq_workspace_bytes(d, 129) == 0 and hq.hq_workspace_bytes(d, -1) == 0
+    assert hq.hq_workspace_bytes(d, 128) == hq.hq_workspace_bytes(d, 32)  # at most 32 rows per launch
     assert hq.hq_workspace_bytes(d, 16) % 16 == 0
 
 
@@ -108,22 +116,23 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert lib.hq_pack_weights(D, None, FAKE, FAKE, None) == E
     assert lib.hq_pack_weights(D, FAKE, FAKE, FAKE + 8, None) == E  # blob must be 16-byte aligned
     # activations
-    assert lib.hq_rotate_quant_act(FAKE, 129, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, -1, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 100, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 96, 64, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 48, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(None, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, FAKE, FAKE, 2, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 129, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, -1, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 100, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(None, 4, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, None, None, FAKE, 0, None) == E  # no output at all
+    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, FAKE, FAKE + 8, FAKE, 0, None) == E  # operand alignment
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, FAKE, FAKE, FAKE, 2, None) == E
     # gemm
-    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 129, FAKE, None, FAKE, 0, None) == E
-    assert lib.hq_verify_gemm(D, None, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
-    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, None, 4, FAKE, None, FAKE, 0, None) == E  # W4 needs gsum
-    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, None, 0, None) == E  # workspace
-    assert lib.hq_verify_gemm(D, FAKE + 8, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
-    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 8, None) == E
-    assert lib.hq_verify_gemm(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 129, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, None, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, None, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, None, 0, None) == E  # workspace
+    assert lib.hq_verify_gemm(D, FAKE + 8, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE + 8, FAKE, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 8, None) == E
+    assert lib.hq_verify_gemm(ctypes.byref(bad), FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     # unpack / status / self-test
     assert lib.hq_unpack_codes(D, FAKE, FAKE, FAKE, None, None) == E  # W4 needs zeros
     assert lib.hq_workspace_status(None, None) == E
@@ -135,5 +144,5 @@ def test_empty_batch_is_a_no_op():
     lib = hq.load()
     d = hq.make_desc(256, 256, 32, "w4")
     # M = 0: nothing to do, nothing launched, pointers never touched
-    assert lib.hq_rotate_quant_act(None, 0, 256, 32, None, None, None, None, 0, None) == hq.HQ_OK
-    assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_rotate_quant_act(None, 0, 256, None, None, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK

@@ -61,12 +61,25 @@ def assert_close(y, ref_out):
     assert strict.mean() >= STRICT_FRACTION, f"only {strict.mean():.5f} within the elementwise tolerance"
 
 
-def gpu_act(X, G, signs_dev):
+def gpu_act(X, signs_dev):
     M, K = X.shape
-    qx, sx, gsum = hq.act_buffers(M, K, G, DEV)
-    hq.hq_rotate_quant_act(X, M, K, G, signs_dev, qx, sx, gsum)
+    qx, qop, sx = hq.act_buffers(M, K, DEV)
+    qop.fill_(0xFF)  # padding must be written, not left over
+    hq.hq_rotate_quant_act(X, M, K, signs_dev, qx, qop, sx)
     torch.cuda.synchronize()
-    return qx, sx, gsum
+    return qx, qop, sx
+
+
+def check_act(qx, qop, sx, rq, rs):
+    M, K = rq.shape
+    assert np.array_equal(qx.cpu().numpy(), rq)
+    # the GEMM operand holds the same integers as fp16, exactly, and zeros past K
+    op = qop.cpu().numpy()
+    assert np.array_equal(hq.decode_act_operand(op, M, K).astype(np.float64), rq.astype(np.float64))
+    nb = (K + 127) // 128
+    full = hq.decode_act_operand(op, M, nb * 128)
+    assert not full[:, K:].astype(np.float64).any()
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
 
 
 def signs_pair(seed, K):
@@ -83,11 +96,9 @@ ACT_CASES = [(1, 32, 32), (3, 64, 16), (16, 256, 32), (17, 256, 64), (16, 4096, 
 def test_rotate_quant_act_bit_exact(M, K, G):
     X = synth.activations(M, K, seed=M * 7 + K, outlier_channels=min(2, K), heavy_frac=0.01)
     s_host, s_dev = signs_pair(M + K, K)
-    qx, sx, gsum = gpu_act(X.to(DEV), G, s_dev)
-    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
-    assert np.array_equal(qx.cpu().numpy(), rq)
-    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
-    assert np.array_equal(gsum.cpu().numpy(), rg)
+    qx, qop, sx = gpu_act(X.to(DEV), s_dev)
+    rq, rs, _ = oracle.quant_act(X.numpy(), G, s_host)
+    check_act(qx, qop, sx, rq, rs)
 
 
 def test_rotate_quant_act_degenerate_rows():
@@ -100,11 +111,9 @@ def test_rotate_quant_act_degenerate_rows():
     X[4, :32] = 3.0                  # constant block
     X[5] = 1e30                      # huge values
     s_host, s_dev = signs_pair(9, K)
-    qx, sx, gsum = gpu_act(X.to(DEV), G, s_dev)
-    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
-    assert np.array_equal(qx.cpu().numpy(), rq)
-    assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
-    assert np.array_equal(gsum.cpu().numpy(), rg)
+    qx, qop, sx = gpu_act(X.to(DEV), s_dev)
+    rq, rs, _ = oracle.quant_act(X.numpy(), G, s_host)
+    check_act(qx, qop, sx, rq, rs)
     assert sx[1].item() == 0.0 and not qx[1].any()
 
 
@@ -114,7 +123,7 @@ def test_rotate_quant_act_nan_does_not_crash():
     X[0, 3] = float("nan")
     X[1, 9] = float("inf")
     _, s_dev = signs_pair(1, K)
-    gpu_act(X.to(DEV), G, s_dev)  # values unspecified; it must return
+    gpu_act(X.to(DEV), s_dev)  # values unspecified; it must return
 
 
 # ----------------------------------------------------------- packing ---
@@ -154,7 +163,7 @@ def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     if layer is None:
         layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
     ws = hq.workspace(layer.desc, M, DEV)
-    bufs = hq.act_buffers(M, K, G, DEV)
+    bufs = hq.act_buffers(M, K, DEV)
     P = torch.empty((M, layer.N, K // G), dtype=torch.int32, device=DEV) if check else None
     Y = hq.verify_linear(layer, X.to(DEV), ws, bufs=bufs, partials=P, flags=flags)
     assert hq.hq_workspace_status(ws) == hq.HQ_OK

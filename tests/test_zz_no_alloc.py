@@ -28,17 +28,20 @@ def test_noalloc_refuses_calls_larger_than_its_array():
     lib = hq.load()
     d = hq.make_desc(4096, 4096, 64, "w4")
     fake = 0x10000  # never dereferenced: the size check comes first
-    assert hq.hq_workspace_bytes(d, 33) > hq.HQ_NOALLOC_SCRATCH_BYTES
-    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(d), fake, fake, fake, fake, 33, fake, None, 0, None)
+    # every M fits (the GEMM runs at most 32 rows per launch); a huge N does not
+    assert hq.hq_workspace_bytes(d, 128) <= hq.HQ_NOALLOC_SCRATCH_BYTES
+    wide = hq.make_desc(4096, 128 * 20000, 64, "w4")
+    assert hq.hq_workspace_bytes(wide, 32) > hq.HQ_NOALLOC_SCRATCH_BYTES
+    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(wide), fake, fake, fake, 32, fake, None, 0, None)
     assert rc == hq.HQ_ERR_UNSUPPORTED
-    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, fake, fake, fake, 16, fake, None, 0, None)
+    rc = lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, fake, fake, 16, fake, None, 0, None)
     assert rc == hq.HQ_ERR_INVALID_ARG
-    assert lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, None, None, None, 0, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_verify_gemm_noalloc(ctypes.byref(d), None, None, None, 0, None, None, 0, None) == hq.HQ_OK
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("fmt,M,K,N,G", [("w4", 16, 4096, 1024, 64), ("w8", 32, 4096, 384, 128),
-                                         ("w4", 5, 512, 200, 32)])
+                                         ("w4", 5, 512, 200, 32), ("w4", 70, 1024, 256, 64)])
 def test_noalloc_matches_workspace_entry_point_twice(fmt, M, K, N, G):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -47,16 +50,16 @@ def test_noalloc_matches_workspace_entry_point_twice(fmt, M, K, N, G):
     W = synth.weights(N, K, seed=N + 5).to(dev)
     signs = hq.hq_make_signs(17, K)
     layer = hq.pack_layer(W, G, fmt, signs)
-    qx, sx, gsum = hq.act_buffers(M, K, G, dev)
-    hq.hq_rotate_quant_act(X, M, K, G, layer.signs, qx, sx, gsum)
+    _, qop, sx = hq.act_buffers(M, K, dev, int8_codes=False)
+    hq.hq_rotate_quant_act(X, M, K, layer.signs, None, qop, sx)
     ws = hq.workspace(layer.desc, M, dev)
     y_ref = torch.empty((M, N), dtype=torch.float32, device=dev)
-    hq.hq_verify_gemm(layer.desc, layer.blob, qx, sx, gsum, M, y_ref, None, ws)
+    hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, y_ref, None, ws)
     assert hq.hq_workspace_status(ws) == hq.HQ_OK
     ref = y_ref.cpu().numpy().astype(np.float64)
     for call in range(2):
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
-        hq.hq_verify_gemm_noalloc(layer.desc, layer.blob, qx, sx, gsum, M, y)
+        hq.hq_verify_gemm_noalloc(layer.desc, layer.blob, qop, sx, M, y)
         torch.cuda.synchronize()
         got = y.cpu().numpy().astype(np.float64)
         assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref)), f"call {call + 1} differs"
