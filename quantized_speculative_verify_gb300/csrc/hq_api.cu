@@ -61,13 +61,13 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.NGK = g.NGK;
     a.KTILES = g.KTILES;
     a.T = g.NB * g.KTILES;
-    // Two thread blocks per SM (eight consumer warps) keep enough loads and
-    // tensor-core steps in flight; each block's stage ring is about 64 KB.
+    // Three thread blocks per SM (twelve consumer warps) keep enough loads and
+    // tensor-core steps in flight; each block's stage ring is about 60 KB.
     // Small layers get fewer blocks so that every block streams at least
     // MIN_TILES tiles and an n-block is split between few blocks (the last
     // one to finish sums the others' partial sums).
     constexpr int MIN_TILES = 4;
-    int grid = 2 * sms;
+    int grid = 3 * sms;
     if (grid > a.T / MIN_TILES) grid = a.T / MIN_TILES;
     if (grid < 1) grid = 1;
     if (grid > MAX_CTAS) grid = MAX_CTAS;
@@ -80,8 +80,9 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     for (int m0 = 0; m0 < M; m0 += MAX_M_LAUNCH) {
         a.m0 = m0;
         a.M = M - m0 < MAX_M_LAUNCH ? M - m0 : MAX_M_LAUNCH;
-        a.act_bytes = a.M * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
-        int stages = (64 * 1024) / (g.tile_bytes + a.act_bytes);
+        const int mrows = a.M <= 8 ? 8 : a.M <= 16 ? 16 : 32;  // staged activation rows (zero past M)
+        a.act_bytes = mrows * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
+        int stages = (60 * 1024) / (g.tile_bytes + a.act_bytes);
         if (stages < 2) stages = 2;
         if (stages > 16) stages = 16;
         a.stages = stages;

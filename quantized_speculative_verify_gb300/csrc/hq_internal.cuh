@@ -149,14 +149,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Test the phase; a thread whose phase is not complete may be suspended by
+// the hardware until it completes (or for at most ~1 ms, the hint), instead
+// of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -171,7 +174,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     uint32_t it = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((++it & 255u) == 0u && global_timer_ns() - t0 > limit_ns) {
+        if ((++it & 15u) == 0u && global_timer_ns() - t0 > limit_ns) {
             if (err) atomicExch(err, DEV_ERR_TIMEOUT);
             return false;
         }

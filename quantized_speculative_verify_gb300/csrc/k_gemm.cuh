@@ -119,6 +119,7 @@ __device__ __forceinline__ void scale_add2(float &f0, float &f1, float a0, float
 
 template <int FMT, int G, int MT>
 struct GemmCfg {
+    static constexpr int MROWS = 8 * MT;          // activation rows staged per block (zero past M)
     static constexpr int NW = 2;                  // row tiles per consumer warp
     static constexpr int KT = G > 128 ? G : 128;  // features per tile
     static constexpr int STEPS = KT / 32;         // 32-feature steps per tile
@@ -127,13 +128,16 @@ struct GemmCfg {
     static constexpr int THREADS = (NCW + 1) * 32;
 };
 
-template <int FMT, int G, int MT>
+// CHECK: also write the exact integer partial sums (check mode).
+template <int FMT, int G, int MT, bool CHECK>
 __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(const GemmArgs a) {
     using C = GemmCfg<FMT, G, MT>;
-    constexpr int KT = C::KT, NCW = C::NCW, NW = C::NW, STEPS = C::STEPS;
+    constexpr int KT = C::KT, NCW = C::NCW, NW = C::NW;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = a.stages;
-    const int stage_bytes = a.tile_bytes + a.act_bytes;
+    const int stage_bytes = a.tile_bytes + a.act_bytes;  // shared-memory footprint of a stage
+    // bytes that land in a stage: the weight tile and M rows of each 128-feature activation block
+    const uint32_t tx_bytes = (uint32_t)a.tile_bytes + (uint32_t)a.M * 256u * (uint32_t)(C::KT / 128);
     uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);  // full[S], empty[S]
     int *s_flag = reinterpret_cast<int *>(bars + 2 * S);
@@ -151,6 +155,17 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
         }
         fence_mbar_init();
     }
+    if (a.M < C::MROWS) {
+        // activation rows past M are never copied: keep them zero so the B
+        // operand loads need no bounds check
+        const int pad = (C::MROWS - a.M) * 256 / 16;
+        for (int st = 0; st < S; ++st)
+            for (int kk = 0; kk < KT / 128; ++kk) {
+                uint4 *dst = reinterpret_cast<uint4 *>(ring + (size_t)st * stage_bytes + a.tile_bytes +
+                                                       (size_t)kk * C::MROWS * 256 + (size_t)a.M * 256);
+                for (int q = threadIdx.x; q < pad; q += blockDim.x) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+    }
     __syncthreads();
     pdl_launch_dependents();
 
@@ -162,6 +177,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
             const int KTILES = a.KTILES;
             const int blocks = KT / 128;
             const uint32_t row_bytes = (uint32_t)a.M * 256;  // one 128-feature activation block of this launch
+            const uint32_t region_bytes = (uint32_t)C::MROWS * 256;
             // activation blocks of the i-th tile of this thread block -> its stage
             auto copy_acts = [&](int i, int st) {
                 const int kb = ((t0 + i) % KTILES) * blocks;
@@ -169,14 +185,14 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                 const uint32_t dst = smem_addr(ring + (size_t)st * stage_bytes + a.tile_bytes);
                 const uint32_t fb = smem_addr(&bars[st]);
                 for (int kk = 0; kk < blocks; ++kk)
-                    bulk_copy_g2s(dst + kk * row_bytes, src + (size_t)kk * a.M_total * 256, row_bytes, fb, pol_a);
+                    bulk_copy_g2s(dst + kk * region_bytes, src + (size_t)kk * a.M_total * 256, row_bytes, fb, pol_a);
             };
             int i = 0;
             // Weights never depend on earlier kernels of the stream: the first
             // stages' weight copies go out before waiting for them.
             for (; i < ntl && i < S; ++i) {
                 const uint32_t fb = smem_addr(&bars[i]);
-                mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+                mbar_arrive_expect_tx(fb, tx_bytes);
                 bulk_copy_g2s(smem_addr(ring + (size_t)i * stage_bytes),
                               a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
             }
@@ -187,7 +203,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                 const uint32_t ph = (uint32_t)((i / S) & 1);
                 if (!mbar_wait_bounded(smem_addr(&bars[S + st]), ph ^ 1u, err)) break;
                 const uint32_t fb = smem_addr(&bars[st]);
-                mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+                mbar_arrive_expect_tx(fb, tx_bytes);
                 bulk_copy_g2s(smem_addr(ring + (size_t)st * stage_bytes),
                               a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
                 copy_acts(i, st);
@@ -208,18 +224,28 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
     int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
     const float *sxm = a.sx + a.m0;
     float *Ym = a.Y + (size_t)a.m0 * N;
+    // byte offsets of this lane's B operand rows (token tt*8 + g8) in a stage
+    uint32_t boff[MT];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) boff[tt] = (uint32_t)(tt * 8 + g8) * 256u;
 
     float acc[NW][MT][4], acc2[NW][MT][4];
     float facc[NW][MT][4];
-    int seg_k0 = 0;
     bool ok = true;
+    // n-blocks whose partial sums this block published: its first n-block
+    // (slot 0) and its last one (slot 1)
+    int pend0 = -1, pend1 = -1;
+    const int first_b = t0 / KTILES;
+
+    // running position: tile t0 + i is n-block b, K tile kt, in stage st of phase ph
+    int b = t0 / KTILES, kt = t0 - b * KTILES, st = 0;
+    uint32_t ph = 0;
+    int seg_k0 = kt;
 
     // A failed (timed-out) wait is sticky: the warp stops waiting but keeps
     // the same control flow, so every consumer warp still reaches each named
     // barrier and every arrival counter is still incremented and reset.
     for (int i = 0; i < ntl; ++i) {
-        const int t = t0 + i;
-        const int b = t / KTILES, kt = t - b * KTILES;
         if (i == 0 || kt == 0) {
             seg_k0 = kt;
 #pragma unroll
@@ -229,8 +255,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
 #pragma unroll
                     for (int e = 0; e < 4; ++e) facc[j][tt][e] = 0.0f;
         }
-        const int st = i % S;
-        if (ok) ok = mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((i / S) & 1), err);
+        if (ok) ok = mbar_wait_bounded(smem_addr(&bars[st]), ph, err);
         const uint8_t *tile = ring + (size_t)st * stage_bytes;
         const uint8_t *acts = tile + a.tile_bytes;
         const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);
@@ -239,15 +264,13 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
         uint4 wchunk[NW];
         uint32_t kA[NW], kB[NW];  // zero-point constants of the lane's current group (4-bit format)
 #pragma unroll
-        for (int c = 0; c < STEPS; ++c) {
+        for (int c = 0; c < C::STEPS; ++c) {
             // B operands: 8 fp16 activation codes of token tt*8 + g8, features c*32 + tig*8 .. +7
             uint4 bq[MT];
 #pragma unroll
             for (int tt = 0; tt < MT; ++tt) {
-                const int tok = tt * 8 + g8;
-                const int q = ((c & 3) * 4 + tig) ^ ((tok & 1) << 2);  // swizzled 16-byte chunk
-                bq[tt] = tok < M ? *reinterpret_cast<const uint4 *>(acts + ((size_t)((c >> 2) * M + tok) * 256 + q * 16))
-                                 : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t q = (uint32_t)(((c & 3) * 4 + tig) ^ (((tt * 8 + g8) & 1) << 2));  // swizzled chunk
+                bq[tt] = *reinterpret_cast<const uint4 *>(acts + (size_t)(c >> 2) * C::MROWS * 256 + boff[tt] + q * 16);
             }
             // A operands: the lane's 16-byte weight chunk (64 features for 4-bit, 32 for 8-bit)
             if (FMT == HQ_W8_SYM || (c & 1) == 0) {
@@ -315,7 +338,6 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
             }
             // end of a group: fold it into the fp32 sums
             auto epilogue = [&](float(&ac)[NW][MT][4], int gl) {
-                const int gg = kt * C::GPT + gl;
 #pragma unroll
                 for (int j = 0; j < NW; ++j) {
                     const int nt = warp * NW + j;
@@ -324,14 +346,17 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                     for (int tt = 0; tt < MT; ++tt) {
                         scale_add2(facc[j][tt][0], facc[j][tt][1], ac[j][tt][0], ac[j][tt][1], sc.x);
                         scale_add2(facc[j][tt][2], facc[j][tt][3], ac[j][tt][2], ac[j][tt][3], sc.y);
-                        if (a.partials && gg < a.NGK) {
+                        if (CHECK) {
+                            const int gg = kt * C::GPT + gl;
+                            if (gg < a.NGK) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int tok = tt * 8 + tig * 2 + (e & 1);
-                                const int n = b * BN + nt * 16 + g8 + 8 * (e >> 1);
-                                if (tok < M && n < N)
-                                    a.partials[((size_t)(a.m0 + tok) * N + n) * a.NGK + gg] =
-                                        __float2int_rn(ac[j][tt][e]);
+                                for (int e = 0; e < 4; ++e) {
+                                    const int tok = tt * 8 + tig * 2 + (e & 1);
+                                    const int n = b * BN + nt * 16 + g8 + 8 * (e >> 1);
+                                    if (tok < M && n < N)
+                                        a.partials[((size_t)(a.m0 + tok) * N + n) * a.NGK + gg] =
+                                            __float2int_rn(ac[j][tt][e]);
+                                }
                             }
                         }
                     }
@@ -350,8 +375,8 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
 
         // end of an n-block segment?
         if (kt == KTILES - 1 || i == ntl - 1) {
-            const bool whole = seg_k0 == 0 && kt == KTILES - 1;
-            if (whole) {
+            if (seg_k0 == 0 && kt == KTILES - 1) {
+                // the whole K range of the n-block: write Y
 #pragma unroll
                 for (int j = 0; j < NW; ++j)
 #pragma unroll
@@ -365,8 +390,9 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                                 Ym[(size_t)tok * N + n] = __fmul_rn(__ldg(sxm + tok), facc[j][tt][e]);
                         }
             } else {
-                // partial: publish, count arrivals, the last contributor finishes
-                const int slot = (b == tile_begin(blockIdx.x, a.T, a.grid) / KTILES) ? 0 : 1;
+                // part of the K range: publish the partial sums now, count the
+                // arrival once this block's tiles are all done
+                const int slot = b == first_b ? 0 : 1;
                 float *mys = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats(M);
 #pragma unroll
                 for (int j = 0; j < NW; ++j)
@@ -378,66 +404,104 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                             const int tok = tt * 8 + tig * 2 + (e & 1);
                             if (tok < M) __stcg(mys + (size_t)tok * BN + row, facc[j][tt][e]);
                         }
-                __threadfence();
-                named_barrier(1, NCW * 32);
-                const int c_lo = cta_of_tile(b * KTILES, a.T, a.grid);
-                const int c_hi = cta_of_tile(b * KTILES + KTILES - 1, a.T, a.grid);
-                if (threadIdx.x == 0) {
-                    const int prev = atomicAdd(&ctr[b], 1);
-                    *s_flag = (prev == c_hi - c_lo) ? 1 : 0;
-                }
-                named_barrier(1, NCW * 32);
-                if (*s_flag) {
-                    // Sum the contributors' partials in ascending K order.  Each
-                    // thread owns 4 consecutive channels of one token and keeps
-                    // up to 8 contributors' 16-byte loads in flight at once.
-                    __threadfence();
-                    for (int gi = threadIdx.x; gi < M * (BN / 4); gi += NCW * 32) {
-                        const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
-                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int cc = c_lo; cc <= c_hi; cc += 8) {
-                            float4 x[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const int c2 = cc + u;
-                                if (c2 <= c_hi) {
-                                    const int sl = (b == tile_begin(c2, a.T, a.grid) / KTILES) ? 0 : 1;
-                                    x[u] = __ldcg(reinterpret_cast<const float4 *>(
-                                        wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats(M) + (size_t)tok * BN + r4));
-                                }
-                            }
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                if (cc + u <= c_hi) {
-                                    sum.x = __fadd_rn(sum.x, x[u].x);
-                                    sum.y = __fadd_rn(sum.y, x[u].y);
-                                    sum.z = __fadd_rn(sum.z, x[u].z);
-                                    sum.w = __fadd_rn(sum.w, x[u].w);
-                                }
-                            }
-                        }
-                        const float sxt = __ldg(sxm + tok);
-                        const int n = b * BN + r4;
-                        float *yr = Ym + (size_t)tok * N;
-                        if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum.x);
-                        if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum.y);
-                        if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum.z);
-                        if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum.w);
-                    }
-                    if (threadIdx.x == 0) atomicExch(&ctr[b], 0);
-                }
-                named_barrier(1, NCW * 32);
+                if (slot == 0)
+                    pend0 = b;
+                else
+                    pend1 = b;
             }
+        }
+        // advance the running position
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (++kt == KTILES) {
+            kt = 0;
+            ++b;
+        }
+    }
+
+    // Arrivals: the last contributor of an n-block sums every contributor's
+    // partial sums in ascending K order (slot 0 of a block's contributor is its
+    // first segment, slot 1 its last), multiplies by the row scale and writes Y.
+    if (pend0 >= 0 || pend1 >= 0) {
+        __threadfence();
+        named_barrier(1, NCW * 32);
+        if (threadIdx.x == 0) {
+            int flags = 0;
+            for (int p = 0; p < 2; ++p) {
+                const int bb = p == 0 ? pend0 : pend1;
+                if (bb < 0) continue;
+                const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
+                const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
+                if (atomicAdd(&ctr[bb], 1) == c_hi - c_lo) flags |= 1 << p;
+            }
+            *s_flag = flags;
+        }
+        named_barrier(1, NCW * 32);
+        const int flags = *s_flag;
+        if (flags) __threadfence();
+        for (int p = 0; p < 2; ++p) {
+            if (!(flags & (1 << p))) continue;
+            const int bb = p == 0 ? pend0 : pend1;
+            const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
+            const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
+            // each thread: up to 4 groups of 4 channels x up to 8 contributors in flight
+            for (int g0 = threadIdx.x; g0 < M * (BN / 4); g0 += 4 * NCW * 32) {
+                float4 sum[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cc = c_lo; cc <= c_hi; cc += 4) {
+                    float4 x[4][4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int c2 = cc + v;
+                        const int sl = (bb == tile_begin(c2, a.T, a.grid) / KTILES) ? 0 : 1;
+                        const float *base = wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats(M);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int gi = g0 + u * NCW * 32;
+                            if (c2 <= c_hi && gi < M * (BN / 4))
+                                x[u][v] = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)gi * 4));
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (cc + v > c_hi) break;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            sum[u].x = __fadd_rn(sum[u].x, x[u][v].x);
+                            sum[u].y = __fadd_rn(sum[u].y, x[u][v].y);
+                            sum[u].z = __fadd_rn(sum[u].z, x[u][v].z);
+                            sum[u].w = __fadd_rn(sum[u].w, x[u][v].w);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int gi = g0 + u * NCW * 32;
+                    if (gi >= M * (BN / 4)) continue;
+                    const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
+                    const float sxt = __ldg(sxm + tok);
+                    const int n = bb * BN + r4;
+                    float *yr = Ym + (size_t)tok * N;
+                    if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum[u].x);
+                    if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum[u].y);
+                    if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum[u].z);
+                    if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum[u].w);
+                }
+            }
+            if (threadIdx.x == 0) atomicExch(&ctr[bb], 0);
         }
     }
 }
 
 // Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers
 // and a flag word.
-template <int FMT, int G, int MT>
+template <int FMT, int G, int MT, bool CHECK>
 cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     using C = GemmCfg<FMT, G, MT>;
-    auto kern = k_verify_gemm<FMT, G, MT>;
+    auto kern = k_verify_gemm<FMT, G, MT, CHECK>;
     const size_t smem = (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16;
     static int configured_for = -1;  // device the attribute was last set for
     int dev = 0;
@@ -464,9 +528,14 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
 // Instances for one format: token buckets {<=8, <=16, <=32} per launch.
 template <int FMT, int G>
 cudaError_t launch_gemm_g(const GemmArgs &a, bool pdl, cudaStream_t s) {
-    if (a.M <= 8) return launch_gemm_instance<FMT, G, 1>(a, pdl, s);
-    if (a.M <= 16) return launch_gemm_instance<FMT, G, 2>(a, pdl, s);
-    return launch_gemm_instance<FMT, G, 4>(a, pdl, s);
+    if (a.partials) {
+        if (a.M <= 8) return launch_gemm_instance<FMT, G, 1, true>(a, pdl, s);
+        if (a.M <= 16) return launch_gemm_instance<FMT, G, 2, true>(a, pdl, s);
+        return launch_gemm_instance<FMT, G, 4, true>(a, pdl, s);
+    }
+    if (a.M <= 8) return launch_gemm_instance<FMT, G, 1, false>(a, pdl, s);
+    if (a.M <= 16) return launch_gemm_instance<FMT, G, 2, false>(a, pdl, s);
+    return launch_gemm_instance<FMT, G, 4, false>(a, pdl, s);
 }
 
 template <int FMT>
