@@ -3,9 +3,12 @@
 
 One step = one verify pass of a 9B-class decoder over M = 16 draft-tree
 tokens: for each of 32 layers the q, k, v, o, fused gate+up and down
-projections, then the LM head -- every linear runs the activation rotation +
-int8 quantization kernel and the W4A8 GEMM kernel of libhq.so (4-bit
-asymmetric weights, group 64).  The pass streams 3.875 GB of packed weights,
+projections, then the LM head -- every activation input runs the rotation +
+int8 quantization kernel once and every linear the W4A8 GEMM kernel of
+libhq.so (4-bit asymmetric weights, group 64).  q, k and v read the same
+input; by default their weights are packed as one [6144][4096] matrix and
+run as one GEMM (the same arithmetic, fewer launches; --no-fuse-qkv runs
+three).  The pass streams 3.875 GB of packed weights,
 far more than the 129 MB L2, so every pass reads its weights from HBM.
 
 Reported (one JSON line on rank 0):
@@ -48,7 +51,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
-    p.add_argument("--fuse-qkv", action="store_true", help="pack q, k, v of a layer as one [6144][4096] weight")
+    p.add_argument("--no-fuse-qkv", action="store_true",
+                   help="run q, k and v as three GEMMs instead of one over their concatenated [6144][4096] weights")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -328,7 +332,7 @@ def run_gpu(args, ranks: Ranks):
     hq.load()
     peak, peak_kind = measured_peaks()
 
-    vp = VerifyPass(torch, hq, synth, device, fuse_qkv=args.fuse_qkv, pdl=not args.no_pdl)
+    vp = VerifyPass(torch, hq, synth, device, fuse_qkv=not args.no_fuse_qkv, pdl=not args.no_pdl)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=device)
@@ -436,7 +440,7 @@ def run_gpu(args, ranks: Ranks):
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": vp.M, "format": "w4_asym", "group": vp.G, "layers": 32,
                        "linears_per_pass": vp.n_gemm, "activation_inputs_per_pass": vp.n_act,
-                       "qkv_fused": bool(args.fuse_qkv), "pdl": not args.no_pdl,
+                       "qkv_fused": not args.no_fuse_qkv, "pdl": not args.no_pdl,
                        "weight_bytes_per_pass": vp.weight_bytes,
                        "l2": "inputs larger than L2: 3.875 GB of packed weights streamed per pass, L2 129 MB",
                        "parallelism": f"replicas x{ranks.world} (independent verify batches)"},

@@ -425,28 +425,36 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
     // partial sums in ascending K order (slot 0 of a block's contributor is its
     // first segment, slot 1 its last), multiplies by the row scale and writes Y.
     if (pend0 >= 0 || pend1 >= 0) {
-        __threadfence();
+        // Publish: the barrier orders every consumer thread's partial-sum
+        // stores before thread 0's release; both arrivals go out together.
         named_barrier(1, NCW * 32);
         if (threadIdx.x == 0) {
-            int flags = 0;
-            for (int p = 0; p < 2; ++p) {
-                const int bb = p == 0 ? pend0 : pend1;
-                if (bb < 0) continue;
-                const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
-                const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
-                if (atomicAdd(&ctr[bb], 1) == c_hi - c_lo) flags |= 1 << p;
+            int last0 = 0, last1 = 0;
+            if (pend0 >= 0) {
+                const int c_lo = cta_of_tile(pend0 * KTILES, a.T, a.grid);
+                const int c_hi = cta_of_tile(pend0 * KTILES + KTILES - 1, a.T, a.grid);
+                last0 = atomic_add_acq_rel_gpu(&ctr[pend0], 1) == c_hi - c_lo;
             }
-            *s_flag = flags;
+            if (pend1 >= 0) {
+                const int c_lo = cta_of_tile(pend1 * KTILES, a.T, a.grid);
+                const int c_hi = cta_of_tile(pend1 * KTILES + KTILES - 1, a.T, a.grid);
+                last1 = atomic_add_acq_rel_gpu(&ctr[pend1], 1) == c_hi - c_lo;
+            }
+            *s_flag = last0 | (last1 << 1);
         }
+        // the acquire by thread 0 is ordered before every thread's loads below
         named_barrier(1, NCW * 32);
         const int flags = *s_flag;
-        if (flags) __threadfence();
         for (int p = 0; p < 2; ++p) {
             if (!(flags & (1 << p))) continue;
             const int bb = p == 0 ? pend0 : pend1;
             const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
             const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
-            // each thread: up to 4 groups of 4 channels x up to 8 contributors in flight
+            // Every contributor after the first starts inside this n-block, so it
+            // is their first n-block (slot 0); the first contributor used slot 1
+            // if it started in an earlier n-block.
+            const int slot_lo = tile_begin(c_lo, a.T, a.grid) < bb * KTILES ? 1 : 0;
+            // each thread: up to 4 groups of 4 channels x up to 4 contributors in flight
             for (int g0 = threadIdx.x; g0 < M * (BN / 4); g0 += 4 * NCW * 32) {
                 float4 sum[4];
 #pragma unroll
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int c2 = cc + v;
-                        const int sl = (bb == tile_begin(c2, a.T, a.grid) / KTILES) ? 0 : 1;
+                        const int sl = c2 == c_lo ? slot_lo : 0;
                         const float *base = wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats(M);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
