@@ -56,6 +56,10 @@ def parse_args():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--summarize-ncu", metavar="CSV",
+                   help="summarize an ncu --csv log of this program into profiles/ and exit")
+    p.add_argument("--ncu-command", default="", help="the ncu command line that produced CSV (recorded)")
+    p.add_argument("--ncu-name", default="decoder_9b", help="workload name used in the summary file names")
     return p.parse_args()
 
 
@@ -349,13 +353,12 @@ def run_gpu(args, ranks: Ranks):
     with torch.cuda.graph(gemm_graph, stream=stream):
         vp.launch(act=False)
 
-    # ---- the timed region: K whole passes
-    for _ in range(max(args.warmup, 3)):
-        graph.replay()
-    torch.cuda.synchronize()
-    ranks.barrier()
+    # ---- the timed region: K whole passes (the clock sampler starts first,
+    # so the warm-up passes also bring the clocks back up after its start-up)
     clocks = ClockSampler(ranks.local)
     time.sleep(0.3)
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ranks.barrier()
@@ -378,9 +381,9 @@ def run_gpu(args, ranks: Ranks):
     passes_per_s = args.steps * ranks.world / (ms_max / 1e3)
 
     # ---- the dominant kernel alone: the same GEMM launches without the activation kernels
-    for _ in range(3):
+    for _ in range(max(args.warmup, 3)):
         gemm_graph.replay()
-    reps = max(10, args.steps // 2)
+    reps = max(20, args.steps // 2)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     g0.record(stream)
@@ -457,8 +460,61 @@ def run_gpu(args, ranks: Ranks):
     return 0
 
 
+def summarize_ncu(args) -> int:
+    """Per-kernel launches, time and share from an ncu --csv log; with DRAM
+    byte metrics present, also the GEMM's traffic record read by the bench."""
+    import collections
+    import csv
+    rows = list(csv.reader(open(args.summarize_ncu)))
+    hi = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    hdr = rows[hi]
+    ix = {h: i for i, h in enumerate(hdr)}
+    scale = {"nsecond": 1e-3, "ns": 1e-3, "usecond": 1.0, "us": 1.0, "msecond": 1e3, "ms": 1e3,
+             "byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per = collections.defaultdict(lambda: collections.defaultdict(float))
+    launches = collections.defaultdict(set)
+    for r in rows[hi + 1:]:
+        if len(r) < len(hdr):
+            continue
+        name = r[ix["Kernel Name"]].replace("(anonymous namespace)::", "").replace("void ", "").split("(")[0]
+        name = name.replace("unnamed>::", "")
+        metric, unit = r[ix["Metric Name"]], r[ix["Metric Unit"]]
+        val = float(r[ix["Metric Value"]].replace(",", "")) * scale.get(unit, 1.0)
+        per[name][metric] += val
+        launches[name].add(r[ix["ID"]])
+    tot_us = sum(d.get("gpu__time_duration.sum", 0.0) for d in per.values())
+    out = [f"# ncu launch list: {args.ncu_name}", "",
+           f"Command: `{args.ncu_command}`" if args.ncu_command else "", "",
+           "Per kernel over the captured launches (ncu serializes launches and runs them with cold caches, so",
+           "compare the shares, not the absolute times, with the bench's CUDA-event timings).", "",
+           "| kernel | launches | total time (us) | share | DRAM read (MB) | DRAM write (MB) |",
+           "|---|---|---|---|---|---|"]
+    for name, d in sorted(per.items(), key=lambda kv: -kv[1].get("gpu__time_duration.sum", 0.0)):
+        t = d.get("gpu__time_duration.sum", 0.0)
+        out.append(f"| `{name}` | {len(launches[name])} | {t:.1f} | {100 * t / tot_us if tot_us else 0:.1f}% | "
+                   f"{d.get('dram__bytes_read.sum', 0) / 1e6:.1f} | {d.get('dram__bytes_write.sum', 0) / 1e6:.1f} |")
+    md = os.path.join(ROOT, "profiles", f"launches_{args.ncu_name}.md")
+    with open(md, "w") as f:
+        f.write("\n".join(out) + "\n")
+    print(md)
+    gemm = [n for n in per if n.startswith("k_verify_gemm")]
+    if gemm and any("dram__bytes_read.sum" in per[n] for n in gemm):
+        n_l = sum(len(launches[n]) for n in gemm)
+        dram = sum(per[n].get("dram__bytes_read.sum", 0) + per[n].get("dram__bytes_write.sum", 0) for n in gemm)
+        rec = {"kernel": "k_verify_gemm", "workload": args.ncu_name, "launches": n_l,
+               "dram_bytes_total": dram, "dram_bytes_per_launch": dram / n_l,
+               "kernel_source_hash": kernel_source_hash(), "command": args.ncu_command}
+        js = os.path.join(ROOT, "profiles", f"k_verify_gemm_{args.ncu_name}_traffic.json")
+        with open(js, "w") as f:
+            json.dump(rec, f, indent=1)
+        print(js)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.summarize_ncu:
+        return summarize_ncu(args)
     ranks = Ranks()
     try:
         if args.impl == "reference":
