@@ -93,11 +93,13 @@ size_t hq_packed_bytes(const hq_layer_desc *desc);
 
 /* Size in bytes of the workspace hq_verify_gemm needs for `desc` and M rows
  * (0 if the arguments are invalid).  The workspace holds the device error
- * word, the split-K arrival counters and the split-K partial sums (sized for
- * at most 32 rows: larger batches run as consecutive 32-row launches).  It must
+ * word, the split-K partial sums (sized for at most 32 rows: larger batches
+ * run as consecutive 32-row launches; 16 MiB) and two counters per 128
+ * output channels, at offsets that depend on neither the layer nor M: one
+ * workspace of the largest size serves calls of every layer and M in turn
+ * (calls that may overlap on the GPU need workspaces of their own).  It must
  * be zero-filled once after allocation; every call leaves it zero-filled
- * again (except for the error word after a timeout, see
- * hq_workspace_status). */
+ * again (except after a time-out, see hq_workspace_status). */
 size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M);
 
 /* Sign vector of the randomized Hadamard transform ("random sign flips
@@ -166,7 +168,12 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *si
  * with fp32 accumulation, which is exact for these ranges).  The fp32 sum
  * over groups is taken in ascending group order; an output whose K range is
  * split across thread blocks sums the blocks' partial sums in ascending K
- * order, so results are deterministic.  flags: HQ_LAUNCH_DEFAULT or
+ * order, so results are deterministic.  The thread blocks that share an
+ * output block wait for one another (bounded) before that sum; the grid never
+ * exceeds the blocks resident at once, but a kernel running concurrently on
+ * another stream that holds SMs for longer than the bound makes the call time
+ * out (HQ_ERR_TIMEOUT from hq_workspace_status; zero the workspace again
+ * before reusing it after a time-out).  flags: HQ_LAUNCH_DEFAULT or
  * HQ_LAUNCH_PDL (see above). */
 int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream);
@@ -192,7 +199,7 @@ int hq_workspace_status(void *workspace, void *stream);
  * synchronize the device.  The pages have no counterpart of this call.
  *
  * The scratch lives in one file-scope device array of
- * HQ_NOALLOC_SCRATCH_BYTES (16 MiB + 64 KiB) that every GPU which loads the
+ * HQ_NOALLOC_SCRATCH_BYTES (16 MiB + 128 KiB) that every GPU which loads the
  * library holds until the process exits.  A call is accepted when
  * hq_workspace_bytes(desc, M) fits in it (any M, for N up to about two
  * million outputs); larger calls return HQ_ERR_UNSUPPORTED and launch
@@ -205,7 +212,7 @@ int hq_workspace_status(void *workspace, void *stream);
  * that may overlap on the GPU (different streams, or graphs replayed
  * concurrently) race and must be serialized by the caller.  Arguments,
  * outputs and flags are those of hq_verify_gemm. */
-#define HQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 64u * 1024u)
+#define HQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 128u * 1024u)
 int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
                            int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream);
 

@@ -54,11 +54,11 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.Y = Y;
     a.partials = partials;
     a.ws = static_cast<uint8_t *>(workspace);
-    a.ws_partial_off = ws_partial_offset(g);
     a.M_total = M;
     a.N = g.N;
     a.K = g.K;
     a.NGK = g.NGK;
+    a.NB = g.NB;
     a.KTILES = g.KTILES;
     a.T = g.NB * g.KTILES;
     // Three thread blocks per SM (twelve consumer warps) keep enough loads and
@@ -141,7 +141,7 @@ size_t hq_packed_bytes(const hq_layer_desc *desc) {
 
 size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M) {
     if (!desc_ok(desc) || M < 0 || M > HQ_MAX_M) return 0;
-    return hq::ws_bytes(geom_of(desc), M);
+    return hq::ws_bytes(geom_of(desc));
 }
 
 int hq_make_signs(uint64_t seed, int32_t K, uint32_t *signs_host) {

@@ -88,19 +88,21 @@ __host__ __device__ inline size_t blob_bytes(const Geom &g) {
     return (size_t)g.NB * (size_t)g.KTILES * (size_t)g.tile_bytes;
 }
 
-// Workspace: [0, 16) error word; [16, 16 + ctr) arrival counters (one per
-// n-block); then partial-sum slots, two per thread block, BN x M floats each.
-__host__ __device__ inline size_t ws_counter_offset() { return 16; }
-__host__ __device__ inline size_t ws_counter_bytes(const Geom &g) { return ((size_t)g.NB * 4 + 15) / 16 * 16; }
-__host__ __device__ inline size_t ws_partial_offset(const Geom &g) { return ws_counter_offset() + ws_counter_bytes(g); }
-__host__ __device__ inline size_t ws_slot_floats(int M) { return (size_t)BN * (size_t)M; }
+// Workspace: [0, 16) error word; then the partial-sum slots, two per thread
+// block, BN x MAX_M_LAUNCH floats each (a launch fills its first M rows);
+// then two counters per n-block (arrivals [NB], then finished reductions
+// [NB]).  Every offset is independent of the layer and of M, so one
+// workspace, large enough for each call, serves calls of any shape in turn.
 // The GEMM handles at most MAX_M_LAUNCH rows per launch (larger batches are
 // run as consecutive launches that reuse the workspace).
 constexpr int MAX_M_LAUNCH = 32;
-__host__ __device__ inline size_t ws_bytes(const Geom &g, int M) {
-    const int m = M < MAX_M_LAUNCH ? M : MAX_M_LAUNCH;
-    return ws_partial_offset(g) + (size_t)MAX_CTAS * 2 * ws_slot_floats(m) * 4;
+__host__ __device__ inline size_t ws_slot_floats() { return (size_t)BN * (size_t)MAX_M_LAUNCH; }
+__host__ __device__ inline size_t ws_partial_offset() { return 16; }
+__host__ __device__ inline size_t ws_counter_offset() {
+    return ws_partial_offset() + (size_t)MAX_CTAS * 2 * ws_slot_floats() * 4;
 }
+__host__ __device__ inline size_t ws_counter_bytes(const Geom &g) { return ((size_t)g.NB * 8 + 15) / 16 * 16; }
+__host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_offset() + ws_counter_bytes(g); }
 
 // Activation operand of the GEMM: fp16 codes in blocks of 128 features,
 // [ceil(K/128)][M][128]; inside a 256-byte row the 16-byte chunk q of token
@@ -211,6 +213,28 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *p >= target (acquire), for at most WAIT_LIMIT_NS; polls with a
+// short sleep in between.  On time-out records DEV_ERR_TIMEOUT in *err and
+// returns false.
+__device__ __forceinline__ bool wait_count_bounded(const int *p, int target, int *err) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(100);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 // Named barrier over `count` threads (a multiple of 32).

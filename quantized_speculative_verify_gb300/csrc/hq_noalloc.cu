@@ -48,14 +48,17 @@ extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blo
         return HQ_ERR_INVALID_ARG;
     const hq::Geom g = hq::make_geom(desc->K, desc->N, desc->group, desc->format);
     // The call needs exactly the workspace hq_verify_gemm would need.
-    if (hq::ws_bytes(g, M) > (size_t)HQ_NOALLOC_SCRATCH_BYTES) return HQ_ERR_UNSUPPORTED;
+    if (hq::ws_bytes(g) > (size_t)HQ_NOALLOC_SCRATCH_BYTES) return HQ_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     const int st = scratch_for_current_device(&scratch);
     if (st != HQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The previous call's contents stay in the array: clear the error word
-    // and the arrival counters, which must start at zero.
-    if (cudaMemsetAsync(scratch, 0, hq::ws_partial_offset(g), s) != cudaSuccess) return HQ_ERR_CUDA;
+    // and the n-block counters, which must start at zero.
+    if (cudaMemsetAsync(scratch, 0, hq::ws_partial_offset(), s) != cudaSuccess) return HQ_ERR_CUDA;
+    if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + hq::ws_counter_offset(), 0, hq::ws_counter_bytes(g), s) !=
+        cudaSuccess)
+        return HQ_ERR_CUDA;
     const cudaError_t e =
         hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, scratch,
                                (flags & HQ_LAUNCH_PDL) != 0, s);

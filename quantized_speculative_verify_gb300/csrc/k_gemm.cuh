@@ -51,9 +51,8 @@ struct GemmArgs {
     float *Y;            // [M_total][N]
     int32_t *partials;   // check mode: [M_total][N][K/G] or NULL
     uint8_t *ws;
-    size_t ws_partial_off;  // byte offset of the partial-sum slots in ws
     int M_total, m0, M;     // rows of the call, first row of this launch, rows of this launch (<= 32)
-    int N, K, NGK, KTILES, T, grid, stages;
+    int N, K, NGK, NB, KTILES, T, grid, stages;
     int tile_bytes, code_bytes, scale_bytes, act_bytes;
 };
 
@@ -126,11 +125,13 @@ struct GemmCfg {
     static constexpr int GPT = KT / G;            // groups per tile
     static constexpr int NCW = NTILES / NW;       // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int BLOCKS_PER_SM = 3;  // the launch puts three blocks on each SM
 };
 
 // CHECK: also write the exact integer partial sums (check mode).
 template <int FMT, int G, int MT, bool CHECK>
-__global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(const GemmArgs a) {
+__global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, MT>::BLOCKS_PER_SM)
+    k_verify_gemm(const GemmArgs a) {
     using C = GemmCfg<FMT, G, MT>;
     constexpr int KT = C::KT, NCW = C::NCW, NW = C::NW;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -140,7 +141,6 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
     const uint32_t tx_bytes = (uint32_t)a.tile_bytes + (uint32_t)a.M * 256u * (uint32_t)(C::KT / 128);
     uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);  // full[S], empty[S]
-    int *s_flag = reinterpret_cast<int *>(bars + 2 * S);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = tile_begin(blockIdx.x, a.T, a.grid);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
     pdl_wait();
     const int g8 = lane >> 2, tig = lane & 3;
     const int M = a.M, N = a.N, KTILES = a.KTILES;
-    float *wsp = reinterpret_cast<float *>(a.ws + a.ws_partial_off);
+    float *wsp = reinterpret_cast<float *>(a.ws + ws_partial_offset());
     int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
     const float *sxm = a.sx + a.m0;
     float *Ym = a.Y + (size_t)a.m0 * N;
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
                 // part of the K range: publish the partial sums now, count the
                 // arrival once this block's tiles are all done
                 const int slot = b == first_b ? 0 : 1;
-                float *mys = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats(M);
+                float *mys = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats();
 #pragma unroll
                 for (int j = 0; j < NW; ++j)
 #pragma unroll
@@ -421,85 +421,80 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS) k_verify_gemm(co
         }
     }
 
-    // Arrivals: the last contributor of an n-block sums every contributor's
-    // partial sums in ascending K order (slot 0 of a block's contributor is its
-    // first segment, slot 1 its last), multiplies by the row scale and writes Y.
+    // Split n-blocks: every contributor arrives, waits until all contributors
+    // of the n-block have arrived, then sums its share of the n-block's
+    // outputs over all contributors' partial sums in ascending K order (slot 0
+    // of a contributor is its first segment, slot 1 its last), multiplies by
+    // the row scale and writes Y.  The wait is safe because every thread block
+    // of the launch is resident: the grid never exceeds the blocks that fit
+    // on the device at once, and dependent kernels are launched only after
+    // every block of this one has started.  The last contributor to finish
+    // resets the n-block's two counters for the next call.
     if (pend0 >= 0 || pend1 >= 0) {
+        int *done = ctr + a.NB;
         // Publish: the barrier orders every consumer thread's partial-sum
         // stores before thread 0's release; both arrivals go out together.
         named_barrier(1, NCW * 32);
         if (threadIdx.x == 0) {
-            int last0 = 0, last1 = 0;
-            if (pend0 >= 0) {
-                const int c_lo = cta_of_tile(pend0 * KTILES, a.T, a.grid);
-                const int c_hi = cta_of_tile(pend0 * KTILES + KTILES - 1, a.T, a.grid);
-                last0 = atomic_add_acq_rel_gpu(&ctr[pend0], 1) == c_hi - c_lo;
-            }
-            if (pend1 >= 0) {
-                const int c_lo = cta_of_tile(pend1 * KTILES, a.T, a.grid);
-                const int c_hi = cta_of_tile(pend1 * KTILES + KTILES - 1, a.T, a.grid);
-                last1 = atomic_add_acq_rel_gpu(&ctr[pend1], 1) == c_hi - c_lo;
-            }
-            *s_flag = last0 | (last1 << 1);
+            if (pend0 >= 0) atomic_add_acq_rel_gpu(&ctr[pend0], 1);
+            if (pend1 >= 0) atomic_add_acq_rel_gpu(&ctr[pend1], 1);
         }
-        // the acquire by thread 0 is ordered before every thread's loads below
-        named_barrier(1, NCW * 32);
-        const int flags = *s_flag;
         for (int p = 0; p < 2; ++p) {
-            if (!(flags & (1 << p))) continue;
             const int bb = p == 0 ? pend0 : pend1;
+            if (bb < 0) continue;
             const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
             const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
+            const int nc = c_hi - c_lo + 1;
+            if (threadIdx.x == 0) {
+                if (ok) ok = wait_count_bounded(&ctr[bb], nc, err);
+            }
+            // thread 0's acquire is ordered before every thread's loads below
+            named_barrier(1, NCW * 32);
             // Every contributor after the first starts inside this n-block, so it
             // is their first n-block (slot 0); the first contributor used slot 1
             // if it started in an earlier n-block.
             const int slot_lo = tile_begin(c_lo, a.T, a.grid) < bb * KTILES ? 1 : 0;
-            // each thread: up to 4 groups of 4 channels x up to 4 contributors in flight
-            for (int g0 = threadIdx.x; g0 < M * (BN / 4); g0 += 4 * NCW * 32) {
-                float4 sum[4];
+            // this contributor's share: outputs [lo, hi) in units of 4 channels
+            const int total = M * (BN / 4);
+            const int per = (total + nc - 1) / nc;
+            const int lo = (blockIdx.x - c_lo) * per;
+            const int hi = lo + per < total ? lo + per : total;
+            for (int gi = lo + (int)threadIdx.x; gi < hi; gi += NCW * 32) {
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                // up to 8 contributors' loads in flight, added in contributor order
+                for (int cc = c_lo; cc <= c_hi; cc += 8) {
+                    float4 x[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int cc = c_lo; cc <= c_hi; cc += 4) {
-                    float4 x[4][4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 8; ++v) {
                         const int c2 = cc + v;
                         const int sl = c2 == c_lo ? slot_lo : 0;
-                        const float *base = wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats(M);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int gi = g0 + u * NCW * 32;
-                            if (c2 <= c_hi && gi < M * (BN / 4))
-                                x[u][v] = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)gi * 4));
-                        }
+                        if (c2 <= c_hi)
+                            x[v] = __ldcg(reinterpret_cast<const float4 *>(
+                                wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats() + (size_t)gi * 4));
                     }
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 8; ++v) {
                         if (cc + v > c_hi) break;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            sum[u].x = __fadd_rn(sum[u].x, x[u][v].x);
-                            sum[u].y = __fadd_rn(sum[u].y, x[u][v].y);
-                            sum[u].z = __fadd_rn(sum[u].z, x[u][v].z);
-                            sum[u].w = __fadd_rn(sum[u].w, x[u][v].w);
-                        }
+                        sum.x = __fadd_rn(sum.x, x[v].x);
+                        sum.y = __fadd_rn(sum.y, x[v].y);
+                        sum.z = __fadd_rn(sum.z, x[v].z);
+                        sum.w = __fadd_rn(sum.w, x[v].w);
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int gi = g0 + u * NCW * 32;
-                    if (gi >= M * (BN / 4)) continue;
-                    const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
-                    const float sxt = __ldg(sxm + tok);
-                    const int n = bb * BN + r4;
-                    float *yr = Ym + (size_t)tok * N;
-                    if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum[u].x);
-                    if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum[u].y);
-                    if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum[u].z);
-                    if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum[u].w);
-                }
+                const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
+                const float sxt = __ldg(sxm + tok);
+                const int n = bb * BN + r4;
+                float *yr = Ym + (size_t)tok * N;
+                if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum.x);
+                if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum.y);
+                if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum.z);
+                if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum.w);
             }
-            if (threadIdx.x == 0) atomicExch(&ctr[bb], 0);
+            // every contributor has passed its wait once all have counted here
+            if (threadIdx.x == 0 && atomicAdd(&done[bb], 1) == nc - 1) {
+                atomicExch(&ctr[bb], 0);
+                atomicExch(&done[bb], 0);
+            }
         }
     }
 }
@@ -520,8 +515,21 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
+    // The split-K reduction makes blocks wait for one another: the grid must
+    // never exceed the blocks that are resident at once.
+    static int resident_for = -1, resident_blocks = 0;
+    if (resident_for != dev) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, smem);
+        if (e != cudaSuccess) return e;
+        resident_blocks = per_sm * device_sm_count();
+        resident_for = dev;
+    }
+    if (resident_blocks < 1) return cudaErrorLaunchOutOfResources;
+    GemmArgs la = a;
+    if (la.grid > resident_blocks) la.grid = resident_blocks;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.grid);
+    cfg.gridDim = dim3((unsigned)la.grid);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -530,7 +538,7 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, la);
 }
 
 // Instances for one format: token buckets {<=8, <=16, <=32} per launch.

@@ -173,7 +173,7 @@ def hq_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
            "hq_selftest_wait_timeout")
 
 
-HQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 64 * 1024
+HQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 128 * 1024
 
 
 def hq_verify_gemm_noalloc(desc, blob, qop, sx, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:

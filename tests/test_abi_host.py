@@ -95,10 +95,14 @@ def test_act_operand_bytes():
 
 def test_workspace_bytes():
     d = hq.make_desc(4096, 4096, 64, "w4")
-    assert hq.hq_workspace_bytes(d, 16) > hq.hq_workspace_bytes(d, 1) > 0
+    assert hq.hq_workspace_bytes(d, 16) == hq.hq_workspace_bytes(d, 1) > 16 * 1024 * 1024
     assert hq.hq_workspace_bytes(d, 129) == 0 and hq.hq_workspace_bytes(d, -1) == 0
     assert hq.hq_workspace_bytes(d, 128) == hq.hq_workspace_bytes(d, 32)  # at most 32 rows per launch
     assert hq.hq_workspace_bytes(d, 16) % 16 == 0
+    # a wider layer needs more counters, at the same offsets: a workspace sized
+    # for the widest layer serves every layer
+    wide = hq.make_desc(4096, 24576, 64, "w4")
+    assert hq.hq_workspace_bytes(wide, 16) - hq.hq_workspace_bytes(d, 16) == (192 - 32) * 8
 
 
 FAKE = 0x10000  # a 16-byte aligned non-NULL value; never dereferenced: every call below fails validation

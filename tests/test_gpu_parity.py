@@ -158,6 +158,10 @@ def test_pack_bit_exact(fmt, K, N, G):
 
 
 # ---------------------------------------------------------------- GEMM ---
+# workspace: 16-byte error word, 512 blocks x 2 slots x 128 x 32 fp32 partial sums, counters
+COUNTER_OFFSET = 16 + 512 * 2 * 128 * 32 * 4
+
+
 def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     M, K = X.shape
     if layer is None:
@@ -168,9 +172,9 @@ def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     Y = hq.verify_linear(layer, X.to(DEV), ws, bufs=bufs, partials=P, flags=flags)
     assert hq.hq_workspace_status(ws) == hq.HQ_OK
     torch.cuda.synchronize()
-    # every call leaves the arrival counters at zero
-    nb = (layer.N + 127) // 128
-    assert not ws[16:16 + 4 * nb].any()
+    # every call leaves the error word and the n-block counters (after 16 MiB
+    # of partial-sum slots) at zero
+    assert not ws[:16].any() and not ws[COUNTER_OFFSET:].any()
     return dict(Y=Y.cpu().numpy(), P=None if P is None else P.cpu().numpy(), layer=layer, ws=ws)
 
 
@@ -214,6 +218,28 @@ def test_gemm_pdl_flag_and_repeat_are_identical():
     r2 = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
     assert np.array_equal(r0["Y"].view(np.uint32), r1["Y"].view(np.uint32))
     assert np.array_equal(r1["Y"].view(np.uint32), r2["Y"].view(np.uint32))
+
+
+def test_shared_workspace_across_layers_and_batches():
+    # one workspace, sized for the widest layer, serves layers of different
+    # width, depth and batch in a PDL chain; every output equals the one
+    # computed with a fresh workspace, bit for bit
+    shapes = [(2048, 3072, 16), (2048, 2048, 16), (2048, 12288, 16), (6144, 2048, 16), (2048, 12288, 5),
+              (2048, 640, 40), (2048, 12288, 16)]
+    layers, inputs = [], []
+    for i, (K, N, M) in enumerate(shapes):
+        s_host, _ = signs_pair(100 + i, K)
+        W = synth.weights(N, K, seed=200 + i)
+        layers.append(hq.pack_layer(W.to(DEV), 64, "w4", s_host))
+        inputs.append(synth.activations(M, K, seed=300 + i, outlier_channels=2).to(DEV))
+    need = max(hq.hq_workspace_bytes(l.desc, x.shape[0]) for l, x in zip(layers, inputs))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    shared = [hq.verify_linear(l, x, ws, flags=hq.HQ_LAUNCH_PDL) for l, x in zip(layers, inputs)]
+    torch.cuda.synchronize()
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    for l, x, y in zip(layers, inputs, shared):
+        fresh = hq.verify_linear(l, x, hq.workspace(l.desc, x.shape[0], DEV))
+        assert torch.equal(y.view(torch.int32), fresh.view(torch.int32))
 
 
 def test_gemm_extreme_codes_int32_headroom():
