@@ -206,13 +206,9 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
-// atomicAdd with release + acquire semantics at GPU scope.  After a named
-// barrier over the block's threads, the release also publishes the other
-// threads' earlier stores (they are ordered before it by the barrier).
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
-    int old;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+// Add without returning the old value, release semantics at GPU scope.
+__device__ __forceinline__ void red_add_release_gpu(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {

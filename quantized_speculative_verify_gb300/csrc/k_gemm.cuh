@@ -436,8 +436,8 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
         // stores before thread 0's release; both arrivals go out together.
         named_barrier(1, NCW * 32);
         if (threadIdx.x == 0) {
-            if (pend0 >= 0) atomic_add_acq_rel_gpu(&ctr[pend0], 1);
-            if (pend1 >= 0) atomic_add_acq_rel_gpu(&ctr[pend1], 1);
+            if (pend0 >= 0) red_add_release_gpu(&ctr[pend0], 1);
+            if (pend1 >= 0) red_add_release_gpu(&ctr[pend1], 1);
         }
         for (int p = 0; p < 2; ++p) {
             const int bb = p == 0 ? pend0 : pend1;
@@ -445,8 +445,11 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
             const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
             const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
             const int nc = c_hi - c_lo + 1;
+            int done_before = 0;
             if (threadIdx.x == 0) {
                 if (ok) ok = wait_count_bounded(&ctr[bb], nc, err);
+                // passed the wait: count it now, the answer arrives during the sums
+                done_before = atomicAdd(&done[bb], 1);
             }
             // thread 0's acquire is ordered before every thread's loads below
             named_barrier(1, NCW * 32);
@@ -490,8 +493,8 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                 if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum.z);
                 if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum.w);
             }
-            // every contributor has passed its wait once all have counted here
-            if (threadIdx.x == 0 && atomicAdd(&done[bb], 1) == nc - 1) {
+            // every contributor has passed its wait once all have counted
+            if (threadIdx.x == 0 && done_before == nc - 1) {
                 atomicExch(&ctr[bb], 0);
                 atomicExch(&done[bb], 0);
             }
