@@ -60,6 +60,8 @@ def parse_args():
                    help="summarize an ncu --csv log of this program into profiles/ and exit")
     p.add_argument("--ncu-command", default="", help="the ncu command line that produced CSV (recorded)")
     p.add_argument("--ncu-name", default="decoder_9b", help="workload name used in the summary file names")
+    p.add_argument("--one-gemm", metavar="K,N,G,FMT,M",
+                   help="time one GEMM layer of this shape alone (K,N,G,w4|w8,M), print its JSON line and exit")
     return p.parse_args()
 
 
@@ -511,10 +513,48 @@ def summarize_ncu(args) -> int:
     return 0
 
 
+def run_one_gemm(args) -> int:
+    """One layer of the given shape: rotate/quantize once, then --steps timed GEMM launches
+    (CUDA events, after --warmup launches); the weights are larger than L2 for the 9B shapes."""
+    import torch
+    from quantized_speculative_verify_gb300 import hq, synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    K, N, G, fmt, M = args.one_gemm.split(",")
+    K, N, G, M = int(K), int(N), int(G), int(M)
+    dev = torch.device("cuda", 0)
+    W = synth.weights(N, K, seed=1, device=dev)
+    layer = hq.pack_layer(W, G, fmt, hq.hq_make_signs(3, K))
+    del W
+    X = synth.activations(M, K, seed=2, device=dev)
+    _, qop, sx = hq.act_buffers(M, K, dev, int8_codes=False)
+    hq.hq_rotate_quant_act(X, M, K, layer.signs, None, qop, sx)
+    ws = hq.workspace(layer.desc, M, dev)
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 1)):
+        hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, None, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, None, ws)
+    e1.record()
+    e1.synchronize()
+    if hq.hq_workspace_status(ws) != hq.HQ_OK:
+        raise SystemExit("device-side wait timed out")
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    print(json.dumps({"gemm": {"K": K, "N": N, "group": G, "format": fmt, "M": M}, "us_per_launch": us,
+                      "weight_bytes": int(layer.blob.numel()), "GB_per_s": layer.blob.numel() / us / 1e3}))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.summarize_ncu:
         return summarize_ncu(args)
+    if args.one_gemm:
+        return run_one_gemm(args)
     ranks = Ranks()
     try:
         if args.impl == "reference":
