@@ -93,6 +93,8 @@ def _load(openmp: bool = False) -> ctypes.CDLL:
         lib.or_output.argtypes = [_P, _P, _P, _I, _I, _I, _P]
         lib.or_verify_gemm.argtypes = [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]
         lib.or_num_threads.argtypes = []
+        lib.or_argmax_rows.argtypes = [_P, _I, _I, _P]
+        lib.or_tree_accept.argtypes = [_P, _P, _P, _I, _P, _P, _P]
         _libs[openmp] = lib
         return lib
 
@@ -279,3 +281,24 @@ def verify_linear(X: np.ndarray, W: np.ndarray, G: int, fmt: str, signs: np.ndar
     P = partials(qx, codes, zeros, G)
     Y = output(P, sx, scales)
     return dict(qx=qx, sx=sx, gsum=gsum, codes=codes, scales=scales, zeros=zeros, P=P, Y=Y)
+
+
+def argmax_rows(logits: np.ndarray) -> np.ndarray:
+    """Greedy token per row: lowest index among equal maxima; the first NaN wins."""
+    L = _c(np.atleast_2d(logits), np.float32)
+    M, V = L.shape
+    g = np.empty(M, dtype=np.int32)
+    _check(_load().or_argmax_rows(_ptr(L), M, V, _ptr(g)), "argmax_rows")
+    return g
+
+
+def tree_accept(g: np.ndarray, parent: np.ndarray, tokens: np.ndarray):
+    """(path of accepted drafted nodes, number accepted, bonus token) for a draft tree."""
+    g, parent, tokens = _c(g, np.int32), _c(parent, np.int32), _c(tokens, np.int32)
+    M = g.shape[0]
+    path = np.full(M, -1, dtype=np.int32)
+    n = np.zeros(1, dtype=np.int32)
+    bonus = np.zeros(1, dtype=np.int32)
+    _check(_load().or_tree_accept(_ptr(g), _ptr(parent), _ptr(tokens), M, _ptr(path), _ptr(n), _ptr(bonus)),
+           "tree_accept")
+    return path[: int(n[0])], int(n[0]), int(bonus[0])

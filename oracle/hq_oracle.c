@@ -419,6 +419,69 @@ int or_verify_gemm(const int8_t *qx, const float *sx, int M, const void *codes, 
 }
 
 /* Number of OpenMP threads this build uses (1 without OpenMP). */
+/* ------------------------------------------------------------------------ */
+/* Tree acceptance (section "Producing several tokens from one model pass"  */
+/* and "Verifying a draft tree without restoring model state": the main    */
+/* model checks the drafted positions together, accepts the valid prefix,  */
+/* adds its own token at the first position it did not confirm; on a tree  */
+/* it accepts the longest valid path).  Readings:                          */
+/*   T1  node 0 is the root (the last committed token); every other node i */
+/*       has a parent p[i] < i and a drafted token t[i];                   */
+/*   T2  row i of the logits is the main model's output after node i; its  */
+/*       greedy token g[i] = argmax_v logits[i][v], the lowest index among */
+/*       equal maxima; a NaN counts as larger than every number (the first */
+/*       NaN wins);                                                        */
+/*   T3  node i >= 1 is valid when its parent is valid (the root is) and   */
+/*       t[i] == g[p[i]];                                                  */
+/*   T4  the accepted node is the deepest valid node, the lowest index     */
+/*       among equally deep ones; the sequence advances by its depth (the  */
+/*       accepted drafted tokens) plus one: the main model's own token g   */
+/*       at the accepted node.                                             */
+/* ------------------------------------------------------------------------ */
+int or_argmax_rows(const float *logits, int M, int V, int32_t *g)
+{
+    if (M < 0 || V <= 0) return 1;
+    for (int i = 0; i < M; ++i) {
+        const float *row = logits + (size_t)i * (size_t)V;
+        int best = 0;
+        for (int v = 1; v < V; ++v) {
+            const float a = row[v], b = row[best];
+            if (isnan(b)) break;                 /* the first NaN wins */
+            if (isnan(a) || a > b) best = v;     /* strictly greater: lowest index on ties */
+        }
+        g[i] = best;
+    }
+    return 0;
+}
+
+/* path[0..depth-1]: the accepted drafted nodes from the root's child down to
+   the accepted node; *n_accept = depth; *bonus = g[accepted node]. */
+int or_tree_accept(const int32_t *g, const int32_t *parent, const int32_t *tokens, int M, int32_t *path,
+                   int32_t *n_accept, int32_t *bonus)
+{
+    if (M <= 0) return 1;
+    int *valid = (int *)malloc(sizeof(int) * (size_t)M);
+    int *depth = (int *)malloc(sizeof(int) * (size_t)M);
+    if (!valid || !depth) { free(valid); free(depth); return 2; }
+    valid[0] = 1;
+    depth[0] = 0;
+    for (int i = 1; i < M; ++i) {
+        const int p = parent[i];
+        if (p < 0 || p >= i) { free(valid); free(depth); return 1; }
+        valid[i] = valid[p] && tokens[i] == g[p];
+        depth[i] = depth[p] + 1;
+    }
+    int best = 0;
+    for (int i = 1; i < M; ++i)
+        if (valid[i] && depth[i] > depth[best]) best = i;
+    *n_accept = depth[best];
+    *bonus = g[best];
+    for (int i = best, d = depth[best]; d > 0; i = parent[i], --d) path[d - 1] = i;
+    free(valid);
+    free(depth);
+    return 0;
+}
+
 int or_num_threads(void)
 {
 #ifdef _OPENMP

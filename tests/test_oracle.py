@@ -451,3 +451,70 @@ def test_openmp_build_matches_single_thread():
     y2 = oracle.verify_gemm(qx, sx, a[0], a[1], a[2], G, openmp=True)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
     assert oracle.num_threads(False) == 1 and oracle.num_threads(True) >= 1
+
+
+# ---------------------------------------------------- tree acceptance ---
+def parse_tree_golden(golden_dir):
+    out = []
+    for line in open(os.path.join(golden_dir, "tree_accept.txt")):
+        if not line.startswith("case"):
+            continue
+        f = [x.strip() for x in line[len("case"):].split("|")]
+        name, par, tok, g, path, adv = f[0], *[np.array(x.split(), dtype=np.int64) for x in f[1:5]], int(f[5])
+        out.append((name, par, tok, g, path, adv))
+    return out
+
+
+def test_tree_accept_golden(golden_dir):
+    cases = parse_tree_golden(golden_dir)
+    assert len(cases) >= 6
+    for name, par, tok, g, path, adv in cases:
+        p, n, bonus = oracle.tree_accept(g, par, tok)
+        assert list(p) == list(path), name
+        assert n + 1 == adv, name
+        last = path[-1] if len(path) else 0
+        assert bonus == g[last], name
+
+
+def test_argmax_rows_matches_numpy_first_index():
+    # numpy.argmax returns the first index of the maximum (and the first NaN)
+    rng = np.random.default_rng(5)
+    L = rng.integers(-3, 4, size=(40, 301)).astype(np.float32)  # many ties
+    L[7, 100] = np.nan
+    L[9, 0] = np.nan
+    L[11] = -np.inf
+    L[12, 200] = np.inf
+    assert np.array_equal(oracle.argmax_rows(L), np.argmax(L, axis=1))
+
+
+def brute_force_accept(g, parent, tokens):
+    """Every root-to-node path checked edge by edge; deepest valid, lowest index."""
+    best, best_path = 0, []
+    for i in range(1, len(parent)):
+        path, j, ok = [], i, True
+        while j != 0:
+            ok &= tokens[j] == g[parent[j]]
+            path.append(j)
+            j = parent[j]
+        if ok and len(path) > len(best_path):
+            best, best_path = i, path[::-1]
+    return best_path, g[best]
+
+
+def test_tree_accept_brute_force_random_trees():
+    rng = np.random.default_rng(6)
+    for trial in range(300):
+        M = int(rng.integers(1, 40))
+        parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, M)], dtype=np.int32)
+        g = rng.integers(0, 4, size=M).astype(np.int32)
+        tokens = rng.integers(0, 4, size=M).astype(np.int32)
+        path, n, bonus = oracle.tree_accept(g, parent, tokens)
+        bp, bb = brute_force_accept(g, parent, tokens)
+        assert list(path) == bp and n == len(bp) and bonus == bb, trial
+
+
+def test_tree_accept_rejects_bad_parents():
+    g = np.zeros(3, dtype=np.int32)
+    for parent in ([-1, 1, 0], [-1, 0, 2], [-1, -1, 0]):
+        with pytest.raises(ValueError):
+            oracle.tree_accept(g, np.array(parent, dtype=np.int32), np.zeros(3, dtype=np.int32))

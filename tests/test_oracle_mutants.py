@@ -37,6 +37,12 @@ MUTANTS = {
                                    "float t = scales[(size_t)n * NG + (g + 1) % NG] * p;"),
     "epilogue_drops_row_scale": ("Y[(size_t)m * N + n] = sx[m] * acc;", "Y[(size_t)m * N + n] = acc;"),
     "splitmix_gamma": ("0x9E3779B97F4A7C15ULL", "0x9E3779B97F4A7C16ULL"),
+    "argmax_ties_last_index": ("if (isnan(a) || a > b) best = v;", "if (isnan(a) || a >= b) best = v;"),
+    "tree_ignores_parent_validity": ("valid[i] = valid[p] && tokens[i] == g[p];", "valid[i] = tokens[i] == g[p];"),
+    "tree_compares_own_greedy": ("valid[i] = valid[p] && tokens[i] == g[p];", "valid[i] = valid[p] && tokens[i] == g[i];"),
+    "tree_ties_highest_index": ("if (valid[i] && depth[i] > depth[best]) best = i;",
+                                "if (valid[i] && depth[i] >= depth[best]) best = i;"),
+    "tree_bonus_from_parent": ("*bonus = g[best];", "*bonus = g[best > 0 ? parent[best] : 0];"),
 }
 
 
