@@ -3,7 +3,8 @@
 
 One step = one verify pass of a 9B-class decoder over M = 16 draft-tree
 tokens: for each of 32 layers the q, k, v, o, fused gate+up and down
-projections, then the LM head -- every activation input runs the rotation +
+projections, then the LM head and the acceptance of the 16-node draft tree
+from its logits -- every activation input runs the rotation +
 int8 quantization kernel once and every linear the W4A8 GEMM kernel of
 libhq.so (4-bit asymmetric weights, group 64).  q, k and v read the same
 input; by default their weights are packed as one [6144][4096] matrix and
@@ -310,6 +311,18 @@ class VerifyPass:
         self.algo_weight_bytes = sum(K * N * (0.5 + 4.5 / self.G) for _, K, N in self.linears)
         self.n_act = len(self.inputs)
         self.n_gemm = len(self.layers)
+        # the draft tree verified by the pass: 16 nodes, the root and three
+        # branches of depth 5 (parents listed first), drafted tokens seeded
+        self.parent = torch.tensor([-1, 0, 1, 2, 3, 4, 0, 6, 7, 8, 9, 0, 11, 12, 13, 14], dtype=torch.int32,
+                                   device=device)[: self.M]
+        gen = torch.Generator(device="cpu").manual_seed(cfg["seed"] + 77)
+        V = self.linears[-1][2]
+        self.tokens = torch.randint(0, V, (self.M,), generator=gen, dtype=torch.int32).to(device)
+        self.greedy = torch.empty(self.M, dtype=torch.int32, device=device)
+        self.path = torch.empty(self.M, dtype=torch.int32, device=device)
+        self.accept_out = torch.empty(2, dtype=torch.int32, device=device)
+        self.accept_ws = torch.empty(hq.hq_tree_accept_workspace_bytes(self.M, V), dtype=torch.uint8, device=device)
+        self.n_accept_kernels = 2
 
     def launch(self, act=True, gemm=True):
         hq = self.hq
@@ -322,6 +335,11 @@ class VerifyPass:
             if gemm:
                 layer = self.layers[li]
                 hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, self.M, self.ys[li], None, self.ws, self.flags)
+        if act and gemm:
+            # accept the draft tree from the LM head's logits
+            V = self.linears[-1][2]
+            hq.hq_tree_accept(self.ys[-1], self.M, V, self.parent, self.tokens, self.greedy, self.path,
+                              self.accept_out[0:1], self.accept_out[1:2], self.accept_ws, self.flags)
 
     def h2d_bytes(self):
         return sum(inp[2].numel() * 4 for inp in self.inputs)
@@ -445,6 +463,7 @@ def run_gpu(args, ranks: Ranks):
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": vp.M, "format": "w4_asym", "group": vp.G, "layers": 32,
                        "linears_per_pass": vp.n_gemm, "activation_inputs_per_pass": vp.n_act,
+                       "tree_accept": "16-node draft tree accepted from the LM head's logits each pass",
                        "qkv_fused": not args.no_fuse_qkv, "pdl": not args.no_pdl,
                        "weight_bytes_per_pass": vp.weight_bytes,
                        "l2": "inputs larger than L2: 3.875 GB of packed weights streamed per pass, L2 129 MB",
@@ -456,7 +475,7 @@ def run_gpu(args, ranks: Ranks):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks.summary(),
-            "gpu_launches": args.steps * (vp.n_act + vp.n_gemm),
+            "gpu_launches": args.steps * (vp.n_act + vp.n_gemm + vp.n_accept_kernels),
         }
         print(json.dumps(line))
     return 0

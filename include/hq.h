@@ -216,6 +216,34 @@ int hq_workspace_status(void *workspace, void *stream);
 int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
                            int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream);
 
+/* Draft-tree acceptance, after the verify pass (sections "Producing several
+ * tokens from one model pass": the main model checks the drafted positions
+ * together, accepts the valid prefix and adds its own token at the first
+ * position it does not confirm; and "Verifying a draft tree without restoring
+ * model state": on a tree, the longest valid path is accepted).
+ *   logits    fp32 [M][V], row i = the main model's output after tree node i
+ *   M         1..HQ_MAX_M tree nodes; node 0 is the root (the last committed
+ *             token)
+ *   parent    int32 [M], parent[0] ignored, 0 <= parent[i] < i otherwise
+ *   tokens    int32 [M], the drafted token of each node (tokens[0] ignored)
+ *   greedy    int32 [M] out: argmax of each row (lowest index among equal
+ *             maxima; a NaN ranks above every number, the first NaN wins)
+ *   path      int32 [M] out: the accepted drafted nodes from the root's child
+ *             down, n_accept of them; the other entries -1
+ *   n_accept  int32 out: accepted drafted tokens (the sequence advances by
+ *             n_accept + 1); -1 (and bonus -1) if parent is not a tree listed
+ *             parents-first
+ *   bonus     int32 out: greedy[accepted node], the main model's own token
+ *   workspace hq_tree_accept_workspace_bytes(M, V) bytes, 16-byte aligned
+ * A node i > 0 is valid when its parent is and tokens[i] == greedy[parent[i]];
+ * the deepest valid node is accepted, the lowest index among equally deep
+ * ones.  All pointers are device memory.  flags: HQ_LAUNCH_DEFAULT or
+ * HQ_LAUNCH_PDL. */
+size_t hq_tree_accept_workspace_bytes(int32_t M, int32_t V);
+int hq_tree_accept(const float *logits, int32_t M, int32_t V, const int32_t *parent, const int32_t *tokens,
+                   int32_t *greedy, int32_t *path, int32_t *n_accept, int32_t *bonus, void *workspace, uint32_t flags,
+                   void *stream);
+
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing will ever complete, giving up after
  * `limit_ns` nanoseconds (1000..100000000) and setting the error word of

@@ -227,3 +227,26 @@ int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream) {
 }
 
 }  // extern "C"
+
+extern "C" {
+
+size_t hq_tree_accept_workspace_bytes(int32_t M, int32_t V) {
+    if (M <= 0 || M > HQ_MAX_M || V <= 0) return 0;
+    return ((size_t)M * (size_t)hq::accept_chunks(V) * 8 + 15) / 16 * 16;
+}
+
+int hq_tree_accept(const float *logits, int32_t M, int32_t V, const int32_t *parent, const int32_t *tokens,
+                   int32_t *greedy, int32_t *path, int32_t *n_accept, int32_t *bonus, void *workspace, uint32_t flags,
+                   void *stream) {
+    if (M <= 0 || M > HQ_MAX_M || V <= 0) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (!logits || !parent || !tokens || !greedy || !path || !n_accept || !bonus || !workspace)
+        return HQ_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(parent, 4) || !aligned(tokens, 4) || !aligned(greedy, 4) ||
+        !aligned(path, 4) || !aligned(n_accept, 4) || !aligned(bonus, 4) || !aligned(workspace, 16))
+        return HQ_ERR_INVALID_ARG;
+    return cuda_status(hq::launch_tree_accept(logits, M, V, parent, tokens, greedy, path, n_accept, bonus, workspace,
+                                              (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -250,5 +250,11 @@ cudaError_t launch_unpack(const Geom &g, const void *blob, uint8_t *codes, float
 cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
                                int32_t *partials, void *workspace, bool pdl, cudaStream_t s);
 cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s);
+// Draft-tree acceptance: ACCEPT_CHUNK logits per thread block of the argmax.
+constexpr int ACCEPT_CHUNK = 8192;
+int accept_chunks(int V);
+cudaError_t launch_tree_accept(const float *logits, int M, int V, const int32_t *parent, const int32_t *tokens,
+                               int32_t *g_out, int32_t *path, int32_t *n_accept, int32_t *bonus, void *workspace,
+                               bool pdl, cudaStream_t s);
 int device_sm_count();
 }  // namespace hq

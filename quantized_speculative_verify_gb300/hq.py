@@ -30,7 +30,7 @@ HQ_MAX_M = 128
 FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 
 # Every symbol include/hq.h declares.
-EXPORTS = ("hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
+EXPORTS = ("hq_tree_accept_workspace_bytes", "hq_tree_accept", "hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
            "hq_make_signs",
            "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
            "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc")
@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         "hq_workspace_status": (ctypes.c_int, [P, P]),
         "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
         "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, I32, P, P, U32, P]),
+        "hq_tree_accept_workspace_bytes": (SZ, [I32, I32]),
+        "hq_tree_accept": (ctypes.c_int, [P, I32, I32, P, P, P, P, P, P, P, U32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -273,3 +275,26 @@ def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torc
     hq_rotate_quant_act(X, M, K, layer.signs, qx, qop, sx, flags, stream)
     hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, partials, ws, flags, stream)
     return Y
+
+
+def hq_tree_accept_workspace_bytes(M: int, V: int) -> int:
+    return int(load().hq_tree_accept_workspace_bytes(int(M), int(V)))
+
+
+def hq_tree_accept(logits, M: int, V: int, parent, tokens, greedy, path, n_accept, bonus, workspace, flags: int = 0,
+                   stream=None) -> None:
+    _check(load().hq_tree_accept(_ptr(logits), M, V, _ptr(parent), _ptr(tokens), _ptr(greedy), _ptr(path),
+                                 _ptr(n_accept), _ptr(bonus), _ptr(workspace), flags, _stream(stream)),
+           "hq_tree_accept")
+
+
+def tree_accept(logits: torch.Tensor, parent: torch.Tensor, tokens: torch.Tensor, flags: int = 0, stream=None):
+    """Greedy tokens, accepted path, number accepted and bonus token of a draft tree (device tensors)."""
+    M, V = logits.shape
+    dev = logits.device
+    greedy = torch.empty(M, dtype=torch.int32, device=dev)
+    path = torch.empty(M, dtype=torch.int32, device=dev)
+    out = torch.empty(2, dtype=torch.int32, device=dev)
+    ws = torch.empty(hq_tree_accept_workspace_bytes(M, V), dtype=torch.uint8, device=dev)
+    hq_tree_accept(logits, M, V, parent, tokens, greedy, path, out[0:1], out[1:2], ws, flags, stream)
+    return greedy, path, out

@@ -150,3 +150,18 @@ def test_empty_batch_is_a_no_op():
     # M = 0: nothing to do, nothing launched, pointers never touched
     assert lib.hq_rotate_quant_act(None, 0, 256, None, None, None, None, 0, None) == hq.HQ_OK
     assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK
+
+
+def test_tree_accept_sizes_and_validation():
+    lib = hq.load()
+    assert hq.hq_tree_accept_workspace_bytes(16, 151552) == 16 * 19 * 8
+    assert hq.hq_tree_accept_workspace_bytes(0, 100) == 0 and hq.hq_tree_accept_workspace_bytes(129, 100) == 0
+    assert hq.hq_tree_accept_workspace_bytes(4, 0) == 0
+    E = hq.HQ_ERR_INVALID_ARG
+    args = [FAKE, 4, 100, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None]
+    assert lib.hq_tree_accept(*args[:1], 0, *args[2:]) == E          # M = 0
+    assert lib.hq_tree_accept(*args[:1], 129, *args[2:]) == E        # M > HQ_MAX_M
+    assert lib.hq_tree_accept(*args[:2], 0, *args[3:]) == E          # V = 0
+    assert lib.hq_tree_accept(None, *args[1:]) == E
+    assert lib.hq_tree_accept(*args[:9], FAKE + 8, 0, None) == E     # workspace alignment
+    assert lib.hq_tree_accept(*args[:10], 2, None) == E              # unknown flag

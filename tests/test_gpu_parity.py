@@ -350,3 +350,58 @@ def test_workload_decoder_9b_each_shape():
         check_full_layer(K, N, cfg["G"], cfg["fmt"], cfg["M"], synth.layer_seed(cfg["seed"], i), cfg["w"], cfg["x"],
                          count=256)
         torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------- tree acceptance ---
+def random_tree(rng, M, branchy):
+    if branchy:
+        return np.array([-1] + [int(rng.integers(0, i)) for i in range(1, M)], dtype=np.int32)
+    return np.arange(-1, M - 1, dtype=np.int32)  # a chain
+
+
+def gpu_accept(L, parent, tokens, flags=0):
+    greedy, path, out = hq.tree_accept(torch.from_numpy(L).to(DEV), torch.from_numpy(parent).to(DEV),
+                                       torch.from_numpy(tokens).to(DEV), flags=flags)
+    torch.cuda.synchronize()
+    return greedy.cpu().numpy(), path.cpu().numpy(), int(out[0].item()), int(out[1].item())
+
+
+@pytest.mark.parametrize("M,V,branchy", [(1, 1, False), (5, 7, False), (16, 151552, True), (16, 151552, False),
+                                         (128, 8193, True), (33, 32003, True), (16, 8192, False)])
+def test_tree_accept_matches_oracle(M, V, branchy):
+    rng = np.random.default_rng(M * 1000 + V)
+    # integer-valued logits: many ties, so the lowest-index rule is exercised
+    L = rng.integers(-50, 50, size=(M, V)).astype(np.float32)
+    L[:, int(rng.integers(0, V))] = 60.0
+    if V > 10:
+        L[0, 3] = np.nan if M > 1 else L[0, 3]
+        L[min(1, M - 1), 5] = np.inf
+        L[M - 1] = -0.0
+        L[M - 1, V // 2] = 0.0
+    parent = random_tree(rng, M, branchy)
+    g_ref = oracle.argmax_rows(L)
+    # drafts agree with the main model with probability 3/4
+    tokens = np.where(rng.random(M) < 0.75, g_ref[np.maximum(parent, 0)], rng.integers(0, V, size=M)).astype(np.int32)
+    path_ref, n_ref, bonus_ref = oracle.tree_accept(g_ref, parent, tokens)
+    g, path, n, bonus = gpu_accept(L, parent, tokens, flags=hq.HQ_LAUNCH_PDL)
+    assert np.array_equal(g, g_ref)
+    assert n == n_ref and bonus == bonus_ref
+    assert np.array_equal(path[:n], path_ref) and (path[n:] == -1).all()
+
+
+def test_tree_accept_page_example():
+    # five drafted tokens, the main model agrees with the first four: the pass advances five
+    V = 64
+    L = np.zeros((6, V), dtype=np.float32)
+    for i, tok in enumerate([21, 22, 23, 24, 25, 26]):
+        L[i, tok] = 1.0
+    parent = np.arange(-1, 5, dtype=np.int32)
+    tokens = np.array([11, 21, 22, 23, 24, 40], dtype=np.int32)
+    g, path, n, bonus = gpu_accept(L, parent, tokens)
+    assert list(path[:n]) == [1, 2, 3, 4] and n + 1 == 5 and bonus == 25
+
+
+def test_tree_accept_reports_bad_parent():
+    L = np.zeros((3, 10), dtype=np.float32)
+    g, path, n, bonus = gpu_accept(L, np.array([-1, 2, 0], dtype=np.int32), np.zeros(3, dtype=np.int32))
+    assert n == -1 and bonus == -1
