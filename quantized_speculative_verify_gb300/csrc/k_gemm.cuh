@@ -422,82 +422,122 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     }
 
     // Split n-blocks: every contributor arrives, waits until all contributors
-    // of the n-block have arrived, then sums its share of the n-block's
+    // of the n-block have arrived, then sums its 1/nc share of the n-block's
     // outputs over all contributors' partial sums in ascending K order (slot 0
     // of a contributor is its first segment, slot 1 its last), multiplies by
-    // the row scale and writes Y.  The wait is safe because every thread block
-    // of the launch is resident: the grid never exceeds the blocks that fit
-    // on the device at once, and dependent kernels are launched only after
-    // every block of this one has started.  The last contributor to finish
-    // resets the n-block's two counters for the next call.
+    // the row scale and writes Y.  The wait is safe because every thread
+    // block of the launch is resident: the grid never exceeds the blocks that
+    // fit on the device at once, and dependent kernels are launched only
+    // after every block of this one has started.  The last contributor to
+    // finish resets the n-block's two counters for the next call.  Threads 0
+    // and 1 serve the two pending n-blocks at the same time.
     if (pend0 >= 0 || pend1 >= 0) {
         int *done = ctr + a.NB;
-        // Publish: the barrier orders every consumer thread's partial-sum
-        // stores before thread 0's release; both arrivals go out together.
+        // every consumer thread's partial-sum stores precede the arrivals
         named_barrier(1, NCW * 32);
-        if (threadIdx.x == 0) {
-            if (pend0 >= 0) red_add_release_gpu(&ctr[pend0], 1);
-            if (pend1 >= 0) red_add_release_gpu(&ctr[pend1], 1);
+        int my_bb = -1, my_nc = 0, done_before = 0;
+        if (threadIdx.x < 2) {
+            my_bb = threadIdx.x == 0 ? pend0 : pend1;
+            if (my_bb >= 0) {
+                my_nc = cta_of_tile(my_bb * KTILES + KTILES - 1, a.T, a.grid) -
+                        cta_of_tile(my_bb * KTILES, a.T, a.grid) + 1;
+                red_add_release_gpu(&ctr[my_bb], 1);
+                if (ok) ok = wait_count_bounded(&ctr[my_bb], my_nc, err);
+                // passed the wait: count it now, the answer arrives during the sums
+                done_before = atomicAdd(&done[my_bb], 1);
+            }
         }
+        // the acquires of threads 0 and 1 are ordered before every thread's loads below
+        named_barrier(1, NCW * 32);
+        // Shares of both pending n-blocks as one list of 4-channel output
+        // groups (n0 from the first, then the second); two groups per
+        // iteration, with all their loads in flight together.
+        const int total = M * (BN / 4);
+        int e_lo[2], e_cnt[2], e_clo[2], e_chi[2], e_slot[2];
+#pragma unroll
         for (int p = 0; p < 2; ++p) {
             const int bb = p == 0 ? pend0 : pend1;
+            e_cnt[p] = 0;
+            e_lo[p] = e_clo[p] = e_chi[p] = e_slot[p] = 0;
             if (bb < 0) continue;
             const int c_lo = cta_of_tile(bb * KTILES, a.T, a.grid);
             const int c_hi = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid);
             const int nc = c_hi - c_lo + 1;
-            int done_before = 0;
-            if (threadIdx.x == 0) {
-                if (ok) ok = wait_count_bounded(&ctr[bb], nc, err);
-                // passed the wait: count it now, the answer arrives during the sums
-                done_before = atomicAdd(&done[bb], 1);
-            }
-            // thread 0's acquire is ordered before every thread's loads below
-            named_barrier(1, NCW * 32);
-            // Every contributor after the first starts inside this n-block, so it
-            // is their first n-block (slot 0); the first contributor used slot 1
-            // if it started in an earlier n-block.
-            const int slot_lo = tile_begin(c_lo, a.T, a.grid) < bb * KTILES ? 1 : 0;
-            // this contributor's share: outputs [lo, hi) in units of 4 channels
-            const int total = M * (BN / 4);
             const int per = (total + nc - 1) / nc;
             const int lo = (blockIdx.x - c_lo) * per;
             const int hi = lo + per < total ? lo + per : total;
-            for (int gi = lo + (int)threadIdx.x; gi < hi; gi += NCW * 32) {
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                // up to 8 contributors' loads in flight, added in contributor order
-                for (int cc = c_lo; cc <= c_hi; cc += 8) {
-                    float4 x[8];
+            e_lo[p] = lo;
+            e_cnt[p] = hi > lo ? hi - lo : 0;
+            e_clo[p] = c_lo;
+            e_chi[p] = c_hi;
+            // Every contributor after the first starts inside this n-block, so
+            // it is their first n-block (slot 0); the first contributor used
+            // slot 1 if it started in an earlier n-block.
+            e_slot[p] = tile_begin(c_lo, a.T, a.grid) < bb * KTILES ? 1 : 0;
+        }
+        const int n_all = e_cnt[0] + e_cnt[1];
+        for (int base = 0; base < n_all; base += 2 * NCW * 32) {
+            float4 sum[2];
+            int gis[2], ps[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int idx = base + h * NCW * 32 + (int)threadIdx.x;
+                ps[h] = idx < e_cnt[0] ? 0 : (idx < n_all ? 1 : -1);
+                gis[h] = ps[h] == 0 ? e_lo[0] + idx : (ps[h] == 1 ? e_lo[1] + idx - e_cnt[0] : 0);
+                sum[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const int span = (ps[0] >= 0 ? e_chi[ps[0]] - e_clo[ps[0]] + 1 : 0) >
+                                     (ps[1] >= 0 ? e_chi[ps[1]] - e_clo[ps[1]] + 1 : 0)
+                                 ? (ps[0] >= 0 ? e_chi[ps[0]] - e_clo[ps[0]] + 1 : 0)
+                                 : (ps[1] >= 0 ? e_chi[ps[1]] - e_clo[ps[1]] + 1 : 0);
+            // up to 8 contributors of each group in flight, added in contributor order
+            for (int cc = 0; cc < span; cc += 8) {
+                float4 x[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int p = ps[h];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
-                        const int c2 = cc + v;
-                        const int sl = c2 == c_lo ? slot_lo : 0;
-                        if (c2 <= c_hi)
-                            x[v] = __ldcg(reinterpret_cast<const float4 *>(
-                                wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats() + (size_t)gi * 4));
-                    }
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        if (cc + v > c_hi) break;
-                        sum.x = __fadd_rn(sum.x, x[v].x);
-                        sum.y = __fadd_rn(sum.y, x[v].y);
-                        sum.z = __fadd_rn(sum.z, x[v].z);
-                        sum.w = __fadd_rn(sum.w, x[v].w);
+                        if (p < 0) continue;
+                        const int c2 = e_clo[p] + cc + v;
+                        const int sl = cc + v == 0 ? e_slot[p] : 0;
+                        if (c2 <= e_chi[p])
+                            x[h][v] = __ldcg(reinterpret_cast<const float4 *>(
+                                wsp + ((size_t)c2 * 2 + sl) * ws_slot_floats() + (size_t)gis[h] * 4));
                     }
                 }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int p = ps[h];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        if (p < 0 || e_clo[p] + cc + v > e_chi[p]) continue;
+                        sum[h].x = __fadd_rn(sum[h].x, x[h][v].x);
+                        sum[h].y = __fadd_rn(sum[h].y, x[h][v].y);
+                        sum[h].z = __fadd_rn(sum[h].z, x[h][v].z);
+                        sum[h].w = __fadd_rn(sum[h].w, x[h][v].w);
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (ps[h] < 0) continue;
+                const int bb = ps[h] == 0 ? pend0 : pend1;
+                const int gi = gis[h];
                 const int tok = gi / (BN / 4), r4 = (gi - tok * (BN / 4)) * 4;
                 const float sxt = __ldg(sxm + tok);
                 const int n = bb * BN + r4;
                 float *yr = Ym + (size_t)tok * N;
-                if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum.x);
-                if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum.y);
-                if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum.z);
-                if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum.w);
+                if (n + 0 < N) yr[n + 0] = __fmul_rn(sxt, sum[h].x);
+                if (n + 1 < N) yr[n + 1] = __fmul_rn(sxt, sum[h].y);
+                if (n + 2 < N) yr[n + 2] = __fmul_rn(sxt, sum[h].z);
+                if (n + 3 < N) yr[n + 3] = __fmul_rn(sxt, sum[h].w);
             }
-            // every contributor has passed its wait once all have counted
-            if (threadIdx.x == 0 && done_before == nc - 1) {
-                atomicExch(&ctr[bb], 0);
-                atomicExch(&done[bb], 0);
-            }
+        }
+        // every contributor has passed its wait once all have counted
+        if (my_bb >= 0 && done_before == my_nc - 1) {
+            atomicExch(&ctr[my_bb], 0);
+            atomicExch(&done[my_bb], 0);
         }
     }
 }
