@@ -89,19 +89,15 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
     }
 
-    // row absmax: warp, then block
+    // row absmax: warp, then every warp reduces the warps' maxima itself
+    // (one block barrier)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) s_red[tid >> 5] = amax;
     __syncthreads();
-    if (tid < 32) {
-        float a = tid < T / 32 ? s_red[tid] : 0.0f;
+    float a = lane < T / 32 ? s_red[lane] : 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (tid == 0) s_red[0] = a;
-    }
-    __syncthreads();
-    const float a = s_red[0];
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     const float s = a == 0.0f ? 0.0f : __fdiv_rn(a, 127.0f);
     if (tid == 0) sx[row] = s;
 
@@ -153,11 +149,15 @@ cudaError_t launch_act_t(const float *X, int M, int K, const uint32_t *signs, in
 
 cudaError_t launch_rotate_quant_act(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop,
                                     float *sx, bool pdl, cudaStream_t s) {
+    // As many threads per row as the row has float4s, up to 1024: the kernel
+    // is latency-bound (one block per row), so the shortest chain per thread
+    // wins (256 threads x 4 float4s at K = 4096 made the pass 4% slower).
     const int n4 = K / 4;
     if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 256 * 2) return launch_act_t<2, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 256 * 4) return launch_act_t<4, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 512 * 4) return launch_act_t<4, 512>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
     if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
     if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
     if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);

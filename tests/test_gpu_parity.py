@@ -89,7 +89,8 @@ def signs_pair(seed, K):
 
 # ------------------------------------------------------- activations ---
 ACT_CASES = [(1, 32, 32), (3, 64, 16), (16, 256, 32), (17, 256, 64), (16, 4096, 64), (32, 4096, 128),
-             (7, 4096, 256), (16, 12288, 64), (128, 4096, 16), (64, 8192, 128), (5, 96, 32), (2, 40960, 256)]
+             (7, 4096, 256), (16, 12288, 64), (128, 4096, 16), (64, 8192, 128), (5, 96, 32), (2, 40960, 256),
+             (4, 2048, 64), (3, 16384, 128), (2, 32768, 256), (9, 1024, 32)]
 
 
 @pytest.mark.parametrize("M,K,G", ACT_CASES)
