@@ -95,6 +95,10 @@ def _load(openmp: bool = False) -> ctypes.CDLL:
         lib.or_num_threads.argtypes = []
         lib.or_argmax_rows.argtypes = [_P, _I, _I, _P]
         lib.or_tree_accept.argtypes = [_P, _P, _P, _I, _P, _P, _P]
+        lib.or_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.or_half_to_double.restype = ctypes.c_double
+        lib.or_tree_attention.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_double, _P]
+        lib.or_tree_commit_kv.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I]
         _libs[openmp] = lib
         return lib
 
@@ -302,3 +306,41 @@ def tree_accept(g: np.ndarray, parent: np.ndarray, tokens: np.ndarray):
     _check(_load().or_tree_accept(_ptr(g), _ptr(parent), _ptr(tokens), M, _ptr(path), _ptr(n), _ptr(bonus)),
            "tree_accept")
     return path[: int(n[0])], int(n[0]), int(bonus[0])
+
+
+def half_to_double(bits: int) -> float:
+    """Value of an IEEE binary16 bit pattern."""
+    return float(_load().or_half_to_double(int(bits) & 0xFFFF))
+
+
+def tree_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, L: int, parent: np.ndarray, scale: float,
+                   openmp: bool = False) -> np.ndarray:
+    """Tree-masked attention of the M tree nodes (fp64).
+
+    q float16 [M][Hq][D]; k, v float16 [Hkv][cap][D] with the committed
+    positions [0, L) and the tree nodes at [L, L + M); parent int32 [M].
+    Returns float64 [M][Hq][D]."""
+    q16 = _c(q, np.float16)
+    k16, v16 = _c(k, np.float16), _c(v, np.float16)
+    M, Hq, D = q16.shape
+    Hkv, cap, D2 = k16.shape
+    if D2 != D or v16.shape != k16.shape:
+        raise ValueError("shape mismatch")
+    par = _c(parent, np.int32)
+    out = np.empty((M, Hq, D), dtype=np.float64)
+    _check(_load(openmp).or_tree_attention(_ptr(q16.view(np.uint16)), _ptr(k16.view(np.uint16)),
+                                           _ptr(v16.view(np.uint16)), cap, L, M, Hq, Hkv, D, _ptr(par),
+                                           float(scale), _ptr(out)), "tree_attention")
+    return out
+
+
+def tree_commit_kv(k: np.ndarray, v: np.ndarray, L: int, path: np.ndarray, n_accept: int):
+    """Copies of k and v [Hkv][cap][D] after moving the accepted path next to the root."""
+    k16, v16 = np.array(k, dtype=np.float16, order="C"), np.array(v, dtype=np.float16, order="C")
+    Hkv, cap, D = k16.shape
+    p = _c(np.asarray(path).reshape(-1), np.int32)
+    if p.size == 0:
+        p = np.zeros(1, dtype=np.int32)
+    _check(_load().or_tree_commit_kv(_ptr(k16.view(np.uint16)), _ptr(v16.view(np.uint16)), cap, L, Hkv, D,
+                                     _ptr(p), int(n_accept)), "tree_commit_kv")
+    return k16, v16

@@ -482,6 +482,134 @@ int or_tree_accept(const int32_t *g, const int32_t *parent, const int32_t *token
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Tree-masked verify attention (section "Verifying a draft tree without    */
+/* restoring model state": an attention layer keeps a cache of every past  */
+/* token; the main model checks every branch of the draft tree in one pass */
+/* and changes its committed state only for the accepted path).  The page  */
+/* gives no mask and no formula.  Readings:                                */
+/*   A1  the M tree nodes are processed in this pass; their keys and values */
+/*       sit in the cache right after the L committed positions (node j at  */
+/*       position L + j);                                                   */
+/*   A2  node i attends to the L committed positions, to every ancestor of  */
+/*       i and to i itself: exactly the prefix its own branch would have    */
+/*       had if decoded alone (the plainest mask; siblings and cousins are  */
+/*       not visible);                                                      */
+/*   A3  the ancestor walk follows parent[] while the parent lies in        */
+/*       [0, node); a parent outside that range ends the walk (the root,    */
+/*       node 0, has none);                                                 */
+/*   A4  attention itself is the textbook one: s = scale * (q . k),         */
+/*       softmax over the visible positions, output = sum_j p_j v_j, with   */
+/*       grouped heads: query head h reads key/value head h / (Hq / Hkv);   */
+/*   A5  q, k, v are IEEE binary16 values; the arithmetic here is double.   */
+/* Commit (section above: state is committed only along the chosen path):  */
+/*   A6  the root stays at position L; accepted node path[d] (depth d + 1)  */
+/*       moves to position L + 1 + d, for d < n_accept; nothing moves when  */
+/*       n_accept <= 0.                                                     */
+/* ------------------------------------------------------------------------ */
+double or_half_to_double(uint16_t h)
+{
+    const int sgn = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);   /* (1 + m/1024) * 2^(e-15) */
+    return sgn ? -v : v;
+}
+
+/* vis[i * M + j] = 1 when tree node j is visible to node i (A2, A3). */
+static void or_tree_visibility(const int32_t *parent, int M, unsigned char *vis)
+{
+    for (int i = 0; i < M; ++i) {
+        for (int j = 0; j < M; ++j) vis[(size_t)i * M + j] = 0;
+        vis[(size_t)i * M + i] = 1;
+        int cur = i;
+        while (cur > 0) {
+            const int p = parent[cur];
+            if (p < 0 || p >= cur) break;
+            vis[(size_t)i * M + p] = 1;
+            cur = p;
+        }
+    }
+}
+
+/* q [M][Hq][D], k and v [Hkv][cap][D] (binary16 bit patterns), out [M][Hq][D]. */
+int or_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, int cap, int L, int M, int Hq,
+                      int Hkv, int D, const int32_t *parent, double scale, double *out)
+{
+    if (M < 1 || L < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0 || cap < L + M) return 1;
+    const int G = Hq / Hkv;
+    unsigned char *vis = (unsigned char *)malloc((size_t)M * (size_t)M);
+    if (!vis) return 2;
+    or_tree_visibility(parent, M, vis);
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic)
+    for (int r = 0; r < M * Hq; ++r) {
+        const int i = r / Hq, h = r % Hq, hk = h / G;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L + M));
+        int *pos = (int *)malloc(sizeof(int) * (size_t)(L + M));
+        if (!s || !pos) {
+            free(s);
+            free(pos);
+            fail = 1;
+            continue;
+        }
+        int n = 0;
+        for (int t = 0; t < L; ++t) pos[n++] = t;
+        for (int j = 0; j < M; ++j)
+            if (vis[(size_t)i * M + j]) pos[n++] = L + j;
+        const uint16_t *qr = q + ((size_t)i * Hq + h) * D;
+        double m = -INFINITY;
+        for (int a = 0; a < n; ++a) {
+            const uint16_t *kr = k + ((size_t)hk * cap + pos[a]) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += or_half_to_double(qr[d]) * or_half_to_double(kr[d]);
+            s[a] = scale * dot;
+            if (s[a] > m) m = s[a];
+        }
+        double den = 0.0;
+        for (int a = 0; a < n; ++a) {
+            s[a] = exp(s[a] - m);
+            den += s[a];
+        }
+        double *o = out + ((size_t)i * Hq + h) * D;
+        for (int d = 0; d < D; ++d) {
+            double num = 0.0;
+            for (int a = 0; a < n; ++a) num += s[a] * or_half_to_double(v[((size_t)hk * cap + pos[a]) * D + d]);
+            o[d] = num / den;
+        }
+        free(s);
+        free(pos);
+    }
+    free(vis);
+    return fail ? 2 : 0;
+}
+
+/* In place on k and v [Hkv][cap][D] (A6). */
+int or_tree_commit_kv(uint16_t *k, uint16_t *v, int cap, int L, int Hkv, int D, const int32_t *path, int n_accept)
+{
+    if (n_accept <= 0) return 0;
+    if (L < 0 || Hkv < 1 || D < 1 || L + 1 + n_accept > cap) return 1;
+    for (int d = 0; d < n_accept; ++d)
+        if (path[d] < 1 || L + path[d] >= cap) return 1;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n_accept * (size_t)D);
+    if (!tmp) return 2;
+    for (int which = 0; which < 2; ++which) {
+        uint16_t *c = which == 0 ? k : v;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int d = 0; d < n_accept; ++d)
+                memcpy(tmp + (size_t)d * D, c + ((size_t)h * cap + L + path[d]) * D, sizeof(uint16_t) * (size_t)D);
+            for (int d = 0; d < n_accept; ++d)
+                memcpy(c + ((size_t)h * cap + L + 1 + d) * D, tmp + (size_t)d * D, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    free(tmp);
+    return 0;
+}
+
 int or_num_threads(void)
 {
 #ifdef _OPENMP

@@ -518,3 +518,169 @@ def test_tree_accept_rejects_bad_parents():
     for parent in ([-1, 1, 0], [-1, 0, 2], [-1, -1, 0]):
         with pytest.raises(ValueError):
             oracle.tree_accept(g, np.array(parent, dtype=np.int32), np.zeros(3, dtype=np.int32))
+
+
+# ------------------------------------------------------ tree attention ---
+# Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling",
+# section "Verifying a draft tree without restoring model state": the main
+# model checks every branch of the draft tree in one pass; an attention layer
+# reads its cache of past tokens.  Reading: a node sees the committed cache,
+# its ancestors and itself.
+
+def _attn_inputs(rng, M, Hq, Hkv, D, L, extra=0, vscale=1.0):
+    q = (rng.standard_normal((M, Hq, D)) * 0.5).astype(np.float16)
+    k = (rng.standard_normal((Hkv, L + M + extra, D)) * 0.5).astype(np.float16)
+    v = (rng.standard_normal((Hkv, L + M + extra, D)) * vscale).astype(np.float16)
+    return q, k, v
+
+
+def _random_tree(rng, M):
+    par = np.zeros(M, dtype=np.int32)
+    for i in range(1, M):
+        par[i] = rng.integers(0, i)
+    return par
+
+
+def _dense_reference(q, k, v, L, parent, scale):
+    """Masked softmax attention with the tree mask from a boolean transitive
+    closure (repeated squaring of the parent relation), numpy fp64 einsum."""
+    M, Hq, D = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    A = np.zeros((M, M), dtype=bool)  # A[i, j]: j is the parent of i
+    for i in range(1, M):
+        if 0 <= parent[i] < i:
+            A[i, parent[i]] = True
+    R = A | np.eye(M, dtype=bool)
+    for _ in range(int(np.ceil(np.log2(max(M, 2)))) + 1):
+        R = R | ((R.astype(np.int64) @ R.astype(np.int64)) > 0)
+    mask = np.concatenate([np.ones((M, L), dtype=bool), R], axis=1)  # [M][L + M]
+    qd, kd, vd = q.astype(np.float64), k[:, : L + M].astype(np.float64), v[:, : L + M].astype(np.float64)
+    kh = np.repeat(kd, G, axis=0)  # [Hq][L+M][D]
+    vh = np.repeat(vd, G, axis=0)
+    s = scale * np.einsum("ihd,htd->iht", qd, kh)
+    s = np.where(mask[:, None, :], s, -np.inf)
+    s = s - s.max(axis=2, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=2, keepdims=True)
+    return np.einsum("iht,htd->ihd", p, vh)
+
+
+def test_half_decoding_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    for b in bits:
+        got = oracle.half_to_double(int(b))
+        r = ref[int(b)]
+        assert (np.isnan(got) and np.isnan(r)) or got == r, hex(int(b))
+
+
+@pytest.mark.parametrize("L,M", [(0, 1), (0, 6), (5, 4), (33, 9)])
+def test_tree_attention_chain_is_causal_attention(L, M):
+    """A chain (node i's parent is i-1) is ordinary causal decoding of L + M
+    tokens: torch's scaled_dot_product_attention (fp64, CPU) with a causal
+    mask offset by L."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(L * 31 + M)
+    Hq = Hkv = 2
+    D = 16
+    q, k, v = _attn_inputs(rng, M, Hq, Hkv, D, L)
+    parent = np.maximum(np.arange(M, dtype=np.int32) - 1, 0)
+    scale = 1.0 / np.sqrt(D)
+    got = oracle.tree_attention(q, k, v, L, parent, scale)
+    Q = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)        # [H][M][D]
+    K = torch.from_numpy(k[:, : L + M].astype(np.float64))              # [H][L+M][D]
+    V = torch.from_numpy(v[:, : L + M].astype(np.float64))
+    mask = torch.ones(M, L + M, dtype=torch.bool).tril(diagonal=L)
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(got, ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tree_attention_matches_dense_closure_reference(seed):
+    rng = np.random.default_rng(100 + seed)
+    M, Hq, Hkv, D, L = int(rng.integers(2, 20)), 8, 2, 12, int(rng.integers(0, 40))
+    q, k, v = _attn_inputs(rng, M, Hq, Hkv, D, L, extra=3)
+    parent = _random_tree(rng, M)
+    got = oracle.tree_attention(q, k, v, L, parent, 0.37)
+    np.testing.assert_allclose(got, _dense_reference(q, k, v, L, parent, 0.37), rtol=1e-12, atol=1e-12)
+
+
+def test_tree_attention_star_tree_sees_root_and_itself():
+    """Every drafted node a child of the root: node i sees the cache, the root
+    and itself, never its siblings (closed form for L = 0: a two-key softmax)."""
+    rng = np.random.default_rng(7)
+    M, H, D = 6, 1, 4
+    q, k, v = _attn_inputs(rng, M, H, H, D, 0)
+    parent = np.zeros(M, dtype=np.int32)
+    got = oracle.tree_attention(q, k, v, 0, parent, 1.0)
+    qd, kd, vd = q.astype(np.float64)[:, 0], k.astype(np.float64)[0], v.astype(np.float64)[0]
+    assert np.array_equal(got[0, 0], vd[0])  # the root sees only itself
+    for i in range(1, M):
+        s0, si = qd[i] @ kd[0], qd[i] @ kd[i]
+        w0 = 1.0 / (1.0 + np.exp(si - s0))
+        np.testing.assert_allclose(got[i, 0], w0 * vd[0] + (1 - w0) * vd[i], rtol=1e-13, atol=1e-14)
+
+
+def test_tree_attention_zero_scale_is_the_mean_of_visible_values():
+    rng = np.random.default_rng(8)
+    M, Hq, Hkv, D, L = 7, 4, 4, 5, 3
+    q, k, v = _attn_inputs(rng, M, Hq, Hkv, D, L)
+    parent = np.array([0, 0, 1, 2, 0, 4, 2], dtype=np.int32)
+    got = oracle.tree_attention(q, k, v, L, parent, 0.0)
+    anc = {0: [0], 1: [0, 1], 2: [0, 1, 2], 3: [0, 1, 2, 3], 4: [0, 4], 5: [0, 4, 5], 6: [0, 1, 2, 6]}
+    for i in range(M):
+        cols = list(range(L)) + [L + j for j in anc[i]]
+        np.testing.assert_allclose(got[i], v[:, cols].astype(np.float64).mean(axis=1), rtol=1e-14, atol=1e-15)
+
+
+def test_tree_attention_grouped_heads_equal_repeated_kv_heads():
+    rng = np.random.default_rng(9)
+    M, Hq, Hkv, D, L = 5, 8, 2, 6, 11
+    q, k, v = _attn_inputs(rng, M, Hq, Hkv, D, L)
+    parent = np.array([0, 0, 1, 1, 3], dtype=np.int32)
+    got = oracle.tree_attention(q, k, v, L, parent, 0.5)
+    rep = oracle.tree_attention(q, np.repeat(k, Hq // Hkv, axis=0), np.repeat(v, Hq // Hkv, axis=0), L, parent, 0.5)
+    np.testing.assert_allclose(got, rep, rtol=0, atol=0)
+
+
+def test_tree_attention_ignores_the_order_of_committed_positions():
+    rng = np.random.default_rng(10)
+    M, Hq, Hkv, D, L = 4, 2, 1, 8, 9
+    q, k, v = _attn_inputs(rng, M, Hq, Hkv, D, L)
+    parent = np.array([0, 0, 1, 0], dtype=np.int32)
+    perm = np.concatenate([rng.permutation(L), np.arange(L, L + M)])
+    a = oracle.tree_attention(q, k, v, L, parent, 0.7)
+    b = oracle.tree_attention(q, k[:, perm], v[:, perm], L, parent, 0.7)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+
+
+def test_tree_attention_invalid_parent_ends_the_ancestor_walk():
+    rng = np.random.default_rng(11)
+    M, H, D, L = 4, 1, 4, 2
+    q, k, v = _attn_inputs(rng, M, H, H, D, L)
+    parent = np.array([0, 0, 3, 2], dtype=np.int32)  # node 2's parent is not before it
+    got = oracle.tree_attention(q, k, v, L, parent, 1.0)
+    # node 2 sees the cache and itself; node 3 sees the cache, node 2 and itself
+    ref = _dense_reference(q, k, v, L, np.array([0, 0, -1, 2], dtype=np.int32), 1.0)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_tree_commit_kv_moves_the_accepted_path_next_to_the_root():
+    rng = np.random.default_rng(12)
+    Hkv, L, M, D = 3, 5, 8, 4
+    cap = L + M + 2
+    k = rng.standard_normal((Hkv, cap, D)).astype(np.float16)
+    v = rng.standard_normal((Hkv, cap, D)).astype(np.float16)
+    path = np.array([2, 5, 7], dtype=np.int32)  # node 2 at depth 1, 5 at depth 2, 7 at depth 3
+    k2, v2 = oracle.tree_commit_kv(k, v, L, path, 3)
+    for d, node in enumerate(path):
+        assert np.array_equal(k2[:, L + 1 + d], k[:, L + node]) and np.array_equal(v2[:, L + 1 + d], v[:, L + node])
+    untouched = [t for t in range(cap) if not (L + 1 <= t < L + 4)]
+    assert np.array_equal(k2[:, untouched], k[:, untouched]) and np.array_equal(v2[:, untouched], v[:, untouched])
+    # a chain path is already in place; no accepted node or a bad tree moves nothing
+    kc, vc = oracle.tree_commit_kv(k, v, L, np.array([1, 2, 3], dtype=np.int32), 3)
+    assert np.array_equal(kc, k) and np.array_equal(vc, v)
+    for n in (0, -1):
+        kn, vn = oracle.tree_commit_kv(k, v, L, path, n)
+        assert np.array_equal(kn, k) and np.array_equal(vn, v)

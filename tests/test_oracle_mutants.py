@@ -43,6 +43,18 @@ MUTANTS = {
     "tree_ties_highest_index": ("if (valid[i] && depth[i] > depth[best]) best = i;",
                                 "if (valid[i] && depth[i] >= depth[best]) best = i;"),
     "tree_bonus_from_parent": ("*bonus = g[best];", "*bonus = g[best > 0 ? parent[best] : 0];"),
+    "half_exponent_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "half_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "attn_node_does_not_see_itself": ("vis[(size_t)i * M + i] = 1;", "vis[(size_t)i * M + i] = (i == 0);"),
+    "attn_sees_every_tree_node": ("if (vis[(size_t)i * M + j]) pos[n++] = L + j;", "pos[n++] = L + j;"),
+    "attn_walk_stops_at_parent": ("vis[(size_t)i * M + p] = 1;\n            cur = p;",
+                                  "vis[(size_t)i * M + p] = 1;\n            break;"),
+    "attn_cache_drops_last_position": ("for (int t = 0; t < L; ++t) pos[n++] = t;",
+                                       "for (int t = 0; t + 1 < L; ++t) pos[n++] = t;"),
+    "attn_ignores_scale": ("s[a] = scale * dot;", "s[a] = dot;"),
+    "attn_kv_head_modulo": ("const int i = r / Hq, h = r % Hq, hk = h / G;",
+                            "const int i = r / Hq, h = r % Hq, hk = h % Hkv;"),
+    "commit_overwrites_root": ("memcpy(c + ((size_t)h * cap + L + 1 + d) * D,", "memcpy(c + ((size_t)h * cap + L + d) * D,"),
 }
 
 
