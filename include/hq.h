@@ -244,6 +244,50 @@ int hq_tree_accept(const float *logits, int32_t M, int32_t V, const int32_t *par
                    int32_t *greedy, int32_t *path, int32_t *n_accept, int32_t *bonus, void *workspace, uint32_t flags,
                    void *stream);
 
+/* Tree-masked verify attention (section "Verifying a draft tree without
+ * restoring model state": an attention layer keeps a cache of every past
+ * token, and the main model checks every branch of the draft tree in one pass
+ * without changing its committed state).  The page gives no mask; node i
+ * attends to the L committed positions, to its ancestors and to itself (the
+ * prefix its branch would have had if decoded alone).  The ancestor walk
+ * follows parent[] while the parent lies in [0, node); a parent outside that
+ * range ends it.  Textbook softmax attention with grouped heads: query head h
+ * reads key/value head h / (Hq / Hkv).
+ *   q        fp16 [M][Hq][D], the tree nodes' queries
+ *   k_cache  fp16 [Hkv][cap][D]: positions [0, L) committed, position L + j
+ *   v_cache  = tree node j (written by this pass's key/value projection)
+ *   cap      positions per head in the cache, >= L + M
+ *   M        1..HQ_MAX_M tree nodes (node 0 the root); L >= 0
+ *   Hq, Hkv  Hq a multiple of Hkv; 64 a multiple of Hq / Hkv
+ *   D        HQ_ATTN_HEAD_DIM
+ *   parent   int32 [M] (device)
+ *   scale    softmax scale (typically 1/sqrt(D)), finite
+ *   out      fp32 [M][Hq][D]
+ *   workspace hq_tree_attention_workspace_bytes(Hkv) bytes, 16-byte aligned;
+ *            its first word is the error word read by hq_workspace_status
+ * The probabilities are rounded to fp16 for the product with V (fp32
+ * accumulation everywhere): |out - exact| <= 2^-11 * max|v| + fp32 rounding.
+ * All pointers are device memory, 16-byte aligned.  flags: HQ_LAUNCH_DEFAULT
+ * or HQ_LAUNCH_PDL.  Launches two kernels (chunks of key positions, then
+ * their merge). */
+#define HQ_ATTN_HEAD_DIM 128
+size_t hq_tree_attention_workspace_bytes(int32_t Hkv);
+int hq_tree_attention(const void *q, const void *k_cache, const void *v_cache, int32_t cap, int32_t L, int32_t M,
+                      int32_t Hq, int32_t Hkv, int32_t D, const int32_t *parent, float scale, float *out,
+                      void *workspace, uint32_t flags, void *stream);
+
+/* Commit of the accepted path into the attention cache (same section: state
+ * is committed only along the chosen path).  The root stays at position L;
+ * accepted node path[d] (depth d + 1) moves to position L + 1 + d for
+ * d < *n_accept, in k_cache and v_cache (layout as in hq_tree_attention);
+ * nothing moves when *n_accept <= 0 (no drafted token accepted, or the -1 of
+ * a malformed tree) or when L + 1 + *n_accept > cap.  path and n_accept are
+ * hq_tree_accept's outputs in device memory, so no host round trip is
+ * needed; path entries outside [1, M) are skipped.  The next committed length
+ * is L + 1 + *n_accept. */
+int hq_tree_commit_kv(void *k_cache, void *v_cache, int32_t cap, int32_t L, int32_t M, int32_t Hkv, int32_t D,
+                      const int32_t *path, const int32_t *n_accept, uint32_t flags, void *stream);
+
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing will ever complete, giving up after
  * `limit_ns` nanoseconds (1000..100000000) and setting the error word of

@@ -226,6 +226,42 @@ int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream) {
     return cuda_status(hq::launch_wait_selftest(workspace, limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
+size_t hq_tree_attention_workspace_bytes(int32_t Hkv) {
+    if (Hkv <= 0 || Hkv > 4096) return 0;
+    return hq::attn_workspace_bytes(Hkv);
+}
+
+int hq_tree_attention(const void *q, const void *k_cache, const void *v_cache, int32_t cap, int32_t L, int32_t M,
+                      int32_t Hq, int32_t Hkv, int32_t D, const int32_t *parent, float scale, float *out,
+                      void *workspace, uint32_t flags, void *stream) {
+    if (M <= 0 || M > HQ_MAX_M || L < 0 || Hq <= 0 || Hkv <= 0 || Hkv > 4096 || Hq % Hkv != 0) return HQ_ERR_INVALID_ARG;
+    if ((long long)L + M > (long long)cap || (long long)cap * Hkv > (1ll << 40)) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0 || !(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+        return HQ_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !parent || !out || !workspace) return HQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(parent, 4) ||
+        !aligned(out, 16) || !aligned(workspace, 16))
+        return HQ_ERR_INVALID_ARG;
+    if (D != HQ_ATTN_HEAD_DIM || 64 % (Hq / Hkv) != 0) return HQ_ERR_UNSUPPORTED;
+    if ((long long)M * Hq > (1ll << 30)) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_tree_attention(q, k_cache, v_cache, cap, L, M, Hq, Hkv, parent, scale, out,
+                                                 workspace, (flags & HQ_LAUNCH_PDL) != 0,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int hq_tree_commit_kv(void *k_cache, void *v_cache, int32_t cap, int32_t L, int32_t M, int32_t Hkv, int32_t D,
+                      const int32_t *path, const int32_t *n_accept, uint32_t flags, void *stream) {
+    if (M <= 0 || M > HQ_MAX_M || L < 0 || Hkv <= 0 || Hkv > 65535 || (long long)L + M > (long long)cap)
+        return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !path || !n_accept) return HQ_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(path, 4) || !aligned(n_accept, 4))
+        return HQ_ERR_INVALID_ARG;
+    if (D != HQ_ATTN_HEAD_DIM) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_tree_commit_kv(k_cache, v_cache, cap, L, M, Hkv, path, n_accept,
+                                                 (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 extern "C" {

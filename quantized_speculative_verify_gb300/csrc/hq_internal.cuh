@@ -256,5 +256,12 @@ int accept_chunks(int V);
 cudaError_t launch_tree_accept(const float *logits, int M, int V, const int32_t *parent, const int32_t *tokens,
                                int32_t *g_out, int32_t *path, int32_t *n_accept, int32_t *bonus, void *workspace,
                                bool pdl, cudaStream_t s);
+// Tree-masked verify attention and the accepted-path cache commit.
+size_t attn_workspace_bytes(int Hkv);
+cudaError_t launch_tree_attention(const void *q, const void *k, const void *v, int cap, int L, int M, int Hq, int Hkv,
+                                  const int32_t *parent, float scale, float *out, void *workspace, bool pdl,
+                                  cudaStream_t s);
+cudaError_t launch_tree_commit_kv(void *k, void *v, int cap, int L, int M, int Hkv, const int32_t *path,
+                                  const int32_t *n_accept, bool pdl, cudaStream_t s);
 int device_sm_count();
 }  // namespace hq

@@ -33,7 +33,10 @@ FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 EXPORTS = ("hq_tree_accept_workspace_bytes", "hq_tree_accept", "hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
            "hq_make_signs",
            "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
-           "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc")
+           "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc", "hq_tree_attention_workspace_bytes",
+           "hq_tree_attention", "hq_tree_commit_kv")
+
+HQ_ATTN_HEAD_DIM = 128
 
 
 class HQError(RuntimeError):
@@ -81,6 +84,9 @@ def load() -> ctypes.CDLL:
         "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, I32, P, P, U32, P]),
         "hq_tree_accept_workspace_bytes": (SZ, [I32, I32]),
         "hq_tree_accept": (ctypes.c_int, [P, I32, I32, P, P, P, P, P, P, P, U32, P]),
+        "hq_tree_attention_workspace_bytes": (SZ, [I32]),
+        "hq_tree_attention": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, I32, P, ctypes.c_float, P, P, U32, P]),
+        "hq_tree_commit_kv": (ctypes.c_int, [P, P, I32, I32, I32, I32, I32, P, P, U32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -298,3 +304,44 @@ def tree_accept(logits: torch.Tensor, parent: torch.Tensor, tokens: torch.Tensor
     ws = torch.empty(hq_tree_accept_workspace_bytes(M, V), dtype=torch.uint8, device=dev)
     hq_tree_accept(logits, M, V, parent, tokens, greedy, path, out[0:1], out[1:2], ws, flags, stream)
     return greedy, path, out
+
+
+def hq_tree_attention_workspace_bytes(Hkv: int) -> int:
+    return int(load().hq_tree_attention_workspace_bytes(int(Hkv)))
+
+
+def hq_tree_attention(q, k_cache, v_cache, cap: int, L: int, M: int, Hq: int, Hkv: int, D: int, parent, scale: float,
+                      out, workspace, flags: int = 0, stream=None) -> None:
+    _check(load().hq_tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), cap, L, M, Hq, Hkv, D, _ptr(parent),
+                                    float(scale), _ptr(out), _ptr(workspace), flags, _stream(stream)),
+           "hq_tree_attention")
+
+
+def hq_tree_commit_kv(k_cache, v_cache, cap: int, L: int, M: int, Hkv: int, D: int, path, n_accept, flags: int = 0,
+                      stream=None) -> None:
+    _check(load().hq_tree_commit_kv(_ptr(k_cache), _ptr(v_cache), cap, L, M, Hkv, D, _ptr(path), _ptr(n_accept),
+                                    flags, _stream(stream)),
+           "hq_tree_commit_kv")
+
+
+def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, parent: torch.Tensor,
+                   scale: float, out: torch.Tensor = None, workspace: torch.Tensor = None, flags: int = 0,
+                   stream=None) -> torch.Tensor:
+    """Tree-masked attention of the M tree nodes.  q fp16 [M][Hq][D]; k_cache,
+    v_cache fp16 [Hkv][cap][D] with the tree nodes at positions [L, L + M);
+    parent int32 [M] (device).  Returns fp32 [M][Hq][D]."""
+    M, Hq, D = q.shape
+    Hkv, cap, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((M, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.zeros(hq_tree_attention_workspace_bytes(Hkv), dtype=torch.uint8, device=q.device)
+    hq_tree_attention(q, k_cache, v_cache, cap, L, M, Hq, Hkv, D, parent, scale, out, workspace, flags, stream)
+    return out
+
+
+def tree_commit_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, M: int, path: torch.Tensor,
+                   n_accept: torch.Tensor, flags: int = 0, stream=None) -> None:
+    """Moves the accepted path next to the root in both caches (in place)."""
+    Hkv, cap, D = k_cache.shape
+    hq_tree_commit_kv(k_cache, v_cache, cap, L, M, Hkv, D, path, n_accept, flags, stream)

@@ -165,3 +165,34 @@ def test_tree_accept_sizes_and_validation():
     assert lib.hq_tree_accept(None, *args[1:]) == E
     assert lib.hq_tree_accept(*args[:9], FAKE + 8, 0, None) == E     # workspace alignment
     assert lib.hq_tree_accept(*args[:10], 2, None) == E              # unknown flag
+
+
+def test_tree_attention_arguments_are_checked_before_launch():
+    lib = hq.load()
+    E, U = hq.HQ_ERR_INVALID_ARG, hq.HQ_ERR_UNSUPPORTED
+    D = hq.HQ_ATTN_HEAD_DIM
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, cap=100, L=50, M=16, Hq=32, Hkv=8, D=D, parent=FAKE, scale=0.1, out=FAKE,
+              ws=FAKE, flags=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.hq_tree_attention(a["q"], a["k"], a["v"], a["cap"], a["L"], a["M"], a["Hq"], a["Hkv"], a["D"],
+                                     a["parent"], a["scale"], a["out"], a["ws"], a["flags"], None)
+    assert call(M=0) == E and call(M=129) == E and call(L=-1) == E
+    assert call(cap=65) == E                      # L + M > cap
+    assert call(Hq=30) == E and call(Hkv=0) == E  # Hq not a multiple of Hkv
+    assert call(q=None) == E and call(ws=None) == E and call(parent=None) == E
+    assert call(k=FAKE + 8) == E and call(out=FAKE + 4) == E
+    assert call(flags=2) == E and call(scale=float("nan")) == E and call(scale=float("inf")) == E
+    assert call(D=64) == U                        # head dimension other than 128
+    assert call(Hq=96, Hkv=1) == U                # 64 not a multiple of Hq / Hkv
+    assert hq.hq_tree_attention_workspace_bytes(8) == 16 + 8 * 4096 * (D + 2) * 4
+    assert hq.hq_tree_attention_workspace_bytes(0) == 0
+    # commit
+    c = lib.hq_tree_commit_kv
+    assert c(FAKE, FAKE, 60, 50, 16, 8, D, FAKE, FAKE, 0, None) == E   # L + M > cap
+    assert c(None, FAKE, 100, 50, 16, 8, D, FAKE, FAKE, 0, None) == E
+    assert c(FAKE, FAKE, 100, 50, 16, 8, D, None, FAKE, 0, None) == E
+    assert c(FAKE, FAKE, 100, 50, 0, 8, D, FAKE, FAKE, 0, None) == E
+    assert c(FAKE, FAKE, 100, 50, 16, 8, 64, FAKE, FAKE, 0, None) == U
+    assert c(FAKE, FAKE, 100, 50, 16, 8, D, FAKE, FAKE, 4, None) == E
