@@ -57,6 +57,10 @@ def parse_args():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-attention", action="store_true", help="skip the tree-masked attention measurement")
+    p.add_argument("--attn-context", type=int, default=8192, help="committed positions of the attention measurement")
+    p.add_argument("--only-attention", action="store_true",
+                   help="run only the tree-attention measurement (for profiling its kernels)")
     p.add_argument("--summarize-ncu", metavar="CSV",
                    help="summarize an ncu --csv log of this program into profiles/ and exit")
     p.add_argument("--ncu-command", default="", help="the ncu command line that produced CSV (recorded)")
@@ -452,6 +456,10 @@ def run_gpu(args, ranks: Ranks):
                "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_host.numel() * 4,
                "ms_per_step": e_ms / e_steps, "steps": e_steps}
 
+    attn = None
+    if not args.no_attention:
+        attn = measure_tree_attention(torch, hq, device, stream, args, peak)
+
     cpu = None
     if not args.no_cpu_baseline and ranks.rank == 0:
         cpu, _, _ = cpu_oracle_sample()
@@ -476,9 +484,65 @@ def run_gpu(args, ranks: Ranks):
             "e2e": e2e,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * (vp.n_act + vp.n_gemm + vp.n_accept_kernels),
+            "tree_attention": attn,
         }
         print(json.dumps(line))
     return 0
+
+
+def measure_tree_attention(torch, hq, device, stream, args, peak):
+    """Tree-masked verify attention of the 9B-class decoder: its 8 attention
+    layers (the other 24 are DeltaNet layers), 16 tree nodes, 32 query heads
+    over 8 key/value heads of 128, fp16 caches of L committed positions each
+    (8 x 33.6 MB at L = 8192: larger than L2, so each pass streams them from
+    HBM).  One step = the 8 layers' attention calls, replayed from a CUDA graph
+    with programmatic dependent launch.  Algorithmic bytes = the K and V rows
+    read (committed + tree positions) plus q in and out."""
+    layers, M, Hq, Hkv, D, L = 8, 16, 32, 8, hq.HQ_ATTN_HEAD_DIM, args.attn_context
+    cap = L + M
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234)
+    caches = [(torch.randn((Hkv, cap, D), generator=gen, device=device, dtype=torch.float16),
+               torch.randn((Hkv, cap, D), generator=gen, device=device, dtype=torch.float16)) for _ in range(layers)]
+    qs = [torch.randn((M, Hq, D), generator=gen, device=device, dtype=torch.float16) for _ in range(layers)]
+    parent = torch.tensor([0, 0, 1, 2, 3, 0, 5, 6, 1, 8, 2, 10, 11, 0, 13, 14], dtype=torch.int32, device=device)
+    outs = [torch.empty((M, Hq, D), dtype=torch.float32, device=device) for _ in range(layers)]
+    ws = torch.zeros(hq.hq_tree_attention_workspace_bytes(Hkv), dtype=torch.uint8, device=device)
+    scale = 1.0 / D ** 0.5
+
+    def step():
+        for i in range(layers):
+            hq.hq_tree_attention(qs[i], caches[i][0], caches[i][1], cap, L, M, Hq, Hkv, D, parent, scale, outs[i],
+                                 ws, hq.HQ_LAUNCH_PDL, stream)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    reps = max(20, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    if hq.hq_workspace_status(ws) != hq.HQ_OK:
+        raise SystemExit("device-side wait timed out in the attention measurement")
+    kv_bytes = layers * 2 * Hkv * (L + M) * D * 2
+    io_bytes = layers * (M * Hq * D * 2 + M * Hq * D * 4)
+    gbs = (kv_bytes + io_bytes) / (ms / 1e3) / 1e9
+    return {"workload": f"9B-class tree verify attention: {layers} layers, M={M} tree nodes, Hq={Hq}, Hkv={Hkv}, "
+                        f"D={D}, L={L} committed positions, fp16 caches",
+            "value": gbs, "unit": "GB/s", "us_per_layer": ms * 1e3 / layers, "ms_per_step": ms,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "algorithmic_bytes_per_layer": (kv_bytes + io_bytes) / layers},
+            "kernels": ["k_tree_attn_split", "k_tree_attn_merge"], "launches_per_step": 2 * layers,
+            "steps": reps}
 
 
 def summarize_ncu(args) -> int:
@@ -532,6 +596,19 @@ def summarize_ncu(args) -> int:
     return 0
 
 
+def run_only_attention(args) -> int:
+    """The tree-attention measurement alone (one line of JSON), for profiling."""
+    import torch
+    from quantized_speculative_verify_gb300 import hq
+    device = torch.device("cuda", 0)
+    hq.load()
+    peak, _ = measured_peaks()
+    stream = torch.cuda.Stream(device=device)
+    torch.cuda.set_stream(stream)
+    print(json.dumps(measure_tree_attention(torch, hq, device, stream, args, peak)))
+    return 0
+
+
 def run_one_gemm(args) -> int:
     """One layer of the given shape: rotate/quantize once, then --steps timed GEMM launches
     (CUDA events, after --warmup launches); the weights are larger than L2 for the 9B shapes."""
@@ -574,6 +651,8 @@ def main():
         return summarize_ncu(args)
     if args.one_gemm:
         return run_one_gemm(args)
+    if args.only_attention:
+        return run_only_attention(args)
     ranks = Ranks()
     try:
         if args.impl == "reference":

@@ -268,8 +268,10 @@ int hq_tree_accept(const float *logits, int32_t M, int32_t V, const int32_t *par
  * The probabilities are rounded to fp16 for the product with V (fp32
  * accumulation everywhere): |out - exact| <= 2^-11 * max|v| + fp32 rounding.
  * All pointers are device memory, 16-byte aligned.  flags: HQ_LAUNCH_DEFAULT
- * or HQ_LAUNCH_PDL.  Launches two kernels (chunks of key positions, then
- * their merge). */
+ * or HQ_LAUNCH_PDL.  With HQ_LAUNCH_PDL the committed positions [0, L) are
+ * read before waiting for the previous kernel of the stream, so that kernel
+ * must not write them (the tree rows, q and parent may be its outputs).
+ * Launches two kernels (chunks of key positions, then their merge). */
 #define HQ_ATTN_HEAD_DIM 128
 size_t hq_tree_attention_workspace_bytes(int32_t Hkv);
 int hq_tree_attention(const void *q, const void *k_cache, const void *v_cache, int32_t cap, int32_t L, int32_t M,

@@ -16,14 +16,18 @@
 // block takes 64 of them and one contiguous chunk of key positions (split
 // KV), and a second kernel merges the chunks.
 //
-// Split kernel: a producer warp copies each 64-key tile of K and V row by row
-// (256-byte bulk copies, L2 evict-first) into a ring of padded shared-memory
-// stages (272-byte rows: the ldmatrix reads of eight rows hit eight different
-// bank groups); four consumer warps each own 16 query rows: S = Q K^T and
+// Split kernel: one producer thread loads each 64-key tile of K and V with
+// four TMA tiled copies (boxes of 64 dimensions x 64 positions of one head,
+// 128-byte swizzle, L2 evict-first) into a ring of shared-memory stages; in a
+// swizzled box the 16-byte chunk c of row r sits at chunk c ^ (r mod 8), so
+// the ldmatrix reads of eight rows hit eight different bank groups.  The
+// tensor maps end at position L + M: rows past it arrive as zeros.  Four
+// consumer warps each own 16 query rows: S = Q K^T and
 // O += P V on fp16 tensor cores with fp32 accumulation, online softmax in
 // base-2 units (s * scale * log2 e), P rounded to fp16 for the second
 // product.  Each block writes its unnormalized O, running maximum and sum;
 // the merge rescales and adds the chunks in ascending order.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -36,14 +40,16 @@ constexpr int AD = HQ_ATTN_HEAD_DIM;          // head dimension
 constexpr int AROWS = 64;                     // query rows per thread block
 constexpr int AKEYS = 64;                     // key positions per stage
 constexpr int ASTAGES = 3;
-constexpr int AROW_BYTES = AD * 2 + 16;       // padded shared-memory row
-constexpr int ATILE_BYTES = AKEYS * AROW_BYTES;
+constexpr int ABOX_DIMS = 64;                 // dimensions per TMA box (128 bytes: the swizzle span)
+constexpr int ABOX_BYTES = AKEYS * ABOX_DIMS * 2;  // 8 KB, a multiple of the 1024-byte swizzle atom
+constexpr int ATILE_BYTES = (AD / ABOX_DIMS) * ABOX_BYTES;
 constexpr int ASTAGE_BYTES = 2 * ATILE_BYTES;  // K tile, then V tile
 constexpr int ACW = 4;                         // consumer warps, 16 rows each
 constexpr int ATHREADS = (ACW + 1) * 32;
 constexpr int AMAX_ROWS_SPLITS = 4096;         // splits x padded rows, per key/value head (workspace)
 constexpr int AMAX_SPLITS = 64;
-constexpr size_t ASMEM = (size_t)ASTAGES * ASTAGE_BYTES + 2 * ASTAGES * 8 + AROWS * 16 + HQ_MAX_M * 4;
+// the ring starts at the first 1024-byte boundary of the dynamic shared memory
+constexpr size_t ASMEM = 1024 + (size_t)ASTAGES * ASTAGE_BYTES + 2 * ASTAGES * 8 + AROWS * 16 + HQ_MAX_M * 4;
 
 struct AttnArgs {
     const __half *q, *k, *v;
@@ -76,15 +82,31 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 3-D TMA tiled load (dimension, position, head) into shared memory,
+// completing on `bar`.  x * 2 bytes is a multiple of 16 (x in {0, 64}).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk c (dimensions 8c .. 8c+7 of a box) of row r in
+// a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-__global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)ASTAGES * ASTAGE_BYTES);  // full[S], empty[S]
+__global__ void __launch_bounds__(ATHREADS, 2)
+    k_tree_attn_split(const AttnArgs a, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)ASTAGES * ASTAGE_BYTES);  // full[S], empty[S]
     uint32_t *s_anc = reinterpret_cast<uint32_t *>(bars + 2 * ASTAGES);                   // [AROWS][4]
     int32_t *s_par = reinterpret_cast<int32_t *>(s_anc + AROWS * 4);                      // [HQ_MAX_M]
 
@@ -104,68 +126,45 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
         }
         fence_mbar_init();
     }
+    __syncthreads();
     pdl_launch_dependents();
-    pdl_wait();
-    // ancestor sets of this block's nodes: bit j of word j / 32 = tree node j visible
-    for (int i = threadIdx.x; i < a.M; i += blockDim.x) s_par[i] = a.parent[i];
-    __syncthreads();
-    if (threadIdx.x < npt) {
-        uint32_t m4[4] = {0u, 0u, 0u, 0u};
-        const int node = node0 + threadIdx.x;
-        if (node < a.M) {
-            m4[node >> 5] |= 1u << (node & 31);
-            int cur = node;
-            for (int step = 0; step < HQ_MAX_M && cur > 0; ++step) {
-                const int p = s_par[cur];
-                if (p < 0 || p >= cur) break;
-                m4[p >> 5] |= 1u << (p & 31);
-                cur = p;
-            }
-        }
-#pragma unroll
-        for (int w = 0; w < 4; ++w) s_anc[threadIdx.x * 4 + w] = m4[w];
-    }
-    __syncthreads();
 
     if (warp == ACW) {
         // ------------------------------------------------------ producer ---
-        const uint64_t pol = policy_evict_first();
-        const size_t head_base = (size_t)hk * (size_t)a.cap;
-        int i = 0;
-        bool ok = true;
-        for (; i < ntiles && ok; ++i) {
-            const int st = i % ASTAGES;
-            const uint32_t ph = (uint32_t)((i / ASTAGES) & 1);
-            if (i >= ASTAGES) ok = mbar_wait_bounded(smem_addr(&bars[ASTAGES + st]), ph ^ 1u, a.err);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            const int p0 = k0 + i * AKEYS;
-            const int nk = k1 - p0 < AKEYS ? k1 - p0 : AKEYS;
-            uint8_t *kt = ring + (size_t)st * ASTAGE_BYTES;
-            uint8_t *vt = kt + ATILE_BYTES;
-            if (nk < AKEYS) {
-                // rows past the chunk are never loaded: zero their values so
-                // that a zero probability times them stays zero
-                for (int r = nk; r < AKEYS; ++r)
-                    reinterpret_cast<uint4 *>(vt + (size_t)r * AROW_BYTES)[lane % 16] = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            auto issue = [&](int i) {
+                const int st = i % ASTAGES;
+                const uint32_t kt = smem_addr(ring + (size_t)st * ASTAGE_BYTES);
+                const uint32_t bar = smem_addr(&bars[st]);
+                mbar_arrive_expect_tx(bar, (uint32_t)ASTAGE_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < AD / ABOX_DIMS; ++bx) {
+                    tma_load_3d(kt + bx * ABOX_BYTES, &tk, bx * ABOX_DIMS, k0 + i * AKEYS, hk, bar, pol);
+                    tma_load_3d(kt + ATILE_BYTES + bx * ABOX_BYTES, &tv, bx * ABOX_DIMS, k0 + i * AKEYS, hk, bar, pol);
+                }
+            };
+            // Committed positions are not written by the kernel before this
+            // one (only the tree rows are): the first stages' tiles that lie
+            // below L are loaded before waiting for it.
+            int i = 0;
+            for (; i < ntiles && i < ASTAGES && k0 + (i + 1) * AKEYS <= a.L; ++i) issue(i);
+            pdl_wait();
+            for (; i < ntiles; ++i) {
+                const int st = i % ASTAGES;
+                const uint32_t ph = (uint32_t)((i / ASTAGES) & 1);
+                if (i >= ASTAGES && !mbar_wait_bounded(smem_addr(&bars[ASTAGES + st]), ph ^ 1u, a.err)) break;
+                issue(i);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(smem_addr(&bars[st]), (uint32_t)nk * (uint32_t)(AD * 2 * 2));
-            __syncwarp();
-            for (int r = lane; r < nk; r += 32) {
-                const size_t src = (head_base + (size_t)(p0 + r)) * AD;
-                bulk_copy_g2s(smem_addr(kt + (size_t)r * AROW_BYTES), a.k + src, AD * 2, smem_addr(&bars[st]), pol);
-                bulk_copy_g2s(smem_addr(vt + (size_t)r * AROW_BYTES), a.v + src, AD * 2, smem_addr(&bars[st]), pol);
-            }
-        }
-        // no copy may still be landing in shared memory when the block exits
-        if (lane == 0)
+            // no copy may still be landing in shared memory when the block exits
             for (int j = i > ASTAGES ? i - ASTAGES : 0; j < i; ++j)
                 mbar_wait_bounded(smem_addr(&bars[j % ASTAGES]), (uint32_t)((j / ASTAGES) & 1), a.err);
+        }
         return;
     }
 
     // ---------------------------------------------------------- consumers ---
+    pdl_wait();
     const int g8 = lane >> 2, t4 = lane & 3;
     const int rA = warp * 16 + g8, rB = rA + 8;  // this lane's two query rows (block-local)
     const int nA = node0 + rA / a.G, nB = node0 + rB / a.G;
@@ -184,6 +183,29 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
             qa[ks][3] = vB ? __ldg(qB + c + 4) : 0u;
         }
     }
+    // Ancestor sets of this block's nodes, only where the chunk reaches the
+    // tree positions: bit j of word j / 32 = tree node j visible.
+    if (k1 > a.L) {
+        for (int i = threadIdx.x; i < a.M; i += ACW * 32) s_par[i] = a.parent[i];
+        named_barrier(1, ACW * 32);
+        if (threadIdx.x < npt) {
+            uint32_t m4[4] = {0u, 0u, 0u, 0u};
+            const int node = node0 + threadIdx.x;
+            if (node < a.M) {
+                m4[node >> 5] |= 1u << (node & 31);
+                int cur = node;
+                for (int step = 0; step < HQ_MAX_M && cur > 0; ++step) {
+                    const int p = s_par[cur];
+                    if (p < 0 || p >= cur) break;
+                    m4[p >> 5] |= 1u << (p & 31);
+                    cur = p;
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) s_anc[threadIdx.x * 4 + w] = m4[w];
+        }
+        named_barrier(1, ACW * 32);
+    }
     const uint32_t *ancA = s_anc + (rA / a.G) * 4, *ancB = s_anc + (rB / a.G) * 4;  // this lane's rows' ancestor sets
 
     float o[AD / 8][4];
@@ -194,9 +216,11 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
     float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.0f, 0.0f};
     bool ok = true;
 
-    // ldmatrix lane addresses (byte offsets inside a tile)
-    const uint32_t k_lane = (uint32_t)(((lane >> 4) * 8 + (lane & 7)) * AROW_BYTES + ((lane >> 3) & 1) * 16);
-    const uint32_t v_lane = (uint32_t)(((((lane >> 3) & 1) * 8) + (lane & 7)) * AROW_BYTES + (lane >> 4) * 16);
+    // ldmatrix rows of this lane: K (non-transposed) row (lane >> 4) * 8 + (lane & 7)
+    // and chunk half (lane >> 3) & 1; V (transposed) row ((lane >> 3) & 1) * 8 +
+    // (lane & 7) and chunk half lane >> 4.  Every row index is r = 8m + (lane & 7).
+    const int k_row = (lane >> 4) * 8 + (lane & 7), k_half = (lane >> 3) & 1;
+    const int v_row = ((lane >> 3) & 1) * 8 + (lane & 7), v_half = lane >> 4;
 
     for (int i = 0; i < ntiles; ++i) {
         const int st = i % ASTAGES;
@@ -217,7 +241,8 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
 #pragma unroll
             for (int np = 0; np < AKEYS / 16; ++np) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kt + k_lane + (uint32_t)(np * 16 * AROW_BYTES + ks * 32), b0, b1, b2, b3);
+                ldsm_x4(kt + (uint32_t)((ks >> 2) * ABOX_BYTES) + swz(np * 16 + k_row, 2 * (ks & 3) + k_half), b0, b1,
+                        b2, b3);
                 mma16816(s[2 * np], qa[ks], b0, b1);
                 mma16816(s[2 * np + 1], qa[ks], b2, b3);
             }
@@ -265,12 +290,15 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
             }
 #pragma unroll
         for (int h = 0; h < 2; ++h) lrun[h] = lrun[h] * alpha[h] + rs[h];
+        // once the maxima settle (alpha == 1 exactly) the rescale is skipped
+        if (!__all_sync(0xffffffffu, alpha[0] == 1.0f && alpha[1] == 1.0f)) {
 #pragma unroll
-        for (int j = 0; j < AD / 8; ++j) {
-            o[j][0] *= alpha[0];
-            o[j][1] *= alpha[0];
-            o[j][2] *= alpha[1];
-            o[j][3] *= alpha[1];
+            for (int j = 0; j < AD / 8; ++j) {
+                o[j][0] *= alpha[0];
+                o[j][1] *= alpha[0];
+                o[j][2] *= alpha[1];
+                o[j][3] *= alpha[1];
+            }
         }
 
         // O += P V: P (fp16) as the A operand, V through transposed ldmatrix
@@ -284,7 +312,8 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
 #pragma unroll
             for (int dp = 0; dp < AD / 16; ++dp) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vt + v_lane + (uint32_t)(kk * 16 * AROW_BYTES + dp * 32), b0, b1, b2, b3);
+                ldsm_x4_t(vt + (uint32_t)((dp >> 2) * ABOX_BYTES) + swz(kk * 16 + v_row, 2 * (dp & 3) + v_half), b0,
+                          b1, b2, b3);
                 mma16816(o[2 * dp], pa, b0, b1);
                 mma16816(o[2 * dp + 1], pa, b2, b3);
             }
@@ -311,24 +340,43 @@ __global__ void __launch_bounds__(ATHREADS, 2) k_tree_attn_split(const AttnArgs 
     }
 }
 
-// One thread block per (node, query head), one thread per dimension.
+// One thread block per (node, query head), one thread per dimension.  The
+// chunks' maxima and sums are read once into shared memory (one load per
+// thread), the weights exp2(m_s - max) computed once, and the partial outputs
+// loaded 32 chunks at a time; chunks are added in ascending order.
 __global__ void __launch_bounds__(AD) k_tree_attn_merge(const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
                                                         int NS, int Hkv, int Hq, int G, int rows_pad,
                                                         float *__restrict__ out) {
+    __shared__ float s_m[AMAX_SPLITS], s_l[AMAX_SPLITS], s_w[AMAX_SPLITS];
     pdl_launch_dependents();
     pdl_wait();
     const int node = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int hk = h / G, row = node * G + (h % G);
     const int d = threadIdx.x;
+    const size_t split_stride = (size_t)Hkv * rows_pad;  // rows between consecutive chunks
+    const size_t r0 = (size_t)hk * rows_pad + row;
+    if (d < NS) {
+        const float2 ml = *reinterpret_cast<const float2 *>(ws_ml + (r0 + d * split_stride) * 2);
+        s_m[d] = ml.x;
+        s_l[d] = ml.y;
+    }
+    __syncthreads();
     float mg = -INFINITY;
-    for (int s = 0; s < NS; ++s) mg = fmaxf(mg, ws_ml[(((size_t)s * Hkv + hk) * rows_pad + row) * 2]);
+    for (int sp = 0; sp < NS; ++sp) mg = fmaxf(mg, s_m[sp]);
+    if (d < NS) s_w[d] = exp2f(s_m[d] - mg);  // 0 for a chunk in which the row saw no key
+    __syncthreads();
     float num = 0.0f, den = 0.0f;
-    for (int s = 0; s < NS; ++s) {
-        const size_t r = ((size_t)s * Hkv + hk) * rows_pad + row;
-        const float2 ml = *reinterpret_cast<const float2 *>(ws_ml + r * 2);
-        const float w = exp2f(ml.x - mg);  // 0 for a chunk in which the row saw no key
-        num += w * ws_o[r * AD + d];
-        den += w * ml.y;
+    const float *o = ws_o + r0 * AD + d;
+    for (int s0 = 0; s0 < NS; s0 += 32) {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = s0 + j < NS ? o[(size_t)(s0 + j) * split_stride * AD] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (s0 + j < NS) {
+                num += s_w[s0 + j] * x[j];
+                den += s_w[s0 + j] * s_l[s0 + j];
+            }
     }
     out[((size_t)node * Hq + h) * AD + d] = num / den;
 }
@@ -361,6 +409,39 @@ __global__ void __launch_bounds__(256) k_tree_commit(__half *k, __half *v, int c
         const int d = idx / RW, w = idx % RW;
         if (s_src[d] >= 0) c[(size_t)(L + 1 + d) * RW + w] = s_rows[d][w];
     }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map of a cache [Hkv][cap][AD] fp16 that ends at position `rows`:
+// boxes of 64 dimensions x AKEYS positions x 1 head, 128-byte swizzle,
+// out-of-range positions filled with zeros.
+cudaError_t cache_map(CUtensorMap *m, const void *base, int rows, int cap, int Hkv) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)AD, (cuuint64_t)rows, (cuuint64_t)Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)AD * 2, (cuuint64_t)cap * AD * 2};
+    const cuuint32_t box[3] = {ABOX_DIMS, AKEYS, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaLaunchConfig_t attn_config(dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t s,
@@ -432,10 +513,15 @@ cudaError_t launch_tree_attention(const void *q, const void *k, const void *v, i
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
+    CUtensorMap tk, tv;
+    e = cache_map(&tk, k, total, cap, Hkv);
+    if (e != cudaSuccess) return e;
+    e = cache_map(&tv, v, total, cap, Hkv);
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg =
         attn_config(dim3((unsigned)ns, (unsigned)Hkv, (unsigned)row_tiles), dim3(ATHREADS), ASMEM, pdl, s, attr);
-    e = cudaLaunchKernelEx(&cfg, k_tree_attn_split, a);
+    e = cudaLaunchKernelEx(&cfg, k_tree_attn_split, a, tk, tv);
     if (e != cudaSuccess) return e;
     cfg = attn_config(dim3((unsigned)(M * Hq)), dim3(AD), 0, true, s, attr);
     return cudaLaunchKernelEx(&cfg, k_tree_attn_merge, (const float *)a.ws_o, (const float *)a.ws_ml, ns, Hkv, Hq, G,
