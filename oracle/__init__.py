@@ -99,6 +99,8 @@ def _load(openmp: bool = False) -> ctypes.CDLL:
         lib.or_half_to_double.restype = ctypes.c_double
         lib.or_tree_attention.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_double, _P]
         lib.or_tree_commit_kv.argtypes = [_P, _P, _I, _I, _I, _I, _P, _I]
+        lib.or_delta_tree.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]
+        lib.or_delta_commit.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I]
         _libs[openmp] = lib
         return lib
 
@@ -344,3 +346,34 @@ def tree_commit_kv(k: np.ndarray, v: np.ndarray, L: int, path: np.ndarray, n_acc
     _check(_load().or_tree_commit_kv(_ptr(k16.view(np.uint16)), _ptr(v16.view(np.uint16)), cap, L, Hkv, D,
                                      _ptr(p), int(n_accept)), "tree_commit_kv")
     return k16, v16
+
+
+def delta_tree(state: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray, beta: np.ndarray,
+               parent: np.ndarray, openmp: bool = False) -> np.ndarray:
+    """Outputs of every tree node of a gated delta-rule layer (fp64).
+
+    state float32 [H][D][D] (committed, read only); q, k, v float32 [M][H][D];
+    alpha, beta float32 [M][H]; parent int32 [M].  Returns float64 [M][H][D]."""
+    st = _c(state, np.float32)
+    q, k, v = _c(q, np.float32), _c(k, np.float32), _c(v, np.float32)
+    al, be, par = _c(alpha, np.float32), _c(beta, np.float32), _c(parent, np.int32)
+    M, H, D = q.shape
+    out = np.empty((M, H, D), dtype=np.float64)
+    _check(_load(openmp).or_delta_tree(_ptr(st), _ptr(q), _ptr(k), _ptr(v), _ptr(al), _ptr(be), _ptr(par), M, H, D,
+                                       _ptr(out)), "delta_tree")
+    return out
+
+
+def delta_commit(state: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray, beta: np.ndarray,
+                 path: np.ndarray, n_accept: int) -> np.ndarray:
+    """The committed state after accepting the root and path[:n_accept] (fp64 copy)."""
+    st = np.array(state, dtype=np.float64, order="C")
+    k, v = _c(k, np.float32), _c(v, np.float32)
+    al, be = _c(alpha, np.float32), _c(beta, np.float32)
+    M, H, D = k.shape
+    p = _c(np.asarray(path).reshape(-1), np.int32)
+    if p.size == 0:
+        p = np.zeros(1, dtype=np.int32)
+    _check(_load().or_delta_commit(_ptr(st), _ptr(k), _ptr(v), _ptr(al), _ptr(be), _ptr(p), int(n_accept), M, H, D),
+           "delta_commit")
+    return st

@@ -610,6 +610,101 @@ int or_tree_commit_kv(uint16_t *k, uint16_t *v, int cap, int L, int Hkv, int D, 
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Rollback-free DeltaNet tree pass (section "Verifying a draft tree        */
+/* without restoring model state": a Gated DeltaNet layer compresses the   */
+/* past into a fixed-size state that every accepted token changes; the     */
+/* verify pass computes the outputs of every tree branch without changing  */
+/* the live state, which is then updated only along the accepted path).    */
+/* The page gives no equations.  Readings:                                 */
+/*   D1  the recurrence is the published gated delta rule (Yang, Kautz and  */
+/*       Hatamizadeh, "Gated Delta Networks", ICLR 2025), per head:         */
+/*         S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T */
+/*         o_t = S_t q_t                                                    */
+/*       S is D x D (rows: value dimensions, columns: key dimensions);      */
+/*       q, k, v, alpha, beta are inputs (their projections, gates and     */
+/*       normalizations come before this step);                            */
+/*   D2  on the tree, node i's state follows from its parent's state by one */
+/*       step with node i's inputs; the root (node 0) and any node whose    */
+/*       parent lies outside [0, i) follow from the committed state;        */
+/*   D3  the committed state is only read; commit replaces it by the state  */
+/*       of the accepted node, i.e. one step for the root and one for each  */
+/*       accepted node path[0..n_accept) in order; nothing changes when     */
+/*       n_accept < 0 (a malformed tree).                                   */
+/* ------------------------------------------------------------------------ */
+/* One step on a D x D state (row-major), in place. */
+static void or_delta_step(double *S, int D, const float *k, const float *v, double alpha, double beta)
+{
+    double *u = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int r = 0; r < D; ++r) {
+        double t = 0.0;
+        for (int c = 0; c < D; ++c) t += S[(size_t)r * D + c] * (double)k[c];
+        u[r] = t;                                   /* (S k)_r */
+    }
+    for (int r = 0; r < D; ++r)
+        for (int c = 0; c < D; ++c)                 /* alpha S (I - beta k k^T) + beta v k^T */
+            S[(size_t)r * D + c] = alpha * (S[(size_t)r * D + c] - beta * u[r] * (double)k[c]) +
+                                   beta * (double)v[r] * (double)k[c];
+    free(u);
+}
+
+/* state [H][D][D]; q, k, v [M][H][D]; alpha, beta [M][H]; out [M][H][D]. */
+int or_delta_tree(const float *state, const float *q, const float *k, const float *v, const float *alpha,
+                  const float *beta, const int32_t *parent, int M, int H, int D, double *out)
+{
+    if (M < 1 || H < 1 || D < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic)
+    for (int r = 0; r < M * H; ++r) {
+        const int i = r / H, h = r % H;
+        int *chain = (int *)malloc(sizeof(int) * (size_t)M);
+        double *S = (double *)malloc(sizeof(double) * (size_t)D * D);
+        if (!chain || !S) { free(chain); free(S); fail = 1; continue; }
+        int n = 0, cur = i;
+        chain[n++] = cur;
+        while (cur > 0) {
+            const int p = parent[cur];
+            if (p < 0 || p >= cur) break;
+            chain[n++] = p;
+            cur = p;
+        }
+        for (size_t e = 0; e < (size_t)D * D; ++e) S[e] = (double)state[(size_t)h * D * D + e];
+        for (int a = n - 1; a >= 0; --a) {            /* from the top of the chain down to node i */
+            const int j = chain[a];
+            const size_t b = ((size_t)j * H + h) * D;
+            or_delta_step(S, D, k + b, v + b, (double)alpha[(size_t)j * H + h], (double)beta[(size_t)j * H + h]);
+        }
+        const float *qi = q + ((size_t)i * H + h) * D;
+        for (int rr = 0; rr < D; ++rr) {
+            double t = 0.0;
+            for (int c = 0; c < D; ++c) t += S[(size_t)rr * D + c] * (double)qi[c];
+            out[((size_t)i * H + h) * D + rr] = t;
+        }
+        free(chain);
+        free(S);
+    }
+    return fail ? 2 : 0;
+}
+
+/* state [H][D][D] in place (double); the root, then path[0..n_accept). */
+int or_delta_commit(double *state, const float *k, const float *v, const float *alpha, const float *beta,
+                    const int32_t *path, int n_accept, int M, int H, int D)
+{
+    if (n_accept < 0) return 0;
+    if (n_accept >= M || H < 1 || D < 1) return 1;
+    for (int d = 0; d < n_accept; ++d)
+        if (path[d] < 1 || path[d] >= M) return 1;
+    for (int h = 0; h < H; ++h) {
+        double *S = state + (size_t)h * D * D;
+        for (int a = -1; a < n_accept; ++a) {
+            const int j = a < 0 ? 0 : path[a];
+            const size_t b = ((size_t)j * H + h) * D;
+            or_delta_step(S, D, k + b, v + b, (double)alpha[(size_t)j * H + h], (double)beta[(size_t)j * H + h]);
+        }
+    }
+    return 0;
+}
+
 int or_num_threads(void)
 {
 #ifdef _OPENMP

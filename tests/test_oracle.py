@@ -684,3 +684,141 @@ def test_tree_commit_kv_moves_the_accepted_path_next_to_the_root():
     for n in (0, -1):
         kn, vn = oracle.tree_commit_kv(k, v, L, path, n)
         assert np.array_equal(kn, k) and np.array_equal(vn, v)
+
+
+# ------------------------------------------------------ DeltaNet tree pass ---
+# Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling",
+# section "Verifying a draft tree without restoring model state" (the state of
+# a Gated DeltaNet layer changes with every accepted token; verification must
+# not change it).  Recurrence: the published gated delta rule,
+# S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T, o_t = S_t q_t.
+
+def _delta_inputs(rng, M, H, D, unit_keys=True):
+    st = rng.standard_normal((H, D, D)).astype(np.float32) * 0.3
+    q = rng.standard_normal((M, H, D)).astype(np.float32)
+    k = rng.standard_normal((M, H, D)).astype(np.float32)
+    if unit_keys:
+        k = (k / np.linalg.norm(k, axis=2, keepdims=True)).astype(np.float32)
+    v = rng.standard_normal((M, H, D)).astype(np.float32)
+    al = rng.uniform(0.6, 1.0, (M, H)).astype(np.float32)
+    be = rng.uniform(0.0, 1.0, (M, H)).astype(np.float32)
+    return st, q, k, v, al, be
+
+
+def _unrolled_chain(st, k, v, al, be, nodes, h):
+    """S after the nodes in order, as the unrolled sum of transition-matrix
+    products: S_c T_1 ... T_n + sum_j beta_j v_j k_j^T T_{j+1} ... T_n with
+    T_j = alpha_j (I - beta_j k_j k_j^T) (numpy fp64 matrix products)."""
+    D = st.shape[1]
+    I = np.eye(D)
+    kd, vd = k.astype(np.float64), v.astype(np.float64)
+    T = [float(al[j, h]) * (I - float(be[j, h]) * np.outer(kd[j, h], kd[j, h])) for j in nodes]
+    def tail(a):
+        P = I.copy()
+        for Tm in T[a:]:
+            P = P @ Tm
+        return P
+    S = st[h].astype(np.float64) @ tail(0)
+    for a, j in enumerate(nodes):
+        S = S + float(be[j, h]) * np.outer(vd[j, h], kd[j, h]) @ tail(a + 1)
+    return S
+
+
+def _root_path(parent, i):
+    chain = [i]
+    while chain[-1] > 0 and 0 <= parent[chain[-1]] < chain[-1]:
+        chain.append(int(parent[chain[-1]]))
+    return chain[::-1]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_delta_tree_matches_unrolled_products_on_every_root_path(seed):
+    rng = np.random.default_rng(200 + seed)
+    M, H, D = 9, 2, 12
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    parent = np.array([0, 0, 1, 1, 0, 4, 2, 6, 3], dtype=np.int32)
+    got = oracle.delta_tree(st, q, k, v, al, be, parent)
+    for i in range(M):
+        for h in range(H):
+            S = _unrolled_chain(st, k, v, al, be, _root_path(parent, i), h)
+            np.testing.assert_allclose(got[i, h], S @ q[i, h].astype(np.float64), rtol=1e-11, atol=1e-11)
+
+
+def test_delta_tree_without_writes_only_decays_the_state():
+    rng = np.random.default_rng(210)
+    M, H, D = 6, 3, 8
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    be[:] = 0.0
+    parent = np.array([0, 0, 1, 2, 0, 4], dtype=np.int32)
+    got = oracle.delta_tree(st, q, k, v, al, be, parent)
+    for i in range(M):
+        decay = np.prod([al[j].astype(np.float64) for j in _root_path(parent, i)], axis=0)  # [H]
+        ref = decay[:, None] * np.einsum("hrc,hc->hr", st.astype(np.float64), q[i].astype(np.float64))
+        np.testing.assert_allclose(got[i], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_delta_rule_overwrites_the_value_stored_under_a_unit_key():
+    """alpha = beta = 1 and |k| = 1: after the step, S k = v exactly (the
+    delta rule replaces what the key retrieves); querying with the node's own
+    key returns its value."""
+    rng = np.random.default_rng(211)
+    M, H, D = 5, 2, 16
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    al[:] = 1.0
+    be[:] = 1.0
+    q = k.copy()
+    got = oracle.delta_tree(st, q, k, v, al, be, np.array([0, 0, 1, 2, 1], dtype=np.int32))
+    np.testing.assert_allclose(got, v.astype(np.float64), rtol=0, atol=1e-6)
+
+
+def test_delta_rule_with_orthonormal_keys_replaces_columns():
+    """Keys e_0, e_1, ... along a chain with alpha = beta = 1: the state is the
+    committed one with column j replaced by v_j for every node j on the path."""
+    rng = np.random.default_rng(212)
+    M, H, D = 4, 1, 6
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    k[:] = 0.0
+    for j in range(M):
+        k[j, 0, j] = 1.0
+    al[:] = 1.0
+    be[:] = 1.0
+    parent = np.array([0, 0, 1, 2], dtype=np.int32)
+    got = oracle.delta_tree(st, q, k, v, al, be, parent)
+    for i in range(M):
+        S = st[0].astype(np.float64).copy()
+        for j in range(i + 1):
+            S[:, j] = v[j, 0]
+        np.testing.assert_allclose(got[i, 0], S @ q[i, 0].astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
+def test_delta_tree_node_ignores_other_branches():
+    rng = np.random.default_rng(213)
+    M, H, D = 7, 2, 8
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    parent = np.array([0, 0, 0, 1, 2, 3, 2], dtype=np.int32)
+    a = oracle.delta_tree(st, q, k, v, al, be, parent)
+    k2, v2 = k.copy(), v.copy()
+    k2[[2, 4, 6]] = rng.standard_normal((3, H, D)).astype(np.float32)  # the other branch of node 5
+    v2[[2, 4, 6]] = rng.standard_normal((3, H, D)).astype(np.float32)
+    b = oracle.delta_tree(st, q, k2, v2, al, be, parent)
+    for i in (0, 1, 3, 5):
+        assert np.array_equal(a[i], b[i])
+
+
+def test_delta_commit_is_the_accepted_nodes_state():
+    rng = np.random.default_rng(214)
+    M, H, D = 8, 2, 8
+    st, q, k, v, al, be = _delta_inputs(rng, M, H, D)
+    parent = np.array([0, 0, 1, 2, 0, 4, 5, 2], dtype=np.int32)
+    path = np.array([4, 5, 6], dtype=np.int32)  # root -> 4 -> 5 -> 6
+    S = oracle.delta_commit(st, k, v, al, be, path, 3)
+    for h in range(H):
+        np.testing.assert_allclose(S[h], _unrolled_chain(st, k, v, al, be, [0, 4, 5, 6], h), rtol=1e-11, atol=1e-11)
+    # the new committed state answers node 6's query as the tree pass did
+    got = oracle.delta_tree(st, q, k, v, al, be, parent)
+    np.testing.assert_allclose(np.einsum("hrc,hc->hr", S, q[6].astype(np.float64)), got[6], rtol=1e-12, atol=1e-12)
+    # no drafted token accepted: only the root advances; a malformed tree changes nothing
+    S0 = oracle.delta_commit(st, k, v, al, be, path, 0)
+    for h in range(H):
+        np.testing.assert_allclose(S0[h], _unrolled_chain(st, k, v, al, be, [0], h), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.delta_commit(st, k, v, al, be, path, -1), st.astype(np.float64))

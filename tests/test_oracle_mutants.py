@@ -54,6 +54,15 @@ MUTANTS = {
     "attn_ignores_scale": ("s[a] = scale * dot;", "s[a] = dot;"),
     "attn_kv_head_modulo": ("const int i = r / Hq, h = r % Hq, hk = h / G;",
                             "const int i = r / Hq, h = r % Hq, hk = h % Hkv;"),
+    "delta_forgets_gate": ("S[(size_t)r * D + c] = alpha * (S[(size_t)r * D + c] - beta * u[r] * (double)k[c]) +",
+                           "S[(size_t)r * D + c] = (S[(size_t)r * D + c] - beta * u[r] * (double)k[c]) +"),
+    "delta_no_erase": ("- beta * u[r] * (double)k[c]) +", "- 0.0 * u[r] * (double)k[c]) +"),
+    "delta_write_unscaled": ("beta * (double)v[r] * (double)k[c];", "(double)v[r] * (double)k[c];"),
+    "delta_chain_skips_root": ("        while (cur > 0) {\n            const int p = parent[cur];\n            if (p < 0 || p >= cur) break;\n            chain[n++] = p;",
+                               "        while (cur > 1) {\n            const int p = parent[cur];\n            if (p < 0 || p >= cur) break;\n            chain[n++] = p;"),
+    "delta_output_transposed": ("for (int c = 0; c < D; ++c) t += S[(size_t)rr * D + c] * (double)qi[c];",
+                                "for (int c = 0; c < D; ++c) t += S[(size_t)c * D + rr] * (double)qi[c];"),
+    "delta_commit_skips_root": ("for (int a = -1; a < n_accept; ++a) {", "for (int a = 0; a < n_accept; ++a) {"),
     "commit_overwrites_root": ("memcpy(c + ((size_t)h * cap + L + 1 + d) * D,", "memcpy(c + ((size_t)h * cap + L + d) * D,"),
 }
 
