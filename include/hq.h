@@ -290,6 +290,41 @@ int hq_tree_attention(const void *q, const void *k_cache, const void *v_cache, i
 int hq_tree_commit_kv(void *k_cache, void *v_cache, int32_t cap, int32_t L, int32_t M, int32_t Hkv, int32_t D,
                       const int32_t *path, const int32_t *n_accept, uint32_t flags, void *stream);
 
+/* Rollback-free DeltaNet tree pass (section "Verifying a draft tree without
+ * restoring model state": a Gated DeltaNet layer keeps a fixed-size state that
+ * every accepted token changes; the verify pass computes every branch's
+ * outputs without changing it, and the state is updated only along the
+ * accepted path).  The page gives no equations; the recurrence is the
+ * published gated delta rule, per head with a D x D state S (rows: value
+ * dimensions, columns: key dimensions):
+ *     S_i = alpha_i S_p (I - beta_i k_i k_i^T) + beta_i v_i k_i^T,  o_i = S_i q_i
+ * with p the parent of tree node i, or the committed state for the root and
+ * for a node whose parent lies outside [0, i).
+ *   state  fp32 [H][D][D], the committed state; only read
+ *   q, k, v  fp32 [M][H][D] (q, k as they enter the recurrence: any
+ *          normalization is applied before); alpha, beta fp32 [M][H]
+ *   parent int32 [M]; M 1..HQ_MAX_M; D = HQ_DELTA_HEAD_DIM
+ *   out    fp32 [M][H][D]
+ * Computed without forming any node's state: o_i = S w_i + sum_j c_j v_j over
+ * node i's root path (w_i, c_j from D-vector steps), fp32 arithmetic.  With
+ * HQ_LAUNCH_PDL the state is read before waiting for the previous kernel of
+ * the stream, which therefore must not write it.  All pointers are device
+ * memory, 16-byte aligned. */
+#define HQ_DELTA_HEAD_DIM 128
+int hq_delta_tree(const float *state, const float *q, const float *k, const float *v, const float *alpha,
+                  const float *beta, const int32_t *parent, int32_t M, int32_t H, int32_t D, float *out,
+                  uint32_t flags, void *stream);
+
+/* Commit of the accepted path into the DeltaNet state (same section): in
+ * place, one step for the root and one for each accepted node path[d],
+ * d < *n_accept, in order (the new state is the accepted node's state).
+ * path and n_accept are hq_tree_accept's outputs in device memory; path
+ * entries outside [1, M) are skipped; nothing changes when *n_accept < 0.
+ * Arguments as in hq_delta_tree. */
+int hq_delta_commit(float *state, const float *k, const float *v, const float *alpha, const float *beta,
+                    const int32_t *path, const int32_t *n_accept, int32_t M, int32_t H, int32_t D, uint32_t flags,
+                    void *stream);
+
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nothing will ever complete, giving up after
  * `limit_ns` nanoseconds (1000..100000000) and setting the error word of

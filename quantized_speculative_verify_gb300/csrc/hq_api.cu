@@ -262,6 +262,34 @@ int hq_tree_commit_kv(void *k_cache, void *v_cache, int32_t cap, int32_t L, int3
                                                  (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
 }
 
+int hq_delta_tree(const float *state, const float *q, const float *k, const float *v, const float *alpha,
+                  const float *beta, const int32_t *parent, int32_t M, int32_t H, int32_t D, float *out,
+                  uint32_t flags, void *stream) {
+    if (M <= 0 || M > HQ_MAX_M || H <= 0 || H > 65535) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (!state || !q || !k || !v || !alpha || !beta || !parent || !out) return HQ_ERR_INVALID_ARG;
+    if (!aligned(state, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(alpha, 4) ||
+        !aligned(beta, 4) || !aligned(parent, 4) || !aligned(out, 16))
+        return HQ_ERR_INVALID_ARG;
+    if (D != HQ_DELTA_HEAD_DIM) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_delta_tree(state, q, k, v, alpha, beta, parent, M, H, out,
+                                             (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int hq_delta_commit(float *state, const float *k, const float *v, const float *alpha, const float *beta,
+                    const int32_t *path, const int32_t *n_accept, int32_t M, int32_t H, int32_t D, uint32_t flags,
+                    void *stream) {
+    if (M <= 0 || M > HQ_MAX_M || H <= 0 || H > 65535) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if (!state || !k || !v || !alpha || !beta || !path || !n_accept) return HQ_ERR_INVALID_ARG;
+    if (!aligned(state, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(alpha, 4) || !aligned(beta, 4) ||
+        !aligned(path, 4) || !aligned(n_accept, 4))
+        return HQ_ERR_INVALID_ARG;
+    if (D != HQ_DELTA_HEAD_DIM) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_delta_commit(state, k, v, alpha, beta, path, n_accept, M, H,
+                                               (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 extern "C" {

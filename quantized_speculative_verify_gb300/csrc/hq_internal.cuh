@@ -263,5 +263,11 @@ cudaError_t launch_tree_attention(const void *q, const void *k, const void *v, i
                                   cudaStream_t s);
 cudaError_t launch_tree_commit_kv(void *k, void *v, int cap, int L, int M, int Hkv, const int32_t *path,
                                   const int32_t *n_accept, bool pdl, cudaStream_t s);
+// Rollback-free DeltaNet tree pass and the accepted-path state commit.
+cudaError_t launch_delta_tree(const float *state, const float *q, const float *k, const float *v, const float *alpha,
+                              const float *beta, const int32_t *parent, int M, int H, float *out, bool pdl,
+                              cudaStream_t s);
+cudaError_t launch_delta_commit(float *state, const float *k, const float *v, const float *alpha, const float *beta,
+                                const int32_t *path, const int32_t *n_accept, int M, int H, bool pdl, cudaStream_t s);
 int device_sm_count();
 }  // namespace hq

@@ -34,9 +34,10 @@ EXPORTS = ("hq_tree_accept_workspace_bytes", "hq_tree_accept", "hq_status_string
            "hq_make_signs",
            "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
            "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc", "hq_tree_attention_workspace_bytes",
-           "hq_tree_attention", "hq_tree_commit_kv")
+           "hq_tree_attention", "hq_tree_commit_kv", "hq_delta_tree", "hq_delta_commit")
 
 HQ_ATTN_HEAD_DIM = 128
+HQ_DELTA_HEAD_DIM = 128
 
 
 class HQError(RuntimeError):
@@ -87,6 +88,8 @@ def load() -> ctypes.CDLL:
         "hq_tree_attention_workspace_bytes": (SZ, [I32]),
         "hq_tree_attention": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, I32, I32, P, ctypes.c_float, P, P, U32, P]),
         "hq_tree_commit_kv": (ctypes.c_int, [P, P, I32, I32, I32, I32, I32, P, P, U32, P]),
+        "hq_delta_tree": (ctypes.c_int, [P, P, P, P, P, P, P, I32, I32, I32, P, U32, P]),
+        "hq_delta_commit": (ctypes.c_int, [P, P, P, P, P, P, P, I32, I32, I32, U32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -345,3 +348,34 @@ def tree_commit_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, M: int,
     """Moves the accepted path next to the root in both caches (in place)."""
     Hkv, cap, D = k_cache.shape
     hq_tree_commit_kv(k_cache, v_cache, cap, L, M, Hkv, D, path, n_accept, flags, stream)
+
+
+def hq_delta_tree(state, q, k, v, alpha, beta, parent, M: int, H: int, D: int, out, flags: int = 0,
+                  stream=None) -> None:
+    _check(load().hq_delta_tree(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(parent), M, H,
+                                D, _ptr(out), flags, _stream(stream)), "hq_delta_tree")
+
+
+def hq_delta_commit(state, k, v, alpha, beta, path, n_accept, M: int, H: int, D: int, flags: int = 0,
+                    stream=None) -> None:
+    _check(load().hq_delta_commit(_ptr(state), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(path),
+                                  _ptr(n_accept), M, H, D, flags, _stream(stream)), "hq_delta_commit")
+
+
+def delta_tree(state: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
+               beta: torch.Tensor, parent: torch.Tensor, out: torch.Tensor = None, flags: int = 0,
+               stream=None) -> torch.Tensor:
+    """Outputs of every tree node of a gated delta-rule layer; the committed
+    state [H][D][D] is only read.  q, k, v fp32 [M][H][D]; alpha, beta [M][H]."""
+    M, H, D = q.shape
+    if out is None:
+        out = torch.empty((M, H, D), dtype=torch.float32, device=q.device)
+    hq_delta_tree(state, q, k, v, alpha, beta, parent, M, H, D, out, flags, stream)
+    return out
+
+
+def delta_commit(state: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor, beta: torch.Tensor,
+                 path: torch.Tensor, n_accept: torch.Tensor, flags: int = 0, stream=None) -> None:
+    """Advances the state (in place) along the root and the accepted path."""
+    M, H, D = k.shape
+    hq_delta_commit(state, k, v, alpha, beta, path, n_accept, M, H, D, flags, stream)

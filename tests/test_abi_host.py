@@ -196,3 +196,24 @@ def test_tree_attention_arguments_are_checked_before_launch():
     assert c(FAKE, FAKE, 100, 50, 0, 8, D, FAKE, FAKE, 0, None) == E
     assert c(FAKE, FAKE, 100, 50, 16, 8, 64, FAKE, FAKE, 0, None) == U
     assert c(FAKE, FAKE, 100, 50, 16, 8, D, FAKE, FAKE, 4, None) == E
+
+
+def test_delta_arguments_are_checked_before_launch():
+    lib = hq.load()
+    E, U = hq.HQ_ERR_INVALID_ARG, hq.HQ_ERR_UNSUPPORTED
+    D = hq.HQ_DELTA_HEAD_DIM
+    t = lib.hq_delta_tree
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, D, FAKE, 0, None) == E    # M = 0
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 129, 4, D, FAKE, 0, None) == E  # M > 128
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 0, D, FAKE, 0, None) == E   # no head
+    assert t(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, FAKE, 0, None) == E
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, None, 0, None) == E
+    assert t(FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, FAKE, 0, None) == E  # q not 16-byte aligned
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, FAKE, 2, None) == E
+    assert t(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 64, FAKE, 0, None) == U
+    c = lib.hq_delta_commit
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, D, 0, None) == E
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 16, 4, D, 0, None) == E
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 4, D, 0, None) == E
+    assert c(FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, 0, None) == E
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 256, 0, None) == U
