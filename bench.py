@@ -60,7 +60,7 @@ def parse_args():
     p.add_argument("--no-attention", action="store_true", help="skip the tree-masked attention measurement")
     p.add_argument("--attn-context", type=int, default=8192, help="committed positions of the attention measurement")
     p.add_argument("--only-attention", action="store_true",
-                   help="run only the tree-attention measurement (for profiling its kernels)")
+                   help="run only the tree-attention and DeltaNet measurements (for profiling their kernels)")
     p.add_argument("--summarize-ncu", metavar="CSV",
                    help="summarize an ncu --csv log of this program into profiles/ and exit")
     p.add_argument("--ncu-command", default="", help="the ncu command line that produced CSV (recorded)")
@@ -456,9 +456,10 @@ def run_gpu(args, ranks: Ranks):
                "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_host.numel() * 4,
                "ms_per_step": e_ms / e_steps, "steps": e_steps}
 
-    attn = None
+    attn = delta = None
     if not args.no_attention:
         attn = measure_tree_attention(torch, hq, device, stream, args, peak)
+        delta = measure_delta_tree(torch, hq, device, stream, args, peak)
 
     cpu = None
     if not args.no_cpu_baseline and ranks.rank == 0:
@@ -485,6 +486,7 @@ def run_gpu(args, ranks: Ranks):
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * (vp.n_act + vp.n_gemm + vp.n_accept_kernels),
             "tree_attention": attn,
+            "delta_tree": delta,
         }
         print(json.dumps(line))
     return 0
@@ -545,6 +547,59 @@ def measure_tree_attention(torch, hq, device, stream, args, peak):
             "steps": reps}
 
 
+def measure_delta_tree(torch, hq, device, stream, args, peak):
+    """Rollback-free DeltaNet tree pass of the 9B-class decoder: its 24 Gated
+    DeltaNet layers, 16 tree nodes, 32 heads with 128 x 128 fp32 states
+    (2 MB per layer).  Three copies of every layer's state (144 MB, larger
+    than L2) are cycled so each step reads its states from HBM, as inside a
+    pass that streams 3.9 GB of weights.  One step = the 24 layers' tree
+    passes from a CUDA graph with programmatic dependent launch.  Algorithmic
+    bytes = the committed states read plus q, k, v, gates in and outputs out."""
+    layers, copies, M, H, D = 24, 3, 16, 32, hq.HQ_DELTA_HEAD_DIM
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4321)
+    states = [torch.randn((H, D, D), generator=gen, device=device) * 0.05 for _ in range(layers * copies)]
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+    qkv = [(torch.randn((M, H, D), generator=gen, device=device),
+            unit(torch.randn((M, H, D), generator=gen, device=device)),
+            torch.randn((M, H, D), generator=gen, device=device),
+            torch.rand((M, H), generator=gen, device=device) * 0.4 + 0.6,
+            torch.rand((M, H), generator=gen, device=device)) for _ in range(layers)]
+    parent = torch.tensor([0, 0, 1, 2, 3, 0, 5, 6, 1, 8, 2, 10, 11, 0, 13, 14], dtype=torch.int32, device=device)
+    outs = [torch.empty((M, H, D), dtype=torch.float32, device=device) for _ in range(layers)]
+    graphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(layers):
+                q, k, v, al, be = qkv[i]
+                hq.hq_delta_tree(states[c * layers + i], q, k, v, al, be, parent, M, H, D, outs[i],
+                                 hq.HQ_LAUNCH_PDL, stream)
+        graphs.append(g)
+    for r in range(max(args.warmup, 3) * copies):
+        graphs[r % copies].replay()
+    reps = max(21, args.steps // 4) // copies * copies
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for r in range(reps):
+        graphs[r % copies].replay()
+    e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    state_bytes = layers * H * D * D * 4
+    io_bytes = layers * (M * H * D * 4 * 4 + M * H * 4 * 2)
+    gbs = (state_bytes + io_bytes) / (ms / 1e3) / 1e9
+    return {"workload": f"9B-class DeltaNet tree pass: {layers} layers, M={M} tree nodes, H={H} heads, "
+                        f"{D}x{D} fp32 states, {copies} copies cycled (inputs larger than L2)",
+            "value": gbs, "unit": "GB/s", "us_per_layer": ms * 1e3 / layers, "ms_per_step": ms,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "algorithmic_bytes_per_layer": (state_bytes + io_bytes) / layers},
+            "kernels": ["k_delta_tree"], "launches_per_step": layers, "steps": reps}
+
+
 def summarize_ncu(args) -> int:
     """Per-kernel launches, time and share from an ncu --csv log; with DRAM
     byte metrics present, also the GEMM's traffic record read by the bench."""
@@ -597,7 +652,7 @@ def summarize_ncu(args) -> int:
 
 
 def run_only_attention(args) -> int:
-    """The tree-attention measurement alone (one line of JSON), for profiling."""
+    """The tree-attention and DeltaNet measurements alone (one line of JSON), for profiling."""
     import torch
     from quantized_speculative_verify_gb300 import hq
     device = torch.device("cuda", 0)
@@ -605,7 +660,8 @@ def run_only_attention(args) -> int:
     peak, _ = measured_peaks()
     stream = torch.cuda.Stream(device=device)
     torch.cuda.set_stream(stream)
-    print(json.dumps(measure_tree_attention(torch, hq, device, stream, args, peak)))
+    print(json.dumps({"tree_attention": measure_tree_attention(torch, hq, device, stream, args, peak),
+                      "delta_tree": measure_delta_tree(torch, hq, device, stream, args, peak)}))
     return 0
 
 
