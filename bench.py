@@ -59,6 +59,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-attention", action="store_true", help="skip the tree-masked attention measurement")
     p.add_argument("--attn-context", type=int, default=8192, help="committed positions of the attention measurement")
+    p.add_argument("--no-sweep", action="store_true", help="skip the K=N=8192 arithmetic-intensity sweep")
     p.add_argument("--only-attention", action="store_true",
                    help="run only the tree-attention and DeltaNet measurements (for profiling their kernels)")
     p.add_argument("--summarize-ncu", metavar="CSV",
@@ -456,6 +457,7 @@ def run_gpu(args, ranks: Ranks):
                "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_host.numel() * 4,
                "ms_per_step": e_ms / e_steps, "steps": e_steps}
 
+    sweep = None if args.no_sweep else measure_sweep(torch, hq, synth, device, stream, args, peak)
     attn = delta = None
     if not args.no_attention:
         attn = measure_tree_attention(torch, hq, device, stream, args, peak)
@@ -487,9 +489,59 @@ def run_gpu(args, ranks: Ranks):
             "gpu_launches": args.steps * (vp.n_act + vp.n_gemm + vp.n_accept_kernels),
             "tree_attention": attn,
             "delta_tree": delta,
+            "sweep": sweep,
         }
         print(json.dumps(line))
     return 0
+
+
+def measure_sweep(torch, hq, synth, device, stream, args, peak):
+    """The arithmetic-intensity sweep: one K=N=8192 layer, W8 G128 and W4 G64,
+    M in {1, ..., 128} rows (activation quantization + GEMM per call, the
+    layer's hot path).  Four copies of the packed layer (153 / 276 MB, larger
+    than L2) are cycled so every call streams its weights from HBM.  Per M:
+    microseconds per call, weight GB/s, integer tera-ops/s (2*M*N*K) and the
+    verify cost ratio t(M) / t(1).  Batches of more than 32 rows run as
+    consecutive 32-row launches that stream the weights again."""
+    out = {}
+    K = N = 8192
+    copies = 4
+    for name in ("sweep_8192_w8", "sweep_8192_w4"):
+        c = synth.CONFIGS[name]
+        signs = hq.hq_make_signs(c["seed"], K)
+        W = synth.weights(N, K, seed=c["seed"], device=device)
+        first = hq.pack_layer(W, c["G"], c["fmt"], signs)
+        layers = [first] + [hq.PackedLayer(first.desc, first.blob.clone(), first.signs) for _ in range(copies - 1)]
+        del W
+        rows = []
+        t1 = None
+        for M in c["Ms"]:
+            X = synth.activations(M, K, seed=c["seed"] + M, device=device)
+            bufs = hq.act_buffers(M, K, device, int8_codes=False)
+            Y = torch.empty((M, N), dtype=torch.float32, device=device)
+            ws = hq.workspace(layers[0].desc, M, device)
+            for i in range(copies * 2):
+                hq.verify_linear(layers[i % copies], X, ws, bufs=bufs, Y=Y, stream=stream)
+            reps = copies * 5
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(reps):
+                hq.verify_linear(layers[i % copies], X, ws, bufs=bufs, Y=Y, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if hq.hq_workspace_status(ws) != hq.HQ_OK:
+                raise SystemExit("device-side wait timed out in the sweep")
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            t1 = us if t1 is None else t1
+            wbytes = layers[0].blob.numel()
+            rows.append({"M": M, "us": us, "weight_gbs": wbytes / us / 1e3, "frac_hbm": wbytes / us / 1e3 / peak,
+                         "int_tops": 2.0 * M * N * K / us / 1e6, "cost_ratio": us / t1})
+        out[name] = {"fmt": c["fmt"], "group": c["G"], "K": K, "N": N, "weight_bytes": layers[0].blob.numel(),
+                     "copies": copies, "rows": rows}
+        del layers
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_tree_attention(torch, hq, device, stream, args, peak):
