@@ -58,7 +58,7 @@ def _check(got, ref, v):
 CASES = [  # M, Hq, Hkv, L
     (1, 8, 8, 0), (1, 32, 8, 1), (2, 4, 1, 0), (5, 8, 2, 63), (16, 32, 8, 64), (16, 32, 8, 65),
     (16, 32, 8, 1000), (31, 16, 4, 300), (64, 8, 8, 129), (128, 32, 8, 40), (128, 16, 1, 7), (17, 64, 4, 200),
-    (3, 32, 32, 5000),
+    (3, 32, 32, 5000), (5, 64, 2, 100), (3, 64, 1, 300), (16, 32, 8, 56), (9, 16, 8, 8),
 ]
 
 
