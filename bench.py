@@ -257,11 +257,26 @@ def run_reference(args, ranks: Ranks):
 
 
 # -------------------------------------------------------------- GPU side ---
+def gemm_source_parts(csrc: str) -> list:
+    """The sources that determine the GEMM's code and launch: its kernel
+    header and instance files, the device helpers (everything before the
+    launcher declarations) and the GEMM launcher of the API file."""
+    def read(f):
+        with open(os.path.join(csrc, f)) as fh:
+            return fh.read()
+    parts = [read("k_gemm.cuh"), read("k_gemm_w4.cu"), read("k_gemm_w8.cu")]
+    internal = read("hq_internal.cuh")
+    parts.append(internal.split("// Launchers (defined in the kernel translation units).")[0])
+    api = read("hq_api.cu")
+    i = api.index("cudaError_t launch_verify_gemm(")
+    parts.append(api[i:api.index("\n}\n", i)])
+    return parts
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("k_gemm.cuh", "hq_internal.cuh", "hq_api.cu"):
-        with open(os.path.join(ROOT, "quantized_speculative_verify_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for part in gemm_source_parts(os.path.join(ROOT, "quantized_speculative_verify_gb300", "csrc")):
+        h.update(part.encode())
     return h.hexdigest()[:16]
 
 
