@@ -59,7 +59,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-attention", action="store_true", help="skip the tree-masked attention measurement")
     p.add_argument("--attn-context", type=int, default=8192, help="committed positions of the attention measurement")
-    p.add_argument("--no-sweep", action="store_true", help="skip the K=N=8192 arithmetic-intensity sweep")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the K=N=8192 arithmetic-intensity sweep and the single-layer timings")
     p.add_argument("--only-attention", action="store_true",
                    help="run only the tree-attention and DeltaNet measurements (for profiling their kernels)")
     p.add_argument("--summarize-ncu", metavar="CSV",
@@ -473,6 +474,7 @@ def run_gpu(args, ranks: Ranks):
                "ms_per_step": e_ms / e_steps, "steps": e_steps}
 
     sweep = None if args.no_sweep else measure_sweep(torch, hq, synth, device, stream, args, peak)
+    layers = None if args.no_sweep else measure_layers(torch, hq, synth, device, stream, peak)
     attn = delta = None
     if not args.no_attention:
         attn = measure_tree_attention(torch, hq, device, stream, args, peak)
@@ -505,6 +507,7 @@ def run_gpu(args, ranks: Ranks):
             "tree_attention": attn,
             "delta_tree": delta,
             "sweep": sweep,
+            "layers": layers,
         }
         print(json.dumps(line))
     return 0
@@ -556,6 +559,65 @@ def measure_sweep(torch, hq, synth, device, stream, args, peak):
                      "copies": copies, "rows": rows}
         del layers
         torch.cuda.empty_cache()
+    return out
+
+
+def measure_layers(torch, hq, synth, device, stream, peak):
+    """The single-layer workloads (tiny 256x256 W4 G32, the 4096x4096 W4 G64
+    projection, the W8 G128 gate+up 4096 -> 2x12288), per M: `warm_us` over
+    cycled copies of the packed layer (repeated calls, weights from HBM where
+    the copies exceed L2), and `cold_us`, the median of 5 single calls each
+    after writing a 512 MB buffer (L2 flushed).  Each call is activation
+    quantization + GEMM, the layer's hot path."""
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    out = {}
+    for name in ("tiny_256", "attn_4096", "gateup_w8"):
+        c = synth.CONFIGS[name]
+        K, N = c["K"], c["N"]
+        signs = hq.hq_make_signs(c["seed"], K)
+        W = synth.weights(N, K, seed=c["seed"], device=device, **c["w"])
+        first = hq.pack_layer(W, c["G"], c["fmt"], signs)
+        del W
+        wbytes = first.blob.numel()
+        copies = max(1, min(8, -(-256 * 1024 * 1024 // wbytes)))
+        packed = [first] + [hq.PackedLayer(first.desc, first.blob.clone(), first.signs) for _ in range(copies - 1)]
+        rows = []
+        for M in c["Ms"]:
+            X = synth.activations(M, K, seed=c["seed"] + 1, device=device, **c["x"])
+            bufs = hq.act_buffers(M, K, device, int8_codes=False)
+            Y = torch.empty((M, N), dtype=torch.float32, device=device)
+            ws = hq.workspace(first.desc, M, device)
+            for i in range(2 * copies):
+                hq.verify_linear(packed[i % copies], X, ws, bufs=bufs, Y=Y, stream=stream)
+            reps = max(20, 2 * copies)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(reps):
+                hq.verify_linear(packed[i % copies], X, ws, bufs=bufs, Y=Y, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            warm = e0.elapsed_time(e1) * 1e3 / reps
+            cold = []
+            for _ in range(5):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                hq.verify_linear(first, X, ws, bufs=bufs, Y=Y, stream=stream)
+                c1.record(stream)
+                c1.synchronize()
+                cold.append(c0.elapsed_time(c1) * 1e3)
+            if hq.hq_workspace_status(ws) != hq.HQ_OK:
+                raise SystemExit("device-side wait timed out in the single-layer timings")
+            cold_us = sorted(cold)[2]
+            rows.append({"M": M, "warm_us": warm, "warm_weight_gbs": wbytes / warm / 1e3, "cold_us": cold_us,
+                         "cold_weight_gbs": wbytes / cold_us / 1e3, "warm_frac_hbm": wbytes / warm / 1e3 / peak})
+        out[name] = {"K": K, "N": N, "fmt": c["fmt"], "group": c["G"], "weight_bytes": wbytes, "copies": copies,
+                     "rows": rows}
+        del packed, first
+        torch.cuda.empty_cache()
+    del flush
     return out
 
 
