@@ -22,9 +22,9 @@
 // stages its committed-state rows (padded rows: conflict-free reads), the
 // nodes' q, k, gates and its value rows in shared memory (one round of
 // loads), walks the nodes (one warp per node, lanes hold 4 dimensions each,
-// dot products by warp shuffles in a fixed order), then forms its 16 rows of
-// S_c w for all nodes (a thread per row, node and half row, four
-// accumulators).  The committed state is read before waiting for the
+// dot products by warp shuffles in a fixed order), then, in the warp that
+// walked a node, forms its 16 rows of S_c w (a thread per row and half row,
+// four accumulators).  The committed state is read before waiting for the
 // previous kernel of the stream: only the commit of the previous step
 // writes it.
 //
@@ -120,12 +120,15 @@ __global__ void __launch_bounds__(DTREE_THREADS, 2) k_delta_tree(const float *__
         reinterpret_cast<float4 *>(s_w + (size_t)i * DD)[lane] = w;
         if (lane < DROWS) s_vs[(size_t)i * DROWS + lane] = vs;
     }
-    __syncthreads();
+    // the products below take node i in the warp that walked it (the same
+    // node-to-warp assignment): no block barrier, warps do not wait for the
+    // deepest walk
+    __syncwarp();
 
     // o_i[row] = S_c[row] . w_i + vs_i[row]: thread (node slot, half, row)
     // sums 64 columns with four accumulators (a quarter warp reads eight
     // different padded rows: no bank conflict), one shuffle joins the halves
-    const int r = threadIdx.x & (DROWS - 1), half = (threadIdx.x >> 4) & 1, slot = threadIdx.x >> 5;
+    const int r = threadIdx.x & (DROWS - 1), half = (threadIdx.x >> 4) & 1, slot = warp;
     const float4 *srow = reinterpret_cast<const float4 *>(s_S + r * DSTRIDE + half * (DD / 2));
     for (int i = slot; i < M; i += NW) {
         const float4 *wp = reinterpret_cast<const float4 *>(s_w + (size_t)i * DD + half * (DD / 2));
