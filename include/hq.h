@@ -19,6 +19,14 @@
  * tokens from one model pass" (the verify batch is the 16-32 token draft
  * tree, "16 rows of work instead of 1").
  *
+ * After the verify pass, the same library accepts the draft tree
+ * (hq_tree_accept) and runs the two stateful layer kinds of the verified model
+ * over the tree without changing their committed state, then commits the
+ * accepted path: tree-masked attention over a KV cache (hq_tree_attention,
+ * hq_tree_commit_kv) and the gated delta-rule DeltaNet layer (hq_delta_tree,
+ * hq_delta_commit).  Source: the same page, section "Verifying a draft tree
+ * without restoring model state".
+ *
  * Conventions
  *   - Row-major everywhere.  X is [M][K], W is [N][K], Y = X W^T is [M][N].
  *   - Pointers are DEVICE pointers unless their name ends in _host.  The
@@ -72,9 +80,11 @@ typedef struct {
 /* Launch with programmatic dependent launch: the kernel may start while the
  * previous kernel of the stream is still running and waits for it (and for
  * its memory) before reading anything that kernel could have produced.
- * hq_verify_gemm additionally starts streaming the packed weights before
- * that wait, so with this flag the blob must not be written by the
- * operation launched immediately before it in the same stream. */
+ * Some inputs are read before that wait, so with this flag they must not be
+ * written by the operation launched immediately before in the same stream:
+ * the blob (hq_verify_gemm streams the packed weights early), the committed
+ * cache positions [0, L) (hq_tree_attention) and the committed state
+ * (hq_delta_tree). */
 #define HQ_LAUNCH_PDL 1u
 
 /* Maximum number of token rows per call. */
@@ -98,8 +108,9 @@ size_t hq_packed_bytes(const hq_layer_desc *desc);
  * output channels, at offsets that depend on neither the layer nor M: one
  * workspace of the largest size serves calls of every layer and M in turn
  * (calls that may overlap on the GPU need workspaces of their own).  It must
- * be zero-filled once after allocation; every call leaves it zero-filled
- * again (except after a time-out, see hq_workspace_status). */
+ * be zero-filled once after allocation; every call leaves the error word and
+ * the counters at zero again (except after a time-out, see
+ * hq_workspace_status); the partial sums need no clearing. */
 size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M);
 
 /* Sign vector of the randomized Hadamard transform ("random sign flips
@@ -186,9 +197,10 @@ int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes,
                     void *stream);
 
 /* Synchronizes `stream`, then reads and clears the error word of a
- * workspace.  Returns HQ_ERR_TIMEOUT if a bounded wait inside
- * hq_verify_gemm gave up since the word was last cleared (the outputs of
- * that call are then incomplete), HQ_OK otherwise. */
+ * workspace (of hq_verify_gemm or hq_tree_attention).  Returns
+ * HQ_ERR_TIMEOUT if a bounded wait inside a call that used the workspace
+ * gave up since the word was last cleared (the outputs of that call are then
+ * incomplete), HQ_OK otherwise. */
 int hq_workspace_status(void *workspace, void *stream);
 
 /* hq_verify_gemm without a caller-supplied workspace, for callers that

@@ -132,7 +132,7 @@ const char *hq_status_string(int status) {
     }
 }
 
-int32_t hq_version(void) { return (1 << 16) | 0; }
+int32_t hq_version(void) { return (1 << 16) | 1; }  // 1.1: tree attention, DeltaNet tree pass and commits
 
 size_t hq_packed_bytes(const hq_layer_desc *desc) {
     if (!desc_ok(desc)) return 0;
