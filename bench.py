@@ -213,9 +213,16 @@ def cpu_oracle_sample(target_s: float = 10.0):
     for _ in range(reps):
         one()
     dt = time.perf_counter() - t
+    # the single-thread build on the same layer, a few repetitions (bounded)
+    t = time.perf_counter()
+    qx, sx, _ = oracle.quant_act(X, G, signs)
+    oracle.verify_gemm(qx, sx, codes, scales, zeros, G, openmp=False)
+    dt1 = time.perf_counter() - t
     return dict(value=wbytes * reps / dt / 1e9, unit="GB/s", cores=oracle.num_threads(True), kind="oracle",
                 sample=f"one 4096x4096 W4 G64 layer (q-projection shape of the pass), M=16, act-quant + GEMM, "
-                       f"{reps} repetitions in {dt:.1f} s"), dt / reps, wbytes
+                       f"{reps} repetitions in {dt:.1f} s",
+                single_thread={"value": wbytes / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                               "sample": f"the same layer once, {dt1:.1f} s"}), dt / reps, wbytes
 
 
 def run_reference(args, ranks: Ranks):
