@@ -481,29 +481,42 @@ def run_gpu(args, ranks: Ranks):
         host_all.copy_(vp.x_all.cpu())
         bufs = [vp.x_all, torch.empty_like(vp.x_all)]
         graphs = [graph, torch.cuda.CUDAGraph()]
+        # the second graph reads the second input buffer and writes the second logits buffer
+        logits_dev = [vp.ys[-1], torch.empty_like(vp.ys[-1])]
         vp.point_inputs_at(bufs[1])
+        vp.ys[-1] = logits_dev[1]
         with torch.cuda.graph(graphs[1], stream=stream):
             vp.launch()
         vp.point_inputs_at(bufs[0])
-        logits_dev = vp.ys[-1]
-        logits_host = torch.empty_like(logits_dev, device="cpu").pin_memory()
-        copy_stream = torch.cuda.Stream(device=device)
+        vp.ys[-1] = logits_dev[0]
+        logits_host = [torch.empty_like(logits_dev[0], device="cpu").pin_memory() for _ in range(2)]
+        h2d_stream = torch.cuda.Stream(device=device)
+        d2h_stream = torch.cuda.Stream(device=device)
         e_steps = max(4, args.steps // 4)
-        done = [torch.cuda.Event(), torch.cuda.Event()]     # the pass that read buffer b is complete
-        copied = [torch.cuda.Event(), torch.cuda.Event()]   # buffer b holds the next step's inputs
+        done = [torch.cuda.Event(), torch.cuda.Event()]     # the pass that used buffer pair b is complete
+        copied = [torch.cuda.Event(), torch.cuda.Event()]   # input buffer b holds the step's inputs
+        read = [torch.cuda.Event(), torch.cuda.Event()]     # logits buffer b was read back
         for b in range(2):
             done[b].record(stream)
+            read[b].record(stream)
 
         def e2e_step(k):
+            # step k's inputs go in on one copy stream while step k-1 runs, and
+            # its logits come back on another while step k+1 runs; the two
+            # buffer pairs alternate between steps
             b = k % 2
-            copy_stream.wait_event(done[b])
-            with torch.cuda.stream(copy_stream):
+            h2d_stream.wait_event(done[b])
+            with torch.cuda.stream(h2d_stream):
                 bufs[b].copy_(host_all, non_blocking=True)
-            copied[b].record(copy_stream)
+            copied[b].record(h2d_stream)
             stream.wait_event(copied[b])
+            stream.wait_event(read[b])       # step k-2's logits are out before they are overwritten
             graphs[b].replay()
             done[b].record(stream)
-            logits_host.copy_(logits_dev, non_blocking=True)
+            d2h_stream.wait_event(done[b])
+            with torch.cuda.stream(d2h_stream):
+                logits_host[b].copy_(logits_dev[b], non_blocking=True)
+            read[b].record(d2h_stream)
 
         for k in range(4):
             e2e_step(k)
@@ -511,14 +524,16 @@ def run_gpu(args, ranks: Ranks):
         ranks.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        copy_stream.wait_event(e0)
+        h2d_stream.wait_event(e0)
         for k in range(e_steps):
             e2e_step(k)
+        for b in range(2):
+            stream.wait_event(read[b])       # every step's logits are on the host
         e1.record(stream)
         e1.synchronize()
         e_ms = ranks.max(e0.elapsed_time(e1))
         e2e = {"value": ranks.sum(vp.algo_weight_bytes * e_steps) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_host.numel() * 4,
+               "h2d_bytes_per_step": vp.h2d_bytes(), "d2h_bytes_per_step": logits_dev[0].numel() * 4,
                "ms_per_step": e_ms / e_steps, "steps": e_steps}
 
     sweep = None if args.no_sweep else measure_sweep(torch, hq, synth, device, stream, args, peak)
