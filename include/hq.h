@@ -86,6 +86,12 @@ typedef struct {
  * cache positions [0, L) (hq_tree_attention) and the committed state
  * (hq_delta_tree). */
 #define HQ_LAUNCH_PDL 1u
+/* hq_verify_gemm only: combine the thread blocks that share an output in a
+ * fixed order, so that results repeat bit for bit from run to run (the blocks
+ * wait for one another before that sum; slower).  Without it, their fp32
+ * partial sums are added into Y atomically as each block finishes, and the
+ * last bits of such outputs may differ between runs. */
+#define HQ_LAUNCH_DETERMINISTIC 2u
 
 /* Maximum number of token rows per call. */
 #define HQ_MAX_M 128
@@ -177,15 +183,20 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *si
  *             before its first use
  * The integer sums P are exact (the codes are multiplied on fp16 tensor cores
  * with fp32 accumulation, which is exact for these ranges).  The fp32 sum
- * over groups is taken in ascending group order; an output whose K range is
- * split across thread blocks sums the blocks' partial sums in ascending K
- * order, so results are deterministic.  The thread blocks that share an
- * output block wait for one another (bounded) before that sum; the grid never
- * exceeds the blocks resident at once, but a kernel running concurrently on
- * another stream that holds SMs for longer than the bound makes the call time
- * out (HQ_ERR_TIMEOUT from hq_workspace_status; zero the workspace again
- * before reusing it after a time-out).  flags: HQ_LAUNCH_DEFAULT or
- * HQ_LAUNCH_PDL (see above). */
+ * over groups is taken in ascending group order.  An output whose K range is
+ * split across thread blocks is the sum of the blocks' partial sums: by
+ * default each block adds sx[m] * (its partial sum) into Y with an fp32
+ * atomic add when it finishes (Y is zeroed first by the kernel itself), so
+ * the order of those adds, and the last bits of such outputs, may change from
+ * run to run; with HQ_LAUNCH_DETERMINISTIC the blocks wait for one another
+ * and sum the partial sums in ascending K order, then multiply by sx[m].
+ * Outputs computed by one block are the same in both modes.  Every wait is
+ * bounded; the grid never exceeds the blocks resident at once, but a kernel
+ * running concurrently on another stream that holds SMs for longer than the
+ * bound makes the call time out (HQ_ERR_TIMEOUT from hq_workspace_status;
+ * zero the workspace again before reusing it after a time-out).  flags: any
+ * of HQ_LAUNCH_PDL, HQ_LAUNCH_DETERMINISTIC (see above); with HQ_LAUNCH_PDL,
+ * Y is written only after the wait for the previous kernel. */
 int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream);
 

@@ -44,7 +44,7 @@ cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream
 }
 
 cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
-                               int32_t *partials, void *workspace, bool pdl, cudaStream_t s) {
+                               int32_t *partials, void *workspace, bool pdl, bool det, cudaStream_t s) {
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
     GemmArgs a;
@@ -54,6 +54,7 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.Y = Y;
     a.partials = partials;
     a.ws = static_cast<uint8_t *>(workspace);
+    a.det = det ? 1 : 0;
     a.M_total = M;
     a.N = g.N;
     a.K = g.K;
@@ -82,7 +83,9 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
         a.M = M - m0 < MAX_M_LAUNCH ? M - m0 : MAX_M_LAUNCH;
         const int mrows = a.M <= 8 ? 8 : a.M <= 16 ? 16 : 32;  // staged activation rows (zero past M)
         a.act_bytes = mrows * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
-        int stages = (60 * 1024) / (g.tile_bytes + a.act_bytes);
+        // about 60 KB of stages; 52 KB at 32 staged rows, whose stash is 8 KB
+        // larger, so that three blocks still fit on an SM
+        int stages = ((mrows > 16 ? 52 : 60) * 1024) / (g.tile_bytes + a.act_bytes);
         if (stages < 2) stages = 2;
         if (stages > 16) stages = 16;
         a.stages = stages;
@@ -132,7 +135,7 @@ const char *hq_status_string(int status) {
     }
 }
 
-int32_t hq_version(void) { return (1 << 16) | 1; }  // 1.1: tree attention, DeltaNet tree pass and commits
+int32_t hq_version(void) { return (1 << 16) | 2; }  // 1.2: HQ_LAUNCH_DETERMINISTIC; split outputs accumulated by default
 
 size_t hq_packed_bytes(const hq_layer_desc *desc) {
     if (!desc_ok(desc)) return 0;
@@ -187,7 +190,7 @@ int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream) {
     if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~(HQ_LAUNCH_PDL | HQ_LAUNCH_DETERMINISTIC)) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
     if (!blob || !qop || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
     if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
@@ -195,7 +198,8 @@ int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop,
         return HQ_ERR_INVALID_ARG;
     const Geom g = geom_of(desc);
     return cuda_status(hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, workspace,
-                                              (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+                                              (flags & HQ_LAUNCH_PDL) != 0, (flags & HQ_LAUNCH_DETERMINISTIC) != 0,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,

@@ -233,6 +233,59 @@ __device__ __forceinline__ bool wait_count_bounded(const int *p, int target, int
     }
 }
 
+__device__ __forceinline__ int atom_add_acquire_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acquire.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_release_cta_shared(uint32_t addr, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta_shared(uint32_t addr) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Wait until the shared-memory word at addr is non-zero (acquire, CTA scope),
+// for at most WAIT_LIMIT_NS.  On time-out records DEV_ERR_TIMEOUT in *err and
+// returns false.
+__device__ __forceinline__ bool wait_flag_bounded(uint32_t addr, int *err) {
+    if (ld_acquire_cta_shared(addr) != 0) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_cta_shared(addr) != 0) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *p >= mark, or until *p has fallen below `own` (the counter was
+// reset, which happens only after the mark was added), for at most
+// WAIT_LIMIT_NS; acquire.  On time-out records DEV_ERR_TIMEOUT in *err and
+// returns false.
+__device__ __forceinline__ bool wait_mark_bounded(const int *p, int mark, int own, int *err) {
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        const int v = ld_acquire_gpu(p);
+        if (v >= mark || v < own) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -248,7 +301,7 @@ cudaError_t launch_pack(const Geom &g, const float *W, const uint32_t *signs, vo
 cudaError_t launch_unpack(const Geom &g, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
                           cudaStream_t s);
 cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
-                               int32_t *partials, void *workspace, bool pdl, cudaStream_t s);
+                               int32_t *partials, void *workspace, bool pdl, bool det, cudaStream_t s);
 cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s);
 // Draft-tree acceptance: ACCEPT_CHUNK logits per thread block of the argmax.
 constexpr int ACCEPT_CHUNK = 8192;

@@ -40,7 +40,7 @@ extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blo
                                       int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream) {
     if (!desc || !hq::desc_valid(desc->K, desc->N, desc->group, desc->format)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~(HQ_LAUNCH_PDL | HQ_LAUNCH_DETERMINISTIC)) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
     if (!blob || !qop || !sx || !Y) return HQ_ERR_INVALID_ARG;
     if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) ||
@@ -61,6 +61,6 @@ extern "C" int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blo
         return HQ_ERR_CUDA;
     const cudaError_t e =
         hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, scratch,
-                               (flags & HQ_LAUNCH_PDL) != 0, s);
+                               (flags & HQ_LAUNCH_PDL) != 0, (flags & HQ_LAUNCH_DETERMINISTIC) != 0, s);
     return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }

@@ -20,10 +20,17 @@
 // Work decomposition (stream-K).  The blob is a sequence of T tiles
 // (n-block major, K minor).  Thread block c owns tiles [c*T/grid,
 // (c+1)*T/grid): one contiguous byte range of the blob.  A block whose range
-// covers an n-block from its first to its last K tile writes Y directly; an
-// n-block split between blocks is finished by whichever contributor arrives
-// last (arrival counter, no waiting), which sums the contributors' fp32
-// partial sums in ascending K order.
+// covers an n-block from its first to its last K tile writes Y directly.  An
+// n-block split between blocks is combined in one of two ways:
+//  - accumulating (default): the block holding the n-block's first K tile
+//    zeroes its outputs when it starts and marks the n-block's counter; each
+//    contributor adds sx * (its partial sum) into Y with fp32 atomic adds as
+//    soon as its segment ends and the mark is visible.  No block waits for
+//    another's tiles; the order of the adds, and so the last bits of a split
+//    output, may differ from run to run.
+//  - deterministic (HQ_LAUNCH_DETERMINISTIC): each contributor stores its
+//    partial sum; when all have arrived they share the work of summing them
+//    in ascending K order, so results repeat bit for bit.
 //
 // Inside a block: one producer thread issues, per tile, a bulk copy of the
 // weight tile and one of the activation block for the tile's features into a
@@ -51,10 +58,15 @@ struct GemmArgs {
     float *Y;            // [M_total][N]
     int32_t *partials;   // check mode: [M_total][N][K/G] or NULL
     uint8_t *ws;
+    int det;                // 1: split outputs summed in fixed order after a wait; 0: accumulated atomically
     int M_total, m0, M;     // rows of the call, first row of this launch, rows of this launch (<= 32)
     int N, K, NGK, NB, KTILES, T, grid, stages;
     int tile_bytes, code_bytes, scale_bytes, act_bytes;
 };
+
+// Added to a split n-block's counter once its outputs are zero (accumulating
+// mode); above any count of arrivals (at most 4 warps x MAX_CTAS blocks).
+constexpr int ZERO_MARK = 1 << 24;
 
 __device__ __forceinline__ int tile_begin(int c, int T, int grid) { return (int)(((long long)c * T) / grid); }
 // thread block whose range contains tile t
@@ -126,6 +138,8 @@ struct GemmCfg {
     static constexpr int NCW = NTILES / NW;       // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int BLOCKS_PER_SM = 3;  // the launch puts three blocks on each SM
+    // accumulating mode: per consumer thread, room for its fp32 sums of one segment
+    static constexpr int STASH_BYTES = NCW * 32 * NW * MT * 4 * 4;
 };
 
 // CHECK: also write the exact integer partial sums (check mode).
@@ -148,11 +162,19 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     const int ntl = t1 - t0;
     int *err = reinterpret_cast<int *>(a.ws);
 
+    // after the ring barriers: the zeroing barrier (accumulating mode: the
+    // consumer warps have zeroed the block's first split n-block) and one
+    // flag per split segment of the block (the producer has seen the
+    // n-block's zeroing mark)
+    uint64_t *zbar = bars + 2 * S;
+    int *sflag = reinterpret_cast<int *>(zbar + 1);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_addr(&bars[i]), 1);
             mbar_init(smem_addr(&bars[S + i]), NCW);
         }
+        mbar_init(smem_addr(zbar), NCW);
+        sflag[0] = sflag[1] = 0;
         fence_mbar_init();
     }
     if (a.M < C::MROWS) {
@@ -168,6 +190,13 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     }
     __syncthreads();
     pdl_launch_dependents();
+
+    const bool det = a.det != 0;
+    // Accumulating mode: this block holds K tile 0 of n-block zb and another
+    // block holds its last K tile -> this block zeroes zb's outputs.
+    const int zb = (t1 - 1) / a.KTILES;
+    const bool zeroer = !det && ntl > 0 && zb * a.KTILES >= t0 && (zb + 1) * a.KTILES > t1;
+    int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
 
     if (warp == NCW) {
         // ------------------------------------------------------ producer ---
@@ -187,6 +216,25 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                 for (int kk = 0; kk < blocks; ++kk)
                     bulk_copy_g2s(dst + kk * region_bytes, src + (size_t)kk * a.M_total * 256, row_bytes, fb, pol_a);
             };
+            // Accumulating mode: after the copies of a tile that ends a split
+            // segment, count this block into the n-block's counter (acquire),
+            // wait until the zeroing mark is in (or the counter was reset,
+            // which happens only after the mark), reset the counter if this
+            // count completes it, and raise the segment's flag for the
+            // consumers (release, CTA scope).  The round trips fall on this
+            // thread, which runs stages ahead of the consumers.
+            int nsplit = 0;
+            auto check = [&](int j) {
+                const int t = t0 + j, bb = t / KTILES, kb = t - bb * KTILES;
+                if (!((kb == KTILES - 1 || j == ntl - 1) && !(bb * KTILES >= t0 && kb == KTILES - 1))) return;
+                const int nc = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid) -
+                               cta_of_tile(bb * KTILES, a.T, a.grid) + 1;
+                const int v = atom_add_acquire_gpu(&ctr[bb], 1);
+                if (v < ZERO_MARK) wait_mark_bounded(&ctr[bb], ZERO_MARK, v + 1, err);
+                if (v == ZERO_MARK + nc - 1) st_release_gpu(&ctr[bb], 0);
+                st_release_cta_shared(smem_addr(&sflag[nsplit]), 1);
+                ++nsplit;
+            };
             int i = 0;
             // Weights never depend on earlier kernels of the stream: the first
             // stages' weight copies go out before waiting for them.
@@ -198,6 +246,14 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
             }
             pdl_wait();
             for (int j = 0; j < i; ++j) copy_acts(j, j);
+            if (!det) {
+                if (zeroer) {
+                    // the consumers' zero stores are ordered before the mark
+                    mbar_wait_bounded(smem_addr(zbar), 0u, err);
+                    red_add_release_gpu(&ctr[zb], ZERO_MARK);
+                }
+                for (int j = 0; j < i; ++j) check(j);
+            }
             for (; i < ntl; ++i) {
                 const int st = i % S;
                 const uint32_t ph = (uint32_t)((i / S) & 1);
@@ -207,6 +263,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                 bulk_copy_g2s(smem_addr(ring + (size_t)st * stage_bytes),
                               a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
                 copy_acts(i, st);
+                if (!det) check(i);
             }
             // No copy may still be landing in shared memory when the block exits.
             const int issued = i;
@@ -221,7 +278,6 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     const int g8 = lane >> 2, tig = lane & 3;
     const int M = a.M, N = a.N, KTILES = a.KTILES;
     float *wsp = reinterpret_cast<float *>(a.ws + ws_partial_offset());
-    int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
     const float *sxm = a.sx + a.m0;
     float *Ym = a.Y + (size_t)a.m0 * N;
     // byte offsets of this lane's B operand rows (token tt*8 + g8) in a stage
@@ -236,6 +292,24 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     // (slot 0) and its last one (slot 1)
     int pend0 = -1, pend1 = -1;
     const int first_b = t0 / KTILES;
+    // Accumulating mode: a split segment whose flag is not yet raised when it
+    // ends parks its sums here (per warp, lane-minor) and adds them after the
+    // block's last tile; def_b is its n-block, def_s its flag.  nsplit counts
+    // the split segments met so far (the producer raises their flags in the
+    // same order).
+    float *stash = reinterpret_cast<float *>(smem + (size_t)S * stage_bytes + (size_t)S * 16 + 16) +
+                   (size_t)warp * (NW * MT * 4 * 32);
+    int def_b = -1, def_s = 0, nsplit = 0;
+    if (zeroer) {
+        // zero zb's outputs; the producer adds the n-block's mark once every
+        // warp has arrived
+        for (int q = threadIdx.x; q < M * BN; q += NCW * 32) {
+            const int tok = q / BN, n = zb * BN + (q - tok * BN);
+            if (n < N) Ym[(size_t)tok * N + n] = 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(zbar));
+    }
 
     // running position: tile t0 + i is n-block b, K tile kt, in stage st of phase ph
     int b = t0 / KTILES, kt = t0 - b * KTILES, st = 0;
@@ -389,7 +463,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                             if (tok < M && n < N)
                                 Ym[(size_t)tok * N + n] = __fmul_rn(__ldg(sxm + tok), facc[j][tt][e]);
                         }
-            } else {
+            } else if (det) {
                 // part of the K range: publish the partial sums now, count the
                 // arrival once this block's tiles are all done
                 const int slot = b == first_b ? 0 : 1;
@@ -408,6 +482,34 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                     pend0 = b;
                 else
                     pend1 = b;
+            } else if (ld_acquire_cta_shared(smem_addr(&sflag[nsplit])) != 0 || i == ntl - 1) {
+                // part of the K range, accumulating mode: once the zeroing is
+                // visible (the segment's flag), add sx * (this block's sum) into Y
+                if (ok) ok = wait_flag_bounded(smem_addr(&sflag[nsplit]), err);
+                ++nsplit;
+#pragma unroll
+                for (int j = 0; j < NW; ++j)
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int row = (warp * NW + j) * 16 + g8 + 8 * (e >> 1);
+                            const int tok = tt * 8 + tig * 2 + (e & 1);
+                            const int n = b * BN + row;
+                            if (tok < M && n < N)
+                                atomicAdd(Ym + (size_t)tok * N + n, __fmul_rn(__ldg(sxm + tok), facc[j][tt][e]));
+                        }
+            } else {
+                // the mark is not visible yet (a segment that ends soon after
+                // the start): park the sums and add them after the last tile
+#pragma unroll
+                for (int j = 0; j < NW; ++j)
+#pragma unroll
+                    for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) stash[((j * MT + tt) * 4 + e) * 32 + lane] = facc[j][tt][e];
+                def_b = b;
+                def_s = nsplit++;
             }
         }
         // advance the running position
@@ -419,6 +521,24 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
             kt = 0;
             ++b;
         }
+    }
+
+    // Accumulating mode: the parked segment, if any.
+    if (def_b >= 0) {
+        if (ok) ok = wait_flag_bounded(smem_addr(&sflag[def_s]), err);
+#pragma unroll
+        for (int j = 0; j < NW; ++j)
+#pragma unroll
+            for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = (warp * NW + j) * 16 + g8 + 8 * (e >> 1);
+                    const int tok = tt * 8 + tig * 2 + (e & 1);
+                    const int n = def_b * BN + row;
+                    if (tok < M && n < N)
+                        atomicAdd(Ym + (size_t)tok * N + n,
+                                  __fmul_rn(__ldg(sxm + tok), stash[((j * MT + tt) * 4 + e) * 32 + lane]));
+                }
     }
 
     // Split n-blocks: every contributor arrives, waits until all contributors
@@ -542,13 +662,14 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     }
 }
 
-// Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers
-// and a flag word.
+// Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers,
+// a flag word and the accumulating mode's stash.
 template <int FMT, int G, int MT, bool CHECK>
 cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     using C = GemmCfg<FMT, G, MT>;
     auto kern = k_verify_gemm<FMT, G, MT, CHECK>;
-    const size_t smem = (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16;
+    const size_t smem =
+        (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16 + C::STASH_BYTES;
     static int configured_for = -1;  // device the attribute was last set for
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -25,6 +25,7 @@ HQ_W4_ASYM = 0
 HQ_W8_SYM = 1
 HQ_LAUNCH_DEFAULT = 0
 HQ_LAUNCH_PDL = 1
+HQ_LAUNCH_DETERMINISTIC = 2
 HQ_MAX_M = 128
 
 FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
@@ -281,7 +282,7 @@ def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torc
     qx, qop, sx = bufs
     if Y is None:
         Y = torch.empty((M, layer.N), dtype=torch.float32, device=X.device)
-    hq_rotate_quant_act(X, M, K, layer.signs, qx, qop, sx, flags, stream)
+    hq_rotate_quant_act(X, M, K, layer.signs, qx, qop, sx, flags & HQ_LAUNCH_PDL, stream)
     hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, partials, ws, flags, stream)
     return Y
 

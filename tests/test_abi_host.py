@@ -136,6 +136,7 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert lib.hq_verify_gemm(D, FAKE + 8, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, FAKE, FAKE + 8, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 8, None) == E
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 4, None) == E  # unknown flag bit
     assert lib.hq_verify_gemm(ctypes.byref(bad), FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     # unpack / status / self-test
     assert lib.hq_unpack_codes(D, FAKE, FAKE, FAKE, None, None) == E  # W4 needs zeros

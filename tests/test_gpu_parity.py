@@ -49,7 +49,9 @@ def assert_close(y, ref_out):
     a few ulp of the partial sums, so the relative part is taken against the
     magnitude of the sum being formed, sx * sum_g |scale * P|; in addition at
     least STRICT_FRACTION of the outputs must meet the tolerance relative to
-    |Y| itself."""
+    |Y| itself.  In the default (accumulating) mode each thread block adds
+    sx * (its partial sum) into Y in whatever order the blocks finish: one
+    more rounding per block, of the same size, well inside the bound."""
     y = np.asarray(y, dtype=np.float64)
     ref = np.asarray(ref_out["Y"], dtype=np.float64)
     err = np.abs(y - ref)
@@ -170,7 +172,10 @@ def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     ws = hq.workspace(layer.desc, M, DEV)
     bufs = hq.act_buffers(M, K, DEV)
     P = torch.empty((M, layer.N, K // G), dtype=torch.int32, device=DEV) if check else None
-    Y = hq.verify_linear(layer, X.to(DEV), ws, bufs=bufs, partials=P, flags=flags)
+    # Y starts as NaN: an output the kernel fails to write (or to zero before
+    # accumulating into it) stays NaN and fails the comparison
+    Y = torch.full((M, layer.N), float("nan"), dtype=torch.float32, device=DEV)
+    hq.verify_linear(layer, X.to(DEV), ws, Y=Y, bufs=bufs, partials=P, flags=flags)
     assert hq.hq_workspace_status(ws) == hq.HQ_OK
     torch.cuda.synchronize()
     # every call leaves the error word and the n-block counters (after 16 MiB
@@ -185,12 +190,13 @@ GEMM_CASES = [("w4", 1, 256, 256, 32), ("w4", 16, 256, 256, 32), ("w4", 3, 512, 
               ("w8", 1, 4096, 256, 256), ("w4", 40, 2048, 1000, 128)]
 
 
+@pytest.mark.parametrize("flags", [hq.HQ_LAUNCH_DEFAULT, hq.HQ_LAUNCH_DETERMINISTIC])
 @pytest.mark.parametrize("fmt,M,K,N,G", GEMM_CASES)
-def test_gemm_partials_bit_exact_and_output_close(fmt, M, K, N, G):
+def test_gemm_partials_bit_exact_and_output_close(fmt, M, K, N, G, flags):
     X = synth.activations(M, K, seed=M + K, outlier_channels=2)
     W = synth.weights(N, K, seed=N + K + 1, outlier_frac=0.005)
     s_host, _ = signs_pair(M * N + K, K)
-    r = run_layer(X, W, G, fmt, s_host, check=True)
+    r = run_layer(X, W, G, fmt, s_host, check=True, flags=flags)
     ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
     assert np.array_equal(r["P"], ref["P"])
     assert_close(r["Y"], ref)
@@ -204,21 +210,31 @@ def test_gemm_unsplit_blocks_are_bit_exact():
     W = synth.weights(N, K, seed=2)
     s_host, _ = signs_pair(5, K)
     for fmt in ("w4", "w8"):
-        r = run_layer(X, W, G, fmt, s_host)
-        ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
-        assert np.array_equal(r["Y"].view(np.uint32), ref["Y"].view(np.uint32))
+        for flags in (hq.HQ_LAUNCH_DEFAULT, hq.HQ_LAUNCH_DETERMINISTIC):
+            r = run_layer(X, W, G, fmt, s_host, flags=flags)
+            ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+            assert np.array_equal(r["Y"].view(np.uint32), ref["Y"].view(np.uint32))
 
 
-def test_gemm_pdl_flag_and_repeat_are_identical():
+def test_gemm_deterministic_flag_repeats_bit_for_bit():
+    # every n-block of this layer is split between thread blocks
     M, K, N, G = 16, 4096, 1024, 64
     X = synth.activations(M, K, seed=11, outlier_channels=2)
     W = synth.weights(N, K, seed=12)
     s_host, _ = signs_pair(13, K)
-    r0 = run_layer(X, W, G, "w4", s_host)
-    r1 = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
-    r2 = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
+    det = hq.HQ_LAUNCH_DETERMINISTIC
+    r0 = run_layer(X, W, G, "w4", s_host, flags=det)
+    r1 = run_layer(X, W, G, "w4", s_host, flags=det | hq.HQ_LAUNCH_PDL, layer=r0["layer"])
+    r2 = run_layer(X, W, G, "w4", s_host, flags=det | hq.HQ_LAUNCH_PDL, layer=r0["layer"])
     assert np.array_equal(r0["Y"].view(np.uint32), r1["Y"].view(np.uint32))
     assert np.array_equal(r1["Y"].view(np.uint32), r2["Y"].view(np.uint32))
+    # the accumulating mode, repeated on the same layer, stays within the
+    # oracle's tolerance every time
+    ref = oracle.verify_linear(X.numpy(), W.numpy(), G, "w4", s_host)
+    assert_close(r0["Y"], ref)
+    for _ in range(3):
+        r = run_layer(X, W, G, "w4", s_host, flags=hq.HQ_LAUNCH_PDL, layer=r0["layer"])
+        assert_close(r["Y"], ref)
 
 
 def test_shared_workspace_across_layers_and_batches():
@@ -235,12 +251,24 @@ def test_shared_workspace_across_layers_and_batches():
         inputs.append(synth.activations(M, K, seed=300 + i, outlier_channels=2).to(DEV))
     need = max(hq.hq_workspace_bytes(l.desc, x.shape[0]) for l, x in zip(layers, inputs))
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
-    shared = [hq.verify_linear(l, x, ws, flags=hq.HQ_LAUNCH_PDL) for l, x in zip(layers, inputs)]
+    det = hq.HQ_LAUNCH_DETERMINISTIC
+    shared = [hq.verify_linear(l, x, ws, flags=hq.HQ_LAUNCH_PDL | det) for l, x in zip(layers, inputs)]
+    # the accumulating mode in the same chain, alternating with the other mode
+    accum = []
+    for l, x in zip(layers, inputs):
+        accum.append(hq.verify_linear(l, x, ws, flags=hq.HQ_LAUNCH_PDL))
+        hq.verify_linear(l, x, ws, flags=hq.HQ_LAUNCH_PDL | det)
     torch.cuda.synchronize()
     assert hq.hq_workspace_status(ws) == hq.HQ_OK
-    for l, x, y in zip(layers, inputs, shared):
-        fresh = hq.verify_linear(l, x, hq.workspace(l.desc, x.shape[0], DEV))
+    assert not ws[:16].any() and not ws[COUNTER_OFFSET:].any()
+    for l, x, y, ya in zip(layers, inputs, shared, accum):
+        fresh = hq.verify_linear(l, x, hq.workspace(l.desc, x.shape[0], DEV), flags=det)
         assert torch.equal(y.view(torch.int32), fresh.view(torch.int32))
+        # same outputs up to the order of the fp32 adds of split outputs:
+        # within 1e-5 of the largest output of the row
+        d = (ya.double() - y.double()).abs()
+        assert not torch.isnan(ya).any()
+        assert (d <= ATOL + RTOL * y.double().abs().amax(dim=1, keepdim=True)).all()
 
 
 def test_gemm_extreme_codes_int32_headroom():
