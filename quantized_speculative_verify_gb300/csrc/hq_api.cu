@@ -83,9 +83,7 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
         a.M = M - m0 < MAX_M_LAUNCH ? M - m0 : MAX_M_LAUNCH;
         const int mrows = a.M <= 8 ? 8 : a.M <= 16 ? 16 : 32;  // staged activation rows (zero past M)
         a.act_bytes = mrows * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
-        // about 60 KB of stages; 52 KB at 32 staged rows, whose stash is 8 KB
-        // larger, so that three blocks still fit on an SM
-        int stages = ((mrows > 16 ? 52 : 60) * 1024) / (g.tile_bytes + a.act_bytes);
+        int stages = (60 * 1024) / (g.tile_bytes + a.act_bytes);
         if (stages < 2) stages = 2;
         if (stages > 16) stages = 16;
         a.stages = stages;

@@ -239,6 +239,12 @@ __device__ __forceinline__ int atom_add_acquire_gpu(int *p, int v) {
     return old;
 }
 
+__device__ __forceinline__ int atom_add_release_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void st_release_cta_shared(uint32_t addr, int v) {
     asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -263,10 +269,6 @@ __device__ __forceinline__ bool wait_flag_bounded(uint32_t addr, int *err) {
             return false;
         }
     }
-}
-
-__device__ __forceinline__ void st_release_gpu(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Wait until *p >= mark, or until *p has fallen below `own` (the counter was

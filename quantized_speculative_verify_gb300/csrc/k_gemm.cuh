@@ -64,8 +64,9 @@ struct GemmArgs {
     int tile_bytes, code_bytes, scale_bytes, act_bytes;
 };
 
-// Added to a split n-block's counter once its outputs are zero (accumulating
-// mode); above any count of arrivals (at most 4 warps x MAX_CTAS blocks).
+// Accumulating mode: added (with the zeroing block's own arrival, + 1) to a
+// split n-block's counter once its outputs are zero; above any count of
+// arrivals (at most MAX_CTAS blocks).
 constexpr int ZERO_MARK = 1 << 24;
 
 __device__ __forceinline__ int tile_begin(int c, int T, int grid) { return (int)(((long long)c * T) / grid); }
@@ -138,8 +139,6 @@ struct GemmCfg {
     static constexpr int NCW = NTILES / NW;       // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int BLOCKS_PER_SM = 3;  // the launch puts three blocks on each SM
-    // accumulating mode: per consumer thread, room for its fp32 sums of one segment
-    static constexpr int STASH_BYTES = NCW * 32 * NW * MT * 4 * 4;
 };
 
 // CHECK: also write the exact integer partial sums (check mode).
@@ -162,18 +161,15 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     const int ntl = t1 - t0;
     int *err = reinterpret_cast<int *>(a.ws);
 
-    // after the ring barriers: the zeroing barrier (accumulating mode: the
-    // consumer warps have zeroed the block's first split n-block) and one
-    // flag per split segment of the block (the producer has seen the
-    // n-block's zeroing mark)
-    uint64_t *zbar = bars + 2 * S;
-    int *sflag = reinterpret_cast<int *>(zbar + 1);
+    // after the ring barriers, accumulating mode: one flag per split segment
+    // of the block, raised by the producer once the n-block's zeroing is
+    // visible
+    int *sflag = reinterpret_cast<int *>(bars + 2 * S);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_addr(&bars[i]), 1);
             mbar_init(smem_addr(&bars[S + i]), NCW);
         }
-        mbar_init(smem_addr(zbar), NCW);
         sflag[0] = sflag[1] = 0;
         fence_mbar_init();
     }
@@ -222,16 +218,23 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
             // which happens only after the mark), reset the counter if this
             // count completes it, and raise the segment's flag for the
             // consumers (release, CTA scope).  The round trips fall on this
-            // thread, which runs stages ahead of the consumers.
+            // thread, which runs stages ahead of the consumers.  The zeroing
+            // block's own n-block needs neither: its mark carries its count,
+            // and its consumers zeroed before a block barrier.  Every access
+            // to a counter is a read-modify-write, so the reset continues the
+            // mark's release sequence and a wait that reads it acquires the
+            // zeroing.
             int nsplit = 0;
             auto check = [&](int j) {
                 const int t = t0 + j, bb = t / KTILES, kb = t - bb * KTILES;
                 if (!((kb == KTILES - 1 || j == ntl - 1) && !(bb * KTILES >= t0 && kb == KTILES - 1))) return;
-                const int nc = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid) -
-                               cta_of_tile(bb * KTILES, a.T, a.grid) + 1;
-                const int v = atom_add_acquire_gpu(&ctr[bb], 1);
-                if (v < ZERO_MARK) wait_mark_bounded(&ctr[bb], ZERO_MARK, v + 1, err);
-                if (v == ZERO_MARK + nc - 1) st_release_gpu(&ctr[bb], 0);
+                if (!(zeroer && bb == zb)) {
+                    const int nc = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid) -
+                                   cta_of_tile(bb * KTILES, a.T, a.grid) + 1;
+                    const int v = atom_add_acquire_gpu(&ctr[bb], 1);
+                    if (v < ZERO_MARK) wait_mark_bounded(&ctr[bb], ZERO_MARK, v + 1, err);
+                    if (v == ZERO_MARK + nc - 1) atomicExch(&ctr[bb], 0);
+                }
                 st_release_cta_shared(smem_addr(&sflag[nsplit]), 1);
                 ++nsplit;
             };
@@ -246,14 +249,8 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
             }
             pdl_wait();
             for (int j = 0; j < i; ++j) copy_acts(j, j);
-            if (!det) {
-                if (zeroer) {
-                    // the consumers' zero stores are ordered before the mark
-                    mbar_wait_bounded(smem_addr(zbar), 0u, err);
-                    red_add_release_gpu(&ctr[zb], ZERO_MARK);
-                }
+            if (!det)
                 for (int j = 0; j < i; ++j) check(j);
-            }
             for (; i < ntl; ++i) {
                 const int st = i % S;
                 const uint32_t ph = (uint32_t)((i / S) & 1);
@@ -292,23 +289,18 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     // (slot 0) and its last one (slot 1)
     int pend0 = -1, pend1 = -1;
     const int first_b = t0 / KTILES;
-    // Accumulating mode: a split segment whose flag is not yet raised when it
-    // ends parks its sums here (per warp, lane-minor) and adds them after the
-    // block's last tile; def_b is its n-block, def_s its flag.  nsplit counts
-    // the split segments met so far (the producer raises their flags in the
-    // same order).
-    float *stash = reinterpret_cast<float *>(smem + (size_t)S * stage_bytes + (size_t)S * 16 + 16) +
-                   (size_t)warp * (NW * MT * 4 * 32);
-    int def_b = -1, def_s = 0, nsplit = 0;
+    // Accumulating mode: nsplit counts the split segments met so far (the
+    // producer raises their flags in the same order).  The zeroing block
+    // zeroes zb's outputs, then adds the mark and its own arrival (release);
+    // mark_old, the count before it, is read after the last tile.
+    int nsplit = 0, mark_old = 0;
     if (zeroer) {
-        // zero zb's outputs; the producer adds the n-block's mark once every
-        // warp has arrived
         for (int q = threadIdx.x; q < M * BN; q += NCW * 32) {
             const int tok = q / BN, n = zb * BN + (q - tok * BN);
             if (n < N) Ym[(size_t)tok * N + n] = 0.0f;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(zbar));
+        named_barrier(1, NCW * 32);
+        if (threadIdx.x == 0) mark_old = atom_add_release_gpu(&ctr[zb], ZERO_MARK + 1);
     }
 
     // running position: tile t0 + i is n-block b, K tile kt, in stage st of phase ph
@@ -482,7 +474,7 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                     pend0 = b;
                 else
                     pend1 = b;
-            } else if (ld_acquire_cta_shared(smem_addr(&sflag[nsplit])) != 0 || i == ntl - 1) {
+            } else {
                 // part of the K range, accumulating mode: once the zeroing is
                 // visible (the segment's flag), add sx * (this block's sum) into Y
                 if (ok) ok = wait_flag_bounded(smem_addr(&sflag[nsplit]), err);
@@ -499,17 +491,6 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
                             if (tok < M && n < N)
                                 atomicAdd(Ym + (size_t)tok * N + n, __fmul_rn(__ldg(sxm + tok), facc[j][tt][e]));
                         }
-            } else {
-                // the mark is not visible yet (a segment that ends soon after
-                // the start): park the sums and add them after the last tile
-#pragma unroll
-                for (int j = 0; j < NW; ++j)
-#pragma unroll
-                    for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) stash[((j * MT + tt) * 4 + e) * 32 + lane] = facc[j][tt][e];
-                def_b = b;
-                def_s = nsplit++;
             }
         }
         // advance the running position
@@ -523,22 +504,11 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
         }
     }
 
-    // Accumulating mode: the parked segment, if any.
-    if (def_b >= 0) {
-        if (ok) ok = wait_flag_bounded(smem_addr(&sflag[def_s]), err);
-#pragma unroll
-        for (int j = 0; j < NW; ++j)
-#pragma unroll
-            for (int tt = 0; tt < MT; ++tt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = (warp * NW + j) * 16 + g8 + 8 * (e >> 1);
-                    const int tok = tt * 8 + tig * 2 + (e & 1);
-                    const int n = def_b * BN + row;
-                    if (tok < M && n < N)
-                        atomicAdd(Ym + (size_t)tok * N + n,
-                                  __fmul_rn(__ldg(sxm + tok), stash[((j * MT + tt) * 4 + e) * 32 + lane]));
-                }
+    // Accumulating mode: if every other contributor of zb counted before the
+    // mark, the mark completed the count and this block resets the counter.
+    if (zeroer && threadIdx.x == 0) {
+        const int nc = cta_of_tile(zb * KTILES + KTILES - 1, a.T, a.grid) - cta_of_tile(zb * KTILES, a.T, a.grid) + 1;
+        if (mark_old == nc - 1) atomicExch(&ctr[zb], 0);
     }
 
     // Split n-blocks: every contributor arrives, waits until all contributors
@@ -662,14 +632,13 @@ __global__ void __launch_bounds__(GemmCfg<FMT, G, MT>::THREADS, GemmCfg<FMT, G, 
     }
 }
 
-// Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers,
-// a flag word and the accumulating mode's stash.
+// Launch one instance.  Dynamic shared memory: the stage ring, 2*S mbarriers
+// and the accumulating mode's two segment flags.
 template <int FMT, int G, int MT, bool CHECK>
 cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     using C = GemmCfg<FMT, G, MT>;
     auto kern = k_verify_gemm<FMT, G, MT, CHECK>;
-    const size_t smem =
-        (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16 + C::STASH_BYTES;
+    const size_t smem = (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16;
     static int configured_for = -1;  // device the attribute was last set for
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
