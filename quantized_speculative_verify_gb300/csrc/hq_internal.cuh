@@ -2,6 +2,7 @@
 // of the quantized speculative-verify linear layer (sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -325,4 +326,28 @@ cudaError_t launch_delta_tree(const float *state, const float *q, const float *k
 cudaError_t launch_delta_commit(float *state, const float *k, const float *v, const float *alpha, const float *beta,
                                 const int32_t *path, const int32_t *n_accept, int M, int H, bool pdl, cudaStream_t s);
 int device_sm_count();
+
+// Per-device results of one-time launch set-up (function attributes,
+// occupancy), safe to use from several host threads at once.  cache[dev]
+// holds value + 1 once known (0: not yet); devices >= CACHE_DEVICES are not
+// cached.  compute(int *out) returns a cudaError_t and writes a non-negative
+// value; concurrent first calls may both compute it, with the same result.
+constexpr int CACHE_DEVICES = 64;
+template <class F>
+cudaError_t cached_per_device(std::atomic<int> (&cache)[CACHE_DEVICES], int dev, int *out, F compute) {
+    const bool cached = dev >= 0 && dev < CACHE_DEVICES;
+    if (cached) {
+        const int c = cache[dev].load(std::memory_order_acquire);
+        if (c > 0) {
+            *out = c - 1;
+            return cudaSuccess;
+        }
+    }
+    int v = 0;
+    const cudaError_t e = compute(&v);
+    if (e != cudaSuccess) return e;
+    if (cached) cache[dev].store(v + 1, std::memory_order_release);
+    *out = v;
+    return cudaSuccess;
+}
 }  // namespace hq

@@ -504,15 +504,16 @@ cudaError_t launch_tree_attention(const void *q, const void *k, const void *v, i
     a.rows_pad = rows_pad;
     a.c_log2 = scale * 1.4426950408889634f;
 
-    static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_for != dev) {
-        e = cudaFuncSetAttribute(k_tree_attn_split, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ASMEM);
-        if (e != cudaSuccess) return e;
-        configured_for = dev;
-    }
+    static std::atomic<int> configured[CACHE_DEVICES];
+    int done = 0;
+    e = cached_per_device(configured, dev, &done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(k_tree_attn_split, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ASMEM);
+    });
+    if (e != cudaSuccess) return e;
     CUtensorMap tk, tv;
     e = cache_map(&tk, k, total, cap, Hkv);
     if (e != cudaSuccess) return e;

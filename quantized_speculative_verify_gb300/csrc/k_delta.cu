@@ -196,16 +196,17 @@ cudaError_t launch_delta_tree(const float *state, const float *q, const float *k
                               const float *beta, const int32_t *parent, int M, int H, float *out, bool pdl,
                               cudaStream_t s) {
     const size_t smem = (size_t)DROWS * DSTRIDE * 4 + (size_t)M * (2 * DD + 2 * DROWS + 3) * 4;
-    static int configured_for = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_for != dev) {
-        e = cudaFuncSetAttribute(k_delta_tree, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static std::atomic<int> configured[CACHE_DEVICES];
+    int done = 0;
+    e = cached_per_device(configured, dev, &done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(k_delta_tree, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)((size_t)DROWS * DSTRIDE * 4 + (size_t)HQ_MAX_M * (2 * DD + 2 * DROWS + 3) * 4));
-        if (e != cudaSuccess) return e;
-        configured_for = dev;
-    }
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = delta_config(dim3((unsigned)H, DD / DROWS), dim3(DTREE_THREADS), smem, pdl, s, attr);
     return cudaLaunchKernelEx(&cfg, k_delta_tree, state, q, k, v, alpha, beta, parent, M, H, out);

@@ -647,25 +647,27 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     using C = GemmCfg<FMT, G, MT>;
     auto kern = k_verify_gemm<FMT, G, MT, CHECK>;
     const size_t smem = (size_t)a.stages * (size_t)(a.tile_bytes + a.act_bytes) + (size_t)a.stages * 16 + 16;
-    static int configured_for = -1;  // device the attribute was last set for
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_for != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        configured_for = dev;
-    }
+    static std::atomic<int> configured[CACHE_DEVICES];
+    int done = 0;
+    e = cached_per_device(configured, dev, &done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    });
+    if (e != cudaSuccess) return e;
     // The split-K reduction makes blocks wait for one another: the grid must
     // never exceed the blocks that are resident at once.
-    static int resident_for = -1, resident_blocks = 0;
-    if (resident_for != dev) {
+    static std::atomic<int> resident[CACHE_DEVICES];
+    int resident_blocks = 0;
+    e = cached_per_device(resident, dev, &resident_blocks, [&](int *v) {
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, smem);
-        if (e != cudaSuccess) return e;
-        resident_blocks = per_sm * device_sm_count();
-        resident_for = dev;
-    }
+        const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, smem);
+        *v = per_sm * device_sm_count();
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     if (resident_blocks < 1) return cudaErrorLaunchOutOfResources;
     GemmArgs la = a;
     if (la.grid > resident_blocks) la.grid = resident_blocks;
