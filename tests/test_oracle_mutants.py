@@ -64,6 +64,17 @@ MUTANTS = {
                                 "for (int c = 0; c < D; ++c) t += S[(size_t)c * D + rr] * (double)qi[c];"),
     "delta_commit_skips_root": ("for (int a = -1; a < n_accept; ++a) {", "for (int a = 0; a < n_accept; ++a) {"),
     "commit_overwrites_root": ("memcpy(c + ((size_t)h * cap + L + 1 + d) * D,", "memcpy(c + ((size_t)h * cap + L + d) * D,"),
+    "commit_reads_parent_row": ("c + ((size_t)h * cap + L + path[d]) * D, sizeof", "c + ((size_t)h * cap + L + path[d] - 1) * D, sizeof"),
+    "attn_softmax_unnormalized": ("o[d] = num / den;", "o[d] = num;"),
+    "attn_values_from_keys": ("num += s[a] * or_half_to_double(v[((size_t)hk * cap + pos[a]) * D + d]);",
+                              "num += s[a] * or_half_to_double(k[((size_t)hk * cap + pos[a]) * D + d]);"),
+    "attn_query_of_kv_head": ("const uint16_t *qr = q + ((size_t)i * Hq + h) * D;",
+                              "const uint16_t *qr = q + ((size_t)i * Hq + hk) * D;"),
+    "delta_chain_applied_leaf_first": ("for (int a = n - 1; a >= 0; --a) {", "for (int a = 0; a < n; ++a) {"),
+    "delta_gate_scales_write": ("S[(size_t)r * D + c] = alpha * (S[(size_t)r * D + c] - beta * u[r] * (double)k[c]) +\n                                   beta * (double)v[r] * (double)k[c];",
+                                "S[(size_t)r * D + c] = alpha * (S[(size_t)r * D + c] - beta * u[r] * (double)k[c] +\n                                   beta * (double)v[r] * (double)k[c]);"),
+    "delta_commit_path_reversed": ("const int j = a < 0 ? 0 : path[a];", "const int j = a < 0 ? 0 : path[n_accept - 1 - a];"),
+    "delta_commit_skips_last": ("for (int a = -1; a < n_accept; ++a) {", "for (int a = -1; a + 1 < n_accept; ++a) {"),
 }
 
 
