@@ -54,7 +54,7 @@ extern "C" {
 typedef enum {
     HQ_OK = 0,
     HQ_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer   */
-    HQ_ERR_UNSUPPORTED = 2, /* valid request this build does not implement  */
+    HQ_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
     HQ_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
     HQ_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up            */
 } hq_status;

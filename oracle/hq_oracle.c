@@ -418,7 +418,7 @@ int or_verify_gemm(const int8_t *qx, const float *sx, int M, const void *codes, 
     return overflow ? 3 : 0;
 }
 
-/* Number of OpenMP threads this build uses (1 without OpenMP). */
+/* Number of OpenMP threads the oracle library uses (1 without OpenMP). */
 /* ------------------------------------------------------------------------ */
 /* Tree acceptance (section "Producing several tokens from one model pass"  */
 /* and "Verifying a draft tree without restoring model state": the main    */
