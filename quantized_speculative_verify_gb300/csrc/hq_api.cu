@@ -102,7 +102,15 @@ namespace {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool desc_ok(const hq_layer_desc *d) { return d && hq::desc_valid(d->K, d->N, d->group, d->format); }
+// A valid layer whose tile count fits the kernels' int tile indices (at most
+// 2^30 tiles of 128 channels x max(128, group) features: far beyond any
+// blob a GPU can hold).
+bool desc_ok(const hq_layer_desc *d) {
+    if (!d || !hq::desc_valid(d->K, d->N, d->group, d->format)) return false;
+    const long long kt = d->group > 128 ? d->group : 128;
+    const long long tiles = ((long long)d->N + hq::BN - 1) / hq::BN * (((long long)d->K + kt - 1) / kt);
+    return tiles <= (1LL << 30);
+}
 
 Geom geom_of(const hq_layer_desc *d) { return hq::make_geom(d->K, d->N, d->group, d->format); }
 

@@ -86,6 +86,19 @@ def test_invalid_desc_has_no_size(K, N, G, fmt):
     assert hq.hq_workspace_bytes(d, 16) == 0
 
 
+def test_tile_count_bound():
+    # the kernels index tiles with ints: at most 2^30 tiles (128 channels x 128 features each) per layer
+    at_bound = hq.hq_layer_desc(1 << 24, 1 << 20, 64, hq.HQ_W4_ASYM)  # 2^13 x 2^17 tiles
+    assert hq.hq_packed_bytes(at_bound) == (1 << 30) * (128 * 128 // 2 + 2 * 128 * 4 + 2 * 128 // 2)
+    beyond = hq.hq_layer_desc(1 << 24, (1 << 20) + 128, 64, hq.HQ_W4_ASYM)
+    assert hq.hq_packed_bytes(beyond) == 0 and hq.hq_workspace_bytes(beyond, 16) == 0
+    lib = hq.load()
+    fake = 0x10000  # never dereferenced: the descriptor is rejected first
+    assert lib.hq_verify_gemm(ctypes.byref(beyond), fake, fake, fake, 16, fake, None, fake, 0, None) == \
+        hq.HQ_ERR_INVALID_ARG
+    assert lib.hq_pack_weights(ctypes.byref(beyond), fake, fake, fake, None) == hq.HQ_ERR_INVALID_ARG
+
+
 def test_act_operand_bytes():
     assert hq.hq_act_operand_bytes(16, 4096) == 16 * 32 * 256
     assert hq.hq_act_operand_bytes(3, 96) == 3 * 1 * 256  # padded to a 128-feature block
