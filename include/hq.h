@@ -67,7 +67,9 @@ typedef enum {
 /* One linear layer.  K = input features (multiple of 32 and of `group`),
  * N = output features (>= 1), group = quantization group along K, one of
  * 16, 32, 64, 128, 256 (independent of the 32-element transform block),
- * format = hq_format. */
+ * format = hq_format.  The layer may have at most 2^30 weight tiles of 128
+ * output features x max(128, group) input features (a blob far larger than
+ * any GPU memory); a descriptor beyond that is invalid. */
 typedef struct {
     int32_t K;
     int32_t N;
