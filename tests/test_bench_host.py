@@ -150,3 +150,33 @@ def test_kernel_source_hash_follows_the_gemm_sources(tmp_path, monkeypatch):
     i = api.index("cudaError_t launch_verify_gemm(")
     (csrc / "hq_api.cu").write_text(api[:i] + api[i:].replace("MIN_TILES = 4", "MIN_TILES = 5", 1))
     assert bench.kernel_source_hash() != h0
+
+
+# ------------------------------------------------------ reference arm ---
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle) prints one JSON line on the
+    same metric, unit and workload as the GPU arm, with its own cpu_baseline
+    and an e2e entry that moves no bytes."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == bench.WORKLOAD
+    assert line["steps"] == 1 and line["warmup"] == 1 and line["value"] > 0
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"] and cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_do_no_work(capsys):
+    class OtherRank:
+        rank = 1
+
+    args = argparse.Namespace(steps=1, warmup=1, gpus=2)
+    assert bench.run_reference(args, OtherRank()) == 0
+    assert capsys.readouterr().out == ""
