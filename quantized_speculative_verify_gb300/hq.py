@@ -110,15 +110,21 @@ def _check(rc: int, what: str) -> None:
 
 
 def _ptr(t) -> int | None:
+    """A device-pointer argument: None, a raw address (int), or a CUDA tensor
+    (which must live on the current device: the library launches there; not
+    checked per pointer, to keep eager launches cheap).  Host tensors and numpy
+    arrays are refused: the kernels read and write device memory, and on a
+    system whose GPU can reach host memory a host buffer would not fault but
+    run silently on host memory."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if isinstance(t, torch.Tensor):
+        if not t.is_cuda:
+            raise TypeError("device memory expected, got a CPU tensor (move it to the GPU first)")
         return t.data_ptr()
-    if isinstance(t, np.ndarray):
-        return t.ctypes.data
-    raise TypeError(f"cannot pass {type(t)} as a pointer")
+    raise TypeError(f"device memory expected, cannot pass {type(t).__name__} as a device pointer")
 
 
 def _stream(stream) -> int | None:

@@ -231,3 +231,19 @@ def test_delta_arguments_are_checked_before_launch():
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 4, D, 0, None) == E
     assert c(FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, D, 0, None) == E
     assert c(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 256, 0, None) == U
+
+
+def test_binding_refuses_host_buffers_as_device_pointers():
+    # the kernels read and write device memory; a host buffer is refused
+    # before the library is called (no GPU needed to see it)
+    import torch
+    d = hq.make_desc(256, 256, 32, "w4")
+    with pytest.raises(TypeError, match="CPU tensor"):
+        hq.hq_rotate_quant_act(torch.zeros((1, 256)), 1, 256, None, None, None, None)
+    with pytest.raises(TypeError, match="ndarray"):
+        hq.hq_verify_gemm(d, np.zeros(16, dtype=np.uint8), None, None, 1, None, None, None)
+    with pytest.raises(TypeError, match="CPU tensor"):
+        hq.tree_attention(torch.zeros((1, 8, hq.HQ_ATTN_HEAD_DIM), dtype=torch.float16),
+                          torch.zeros((1, 4, hq.HQ_ATTN_HEAD_DIM), dtype=torch.float16),
+                          torch.zeros((1, 4, hq.HQ_ATTN_HEAD_DIM), dtype=torch.float16), 3,
+                          torch.zeros(1, dtype=torch.int32), 0.1)
