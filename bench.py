@@ -305,33 +305,41 @@ class VerifyPass:
     """All packed weights, inputs and outputs of one decoder verify pass, resident on the device.
 
     Each activation input (a layer's attention input, read by q, k and v; the
-    o input; the MLP input, read by the fused gate+up; the down input; the LM
-    head input) has its own sign vector, X, and quantized buffers; the
-    layers that read an input are packed with that input's signs."""
+    o input; the MLP input, read by gate and up; the down input; the LM head
+    input) has its own sign vector, X, and quantized buffers; the layers that
+    read an input are packed with that input's signs.  Layers that read the
+    same input run as one GEMM over their weight matrices packed into one blob
+    (hq_pack_weights_at): gate and up always, q, k and v unless
+    --no-fuse-qkv."""
 
     def __init__(self, torch, hq, synth, device, fuse_qkv: bool, pdl: bool):
         cfg = synth.DECODER_9B
-        self.torch, self.hq = torch, hq
+        self.torch, self.hq, self.synth = torch, hq, synth
+        self.cfg = cfg
         self.M, self.G, self.fmt = cfg["M"], cfg["G"], cfg["fmt"]
         self.flags = hq.HQ_LAUNCH_PDL if pdl else hq.HQ_LAUNCH_DEFAULT
-        self.linears = synth.decoder_linears(cfg, fuse_qkv=fuse_qkv)
-        self.layers, self.ys, self.inputs, self.plan = [], [], [], []
+        self.gemms = synth.decoder_gemms(cfg, fuse_qkv=fuse_qkv)
+        self.linears = [(name, K, sum(n for _, n, _ in parts)) for name, K, parts in self.gemms]
+        self.layers, self.fused, self.ys, self.inputs, self.plan = [], [], [], [], []
         seed = cfg["seed"]
         ws_need = 0
         s_host = None
-        for li, (name, K, N) in enumerate(self.linears):
+        for li, (name, K, parts) in enumerate(self.gemms):
             if not name.endswith((".k", ".v")):  # a new activation input
                 s_host = hq.hq_make_signs(synth.layer_seed(seed, 500 + li), K)
                 X = synth.activations(self.M, K, seed=synth.layer_seed(seed, 2000 + li), device=device, **cfg["x"])
-                _, qop, sx = hq.act_buffers(self.M, K, device, int8_codes=False)
-                self.inputs.append([name, K, X, qop, sx, None])
-            W = synth.weights(N, K, seed=synth.layer_seed(seed, li), device=device, **cfg["w"])
-            layer = hq.pack_layer(W, self.G, self.fmt, s_host)
-            del W
+                _, _, qop, sx = hq.act_buffers(self.M, K, self.G, device, int8_codes=False)
+                self.inputs.append([name, K, X, qop, sx, None, s_host])
+            Ws = [synth.weights(n, K, seed=synth.layer_seed(seed, wi), device=device, **cfg["w"])
+                  for _, n, wi in parts]
+            fused = hq.pack_fused(Ws, self.G, self.fmt, s_host)
+            del Ws
+            layer = fused.layer
             if self.inputs[-1][5] is None:
                 self.inputs[-1][5] = layer.signs
             self.layers.append(layer)
-            self.ys.append(torch.empty((self.M, N), dtype=torch.float32, device=device))
+            self.fused.append(fused)
+            self.ys.append(torch.empty((self.M, layer.N), dtype=torch.float32, device=device))
             self.plan.append((len(self.inputs) - 1, li))
             ws_need = max(ws_need, hq.hq_workspace_bytes(layer.desc, self.M))
         self.ws = torch.zeros(ws_need, dtype=torch.uint8, device=device)
@@ -362,13 +370,19 @@ class VerifyPass:
         self.accept_ws = torch.empty(hq.hq_tree_accept_workspace_bytes(self.M, V), dtype=torch.uint8, device=device)
         self.n_accept_kernels = 2
 
+    def part_weights(self, li: int, device):
+        """The fp32 weight matrices of GEMM li's parts, regenerated from their seeds (for checking)."""
+        name, K, parts = self.gemms[li]
+        return [self.synth.weights(n, K, seed=self.synth.layer_seed(self.cfg["seed"], wi), device=device,
+                                   **self.cfg["w"]) for _, n, wi in parts]
+
     def launch(self, act=True, gemm=True):
         hq = self.hq
         done = set()
         for ii, li in self.plan:
-            name, K, X, qop, sx, signs = self.inputs[ii]
+            name, K, X, qop, sx, signs, _ = self.inputs[ii]
             if act and ii not in done:
-                hq.hq_rotate_quant_act(X, self.M, K, signs, None, qop, sx, self.flags)
+                hq.hq_rotate_quant_act(X, self.M, K, self.G, signs, None, None, qop, sx, self.flags)
                 done.add(ii)
             if gemm:
                 layer = self.layers[li]
@@ -582,8 +596,8 @@ def measure_sweep(torch, hq, synth, device, stream, args, peak):
     layer's hot path).  Four copies of the packed layer (153 / 276 MB, larger
     than L2) are cycled so every call streams its weights from HBM.  Per M:
     microseconds per call, weight GB/s, integer tera-ops/s (2*M*N*K) and the
-    verify cost ratio t(M) / t(1).  Batches of more than 32 rows run as
-    consecutive 32-row launches that stream the weights again."""
+    verify cost ratio t(M) / t(1).  Every M runs as one GEMM launch (the
+    rows are the tensor-core MMA's N: 16, 32, 64 or 128)."""
     out = {}
     K = N = 8192
     copies = 4
@@ -598,7 +612,7 @@ def measure_sweep(torch, hq, synth, device, stream, args, peak):
         t1 = None
         for M in c["Ms"]:
             X = synth.activations(M, K, seed=c["seed"] + M, device=device)
-            bufs = hq.act_buffers(M, K, device, int8_codes=False)
+            bufs = hq.act_buffers(M, K, c["G"], device, int8_codes=False)
             Y = torch.empty((M, N), dtype=torch.float32, device=device)
             ws = hq.workspace(layers[0].desc, M, device)
             for i in range(copies * 2):
@@ -647,7 +661,7 @@ def measure_layers(torch, hq, synth, device, stream, peak):
         rows = []
         for M in c["Ms"]:
             X = synth.activations(M, K, seed=c["seed"] + 1, device=device, **c["x"])
-            bufs = hq.act_buffers(M, K, device, int8_codes=False)
+            bufs = hq.act_buffers(M, K, c["G"], device, int8_codes=False)
             Y = torch.empty((M, N), dtype=torch.float32, device=device)
             ws = hq.workspace(first.desc, M, device)
             for i in range(2 * copies):
@@ -872,8 +886,8 @@ def run_one_gemm(args) -> int:
     layer = hq.pack_layer(W, G, fmt, hq.hq_make_signs(3, K))
     del W
     X = synth.activations(M, K, seed=2, device=dev)
-    _, qop, sx = hq.act_buffers(M, K, dev, int8_codes=False)
-    hq.hq_rotate_quant_act(X, M, K, layer.signs, None, qop, sx)
+    _, _, qop, sx = hq.act_buffers(M, K, G, dev, int8_codes=False)
+    hq.hq_rotate_quant_act(X, M, K, G, layer.signs, None, None, qop, sx)
     ws = hq.workspace(layer.desc, M, dev)
     Y = torch.empty((M, N), dtype=torch.float32, device=dev)
     for _ in range(max(args.warmup, 1)):

@@ -64,12 +64,12 @@ typedef enum {
     HQ_W8_SYM = 1   /* "Large":  int8 codes, fp32 scale per group                     */
 } hq_format;
 
-/* One linear layer.  K = input features (multiple of 32 and of `group`),
- * N = output features (>= 1), group = quantization group along K, one of
- * 16, 32, 64, 128, 256 (independent of the 32-element transform block),
- * format = hq_format.  The layer may have at most 2^30 weight tiles of 128
- * output features x max(128, group) input features (a blob far larger than
- * any GPU memory); a descriptor beyond that is invalid. */
+/* One linear layer.  K = input features (multiple of 32 and of `group`, at
+ * most 65536), N = output features (>= 1), group = quantization group along
+ * K, one of 16, 32, 64, 128, 256 (independent of the 32-element transform
+ * block), format = hq_format.  The layer may have at most 2^30 weight tiles
+ * of 128 output features x max(128, group) input features (a blob far larger
+ * than any GPU memory); a descriptor beyond that is invalid. */
 typedef struct {
     int32_t K;
     int32_t N;
@@ -94,6 +94,13 @@ typedef struct {
  * partial sums are added into Y atomically as each block finishes, and the
  * last bits of such outputs may differ between runs. */
 #define HQ_LAUNCH_DETERMINISTIC 2u
+/* hq_verify_gemm only: no output's K range is split between thread blocks:
+ * each thread block takes whole blocks of 128 output channels, so every
+ * output is summed over its groups in ascending order by one thread block and
+ * is bit-identical to the sequential fp32 sum of the definition (see
+ * hq_verify_gemm).  Slower on layers with few 128-channel blocks (fewer thread
+ * blocks than SMs); implies HQ_LAUNCH_DETERMINISTIC. */
+#define HQ_LAUNCH_EXACT_ORDER 4u
 
 /* Maximum number of token rows per call. */
 #define HQ_MAX_M 128
@@ -111,14 +118,14 @@ size_t hq_packed_bytes(const hq_layer_desc *desc);
 
 /* Size in bytes of the workspace hq_verify_gemm needs for `desc` and M rows
  * (0 if the arguments are invalid).  The workspace holds the device error
- * word, the split-K partial sums (sized for at most 32 rows: larger batches
- * run as consecutive 32-row launches; 16 MiB) and two counters per 128
- * output channels, at offsets that depend on neither the layer nor M: one
- * workspace of the largest size serves calls of every layer and M in turn
- * (calls that may overlap on the GPU need workspaces of their own).  It must
- * be zero-filled once after allocation; every call leaves the error word and
- * the counters at zero again (except after a time-out, see
- * hq_workspace_status); the partial sums need no clearing. */
+ * word, the split-K partial sums (two slots of 128 channels x 128 rows per
+ * thread block: 20 MiB) and two counters per 128 output channels, at offsets
+ * that depend on neither the layer nor M: one workspace of the largest size
+ * serves calls of every layer and M in turn (calls that may overlap on the
+ * GPU need workspaces of their own).  It must be zero-filled once after
+ * allocation; every call leaves the error word and the counters at zero
+ * again (except after a time-out, see hq_workspace_status); the partial sums
+ * need no clearing. */
 size_t hq_workspace_bytes(const hq_layer_desc *desc, int32_t M);
 
 /* Sign vector of the randomized Hadamard transform ("random sign flips
@@ -144,9 +151,24 @@ int hq_make_signs(uint64_t seed, int32_t K, uint32_t *signs_host);
 int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *signs, void *blob,
                     void *stream);
 
-/* Size in bytes of the GEMM's activation operand for M rows and K features
- * (0 if the arguments are invalid): M * ceil(K/128) * 256. */
-size_t hq_act_operand_bytes(int32_t M, int32_t K);
+/* Offline, fused layers: pack `rows` rows of weights (fp32 [rows][K]) as the
+ * output channels n0 .. n0 + rows - 1 of the layer `desc`, writing only the
+ * blob's tiles of those channels.  Layers that read the same activations
+ * (the q, k and v projections, or the gate and up projections) are packed
+ * part by part into one blob of N = the sum of their widths and run as one
+ * hq_verify_gemm; Y's columns n0 .. n0 + rows - 1 are that part's outputs,
+ * identical to what the part alone would give (per output, the same
+ * arithmetic).  n0 must be a multiple of 128, and the rows of the last part
+ * may end anywhere before N; channels of the blob that no call packs are
+ * left as they were.  Signs, formats and errors as in hq_pack_weights. */
+int hq_pack_weights_at(const hq_layer_desc *desc, int32_t n0, int32_t rows, const float *W, const uint32_t *signs,
+                       void *blob, void *stream);
+
+/* Size in bytes of the GEMM's activation operand for M rows, K features and
+ * quantization group `group` (0 if the arguments are invalid or M = 0).  The
+ * operand is an opaque buffer written by hq_rotate_quant_act and read by
+ * hq_verify_gemm; its layout is private to this version of the library. */
+size_t hq_act_operand_bytes(int32_t M, int32_t K, int32_t group);
 
 /* Verify pass, step 1: rotate and quantize the activations of M rows
  * (section "How Uzu optimizes bytes and tokens per pass": activations
@@ -154,27 +176,30 @@ size_t hq_act_operand_bytes(int32_t M, int32_t K);
  * transform as the weights).
  *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op),
  *         K a positive multiple of 32, at most 65536
+ *   group quantization group of the layers that read these activations
+ *         (16, 32, 64, 128 or 256, dividing K)
  *   signs uint32 [K/32]
  *   qx    int8 [M][K] (4-byte aligned) or NULL: clamp(rint(x' / sx), -127, 127)
- *   qop   the GEMM's activation operand (hq_act_operand_bytes(M, K) bytes,
- *         16-byte aligned) or NULL: the same codes as IEEE fp16 in blocks of
- *         128 features, [ceil(K/128)][M][128]; within a row of 128 codes the
- *         16-byte chunk c of an odd row m is stored at chunk c ^ 4; codes past
- *         K are zero
+ *   gsum  int32 [M][K/group] (4-byte aligned) or NULL: the sum of the codes
+ *         qx over each group (the correction term of the Medium format:
+ *         sum qx (q - z) = sum qx q - z * gsum)
+ *   qop   the GEMM's activation operand (hq_act_operand_bytes(M, K, group)
+ *         bytes, 16-byte aligned, opaque) or NULL
  *   sx    fp32 [M]:  max_k |x'[m][k]| / 127  (0 for an all-zero row)
- * At least one of qx, qop must be given.  x' is the rotated row: per
+ * At least one of qx, gsum, qop must be given.  x' is the rotated row: per
  * 32-block, sign flip, unnormalized Walsh-Hadamard butterfly at strides 1, 2,
  * 4, 8, 16 in fp32 without fused multiply-add, then multiplication by
  * fp32(1/sqrt(32)).  flags: HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL. */
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *signs, int8_t *qx, void *qop,
-                        float *sx, uint32_t flags, void *stream);
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+                        int32_t *gsum, void *qop, float *sx, uint32_t flags, void *stream);
 
 /* Verify pass, step 2: integer GEMM of the quantized activations against the
  * packed weights with the per-group dequantization epilogue (section "How
  * Uzu optimizes bytes and tokens per pass": both matmul operands integers).
  *   blob      packed by hq_pack_weights for the same desc (16-byte aligned)
- *   qop, sx   from hq_rotate_quant_act with the same M, K and signs
- *   M         0..HQ_MAX_M (0: no-op)
+ *   qop, sx   from hq_rotate_quant_act with the same M, K, group (= desc's)
+ *             and signs
+ *   M         0..HQ_MAX_M (0: no-op); one launch for every M
  *   Y         fp32 [M][N]:
  *               Y[m][n] = sx[m] * sum_g ( scale[n][g] * P[m][n][g] )
  *             with P[m][n][g] = sum_{k in g} qx[m][k] * (code[n][k] - zero[n][g])
@@ -183,8 +208,9 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *si
  *             exactly (slower; for verification)
  *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
  *             before its first use
- * The integer sums P are exact (the codes are multiplied on fp16 tensor cores
- * with fp32 accumulation, which is exact for these ranges).  The fp32 sum
+ * The integer sums P are exact: the codes are multiplied on the fp16 tensor
+ * cores (tcgen05) with fp32 accumulation, exact for these ranges, and the
+ * Medium zero point enters through the group sums.  The fp32 sum
  * over groups is taken in ascending group order.  An output whose K range is
  * split across thread blocks is the sum of the blocks' partial sums: by
  * default each block adds sx[m] * (its partial sum) into Y with an fp32
@@ -197,7 +223,8 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *si
  * running concurrently on another stream that holds SMs for longer than the
  * bound makes the call time out (HQ_ERR_TIMEOUT from hq_workspace_status;
  * zero the workspace again before reusing it after a time-out).  flags: any
- * of HQ_LAUNCH_PDL, HQ_LAUNCH_DETERMINISTIC (see above); with HQ_LAUNCH_PDL,
+ * of HQ_LAUNCH_PDL, HQ_LAUNCH_DETERMINISTIC, HQ_LAUNCH_EXACT_ORDER (see
+ * above); with HQ_LAUNCH_PDL,
  * Y is written only after the wait for the previous kernel. */
 int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream);
@@ -224,22 +251,35 @@ int hq_workspace_status(void *workspace, void *stream);
  * synchronize the device.  The pages have no counterpart of this call.
  *
  * The scratch lives in one file-scope device array of
- * HQ_NOALLOC_SCRATCH_BYTES (16 MiB + 128 KiB) that every GPU which loads the
+ * HQ_NOALLOC_SCRATCH_BYTES (20 MiB + 128 KiB) that every GPU which loads the
  * library holds until the process exits.  A call is accepted when
  * hq_workspace_bytes(desc, M) fits in it (any M, for N up to about two
  * million outputs); larger calls return HQ_ERR_UNSUPPORTED and launch
  * nothing.  The call allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Each call clears the
- * array's control words (error word and arrival counters) on `stream`
- * before the kernel.  All calls on a device share the one array, so calls
- * that may overlap on the GPU (different streams, or graphs replayed
- * concurrently) race and must be serialized by the caller.  Arguments,
- * outputs and flags are those of hq_verify_gemm. */
-#define HQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 128u * 1024u)
+ * array's device address (cudaGetSymbolAddress) with that device current
+ * and zero-fills the array once (a synchronous cudaMemset); make that first
+ * call before any stream capture.  Later calls only launch the GEMM: the
+ * kernels leave the array's error word and counters at zero after every
+ * call whose waits all succeed.  A bounded wait that gives up (see
+ * hq_verify_gemm) leaves the outputs of that call incomplete and records
+ * the time-out in the array; hq_noalloc_status reports it and cleans the
+ * array up.  All calls on a device share the one array, so calls that may
+ * overlap on the GPU (different streams, or graphs replayed concurrently)
+ * race and must be serialized by the caller.  Arguments, outputs and flags
+ * are those of hq_verify_gemm; HQ_LAUNCH_PDL works as there (nothing runs
+ * between the previous kernel and the GEMM). */
+#define HQ_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u + 128u * 1024u)
 int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
                            int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream);
+
+/* Status of the allocation-free calls on the current device: synchronizes
+ * `stream`, then returns HQ_ERR_TIMEOUT if a bounded wait inside an
+ * hq_verify_gemm_noalloc call gave up since the last status call (the
+ * outputs of that call are incomplete; the array's error word and counters
+ * are reset to zero before returning), HQ_OK otherwise (also when no such
+ * call has run on the device).  Allocates nothing. */
+int hq_noalloc_status(void *stream);
 
 /* Draft-tree acceptance, after the verify pass (sections "Producing several
  * tokens from one model pass": the main model checks the drafted positions
@@ -356,6 +396,17 @@ int hq_delta_commit(float *state, const float *k, const float *v, const float *a
  * `workspace` (>= 16 bytes, zero-filled).  hq_workspace_status then
  * returns HQ_ERR_TIMEOUT.  No fault and no hang: the kernel returns. */
 int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream);
+
+/* Self-test of the GEMM's bounded waits between thread blocks: runs
+ * hq_verify_gemm (arguments as there, HQ_LAUNCH_DETERMINISTIC) with every
+ * wait for the other contributors of a split output asking for one arrival
+ * more than there are and giving up after `limit_ns` nanoseconds
+ * (1000..100000000).  On a layer with split outputs (K of several 128-feature
+ * tiles and more tiles than SMs) the waits run out: hq_workspace_status then
+ * returns HQ_ERR_TIMEOUT; Y is unspecified.  No fault and no hang: the kernel
+ * returns.  Zero the workspace before reusing it. */
+int hq_selftest_gemm_wait_timeout(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
+                                  int32_t M, float *Y, void *workspace, int64_t limit_ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -44,7 +44,11 @@ cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream
 }
 
 cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
-                               int32_t *partials, void *workspace, bool pdl, bool det, cudaStream_t s) {
+                               int32_t *partials, void *workspace, uint32_t flags, cudaStream_t s, int wait_extra,
+                               long long wait_ns) {
+    const bool pdl = (flags & HQ_LAUNCH_PDL) != 0;
+    const bool exact = (flags & HQ_LAUNCH_EXACT_ORDER) != 0;
+    const bool det = exact || (flags & HQ_LAUNCH_DETERMINISTIC) != 0;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
     GemmArgs a;
@@ -55,43 +59,58 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.partials = partials;
     a.ws = static_cast<uint8_t *>(workspace);
     a.det = det ? 1 : 0;
-    a.M_total = M;
+    a.nb_align = exact ? 1 : 0;
+    a.wait_extra = wait_extra;
+    a.wait_ns = wait_ns > 0 ? wait_ns : (long long)WAIT_LIMIT_NS;
+    a.M = M;
     a.N = g.N;
     a.K = g.K;
+    a.G = g.G;
+    a.KT = g.KT;
+    a.GPT = g.GPT;
     a.NGK = g.NGK;
     a.NB = g.NB;
     a.KTILES = g.KTILES;
     a.T = g.NB * g.KTILES;
-    // Three thread blocks per SM (twelve consumer warps) keep enough loads and
-    // tensor-core steps in flight; each block's stage ring is about 60 KB.
+    // One thread block per SM (each owns all of its SM's tensor memory).
     // Small layers get fewer blocks so that every block streams at least
-    // MIN_TILES tiles and an n-block is split between few blocks (the last
-    // one to finish sums the others' partial sums).
+    // MIN_TILES tiles and an n-block is split between few blocks.
     constexpr int MIN_TILES = 4;
-    int grid = 3 * sms;
-    if (grid > a.T / MIN_TILES) grid = a.T / MIN_TILES;
+    int grid = sms;
+    if (exact) {
+        // whole n-blocks per block: every output is summed by one block
+        if (grid > g.NB) grid = g.NB;
+    } else if (grid > a.T / MIN_TILES) {
+        grid = a.T / MIN_TILES;
+    }
     if (grid < 1) grid = 1;
     if (grid > MAX_CTAS) grid = MAX_CTAS;
     a.grid = grid;
     a.tile_bytes = g.tile_bytes;
     a.code_bytes = g.code_bytes;
     a.scale_bytes = g.scale_bytes;
-    // Batches of more than MAX_M_LAUNCH rows run as consecutive launches over
-    // row slices; each streams the weights again and reuses the workspace.
-    for (int m0 = 0; m0 < M; m0 += MAX_M_LAUNCH) {
-        a.m0 = m0;
-        a.M = M - m0 < MAX_M_LAUNCH ? M - m0 : MAX_M_LAUNCH;
-        const int mrows = a.M <= 8 ? 8 : a.M <= 16 ? 16 : 32;  // staged activation rows (zero past M)
-        a.act_bytes = mrows * ACT_BLOCK * 2 * (g.KT / ACT_BLOCK);
-        int stages = (60 * 1024) / (g.tile_bytes + a.act_bytes);
-        if (stages < 2) stages = 2;
-        if (stages > 16) stages = 16;
-        a.stages = stages;
-        const cudaError_t e =
-            g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, g.G, pdl, s) : launch_gemm_w8(a, g.G, pdl, s);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    const int MT = act_rows(M);
+    a.act_off = (g.tile_bytes + 127) / 128 * 128;
+    a.act_bytes = (g.KT / ACT_BLOCK) * MT * ACT_BLOCK * 2;
+    a.s_bytes = g.GPT * MT * 4;
+    a.stage_bytes = (a.act_off + a.act_bytes + a.s_bytes + 127) / 128 * 128;
+    a.op_s_offset = (long long)act_code_bytes(M, g.K);
+    // Stage ring: as many stages as fit in ~200 KB of shared memory.
+    int stages = (200 * 1024) / a.stage_bytes;
+    if (stages > MAX_STAGES) stages = MAX_STAGES;
+    if (stages < 2) stages = 2;
+    a.stages = stages;
+    // Tensor memory (512 columns): accumulator slots of MT columns (up to 16,
+    // at least 2) and A buffers of KT/2 columns (up to 4) in what is left.
+    int nd = 256 / MT;
+    if (nd > MAX_ND) nd = MAX_ND;
+    if (nd < 2) nd = 2;
+    int na = (TMEM_COLS - nd * MT) / (g.KT / 2);
+    if (na > MAX_NA) na = MAX_NA;
+    a.na = na;
+    a.nd = nd;
+    if (na < 2 || 2048 + (size_t)stages * a.stage_bytes > (size_t)GEMM_SMEM_LIMIT) return cudaErrorInvalidConfiguration;
+    return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, pdl, s) : launch_gemm_w8(a, pdl, s);
 }
 
 }  // namespace hq
@@ -102,15 +121,12 @@ namespace {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// A valid layer whose tile count fits the kernels' int tile indices (at most
-// 2^30 tiles of 128 channels x max(128, group) features: far beyond any
-// blob a GPU can hold).
-bool desc_ok(const hq_layer_desc *d) {
-    if (!d || !hq::desc_valid(d->K, d->N, d->group, d->format)) return false;
-    const long long kt = d->group > 128 ? d->group : 128;
-    const long long tiles = ((long long)d->N + hq::BN - 1) / hq::BN * (((long long)d->K + kt - 1) / kt);
-    return tiles <= (1LL << 30);
+// A quantization group the operand can be laid out for: 16..256, dividing K.
+bool group_ok(int32_t K, int32_t G) {
+    return (G == 16 || G == 32 || G == 64 || G == 128 || G == 256) && K > 0 && K % G == 0;
 }
+
+using hq::desc_ok;
 
 Geom geom_of(const hq_layer_desc *d) { return hq::make_geom(d->K, d->N, d->group, d->format); }
 
@@ -141,7 +157,7 @@ const char *hq_status_string(int status) {
     }
 }
 
-int32_t hq_version(void) { return (1 << 16) | 2; }  // 1.2: HQ_LAUNCH_DETERMINISTIC; split outputs accumulated by default
+int32_t hq_version(void) { return (2 << 16) | 0; }  // 2.0: tensor-memory GEMM, one launch up to 128 rows; opaque activation operand with group sums
 
 size_t hq_packed_bytes(const hq_layer_desc *desc) {
     if (!desc_ok(desc)) return 0;
@@ -169,26 +185,36 @@ int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *s
     if (!desc_ok(desc) || !W || !signs || !blob) return HQ_ERR_INVALID_ARG;
     if (!aligned(W, 4) || !aligned(signs, 4) || !aligned(blob, 16)) return HQ_ERR_INVALID_ARG;
     const Geom g = geom_of(desc);
-    return cuda_status(hq::launch_pack(g, W, signs, blob, static_cast<cudaStream_t>(stream)));
+    return cuda_status(hq::launch_pack(g, W, g.N, 0, signs, blob, static_cast<cudaStream_t>(stream)));
 }
 
-size_t hq_act_operand_bytes(int32_t M, int32_t K) {
-    if (M < 0 || M > HQ_MAX_M || K <= 0 || K % 32 != 0) return 0;
-    return hq::act_operand_bytes(M, K);
+int hq_pack_weights_at(const hq_layer_desc *desc, int32_t n0, int32_t rows, const float *W, const uint32_t *signs,
+                       void *blob, void *stream) {
+    if (!desc_ok(desc) || !W || !signs || !blob) return HQ_ERR_INVALID_ARG;
+    if (n0 < 0 || n0 % hq::BN != 0 || rows <= 0 || (long long)n0 + rows > desc->N) return HQ_ERR_INVALID_ARG;
+    if (!aligned(W, 4) || !aligned(signs, 4) || !aligned(blob, 16)) return HQ_ERR_INVALID_ARG;
+    const Geom g = geom_of(desc);
+    return cuda_status(hq::launch_pack(g, W, rows, n0 / hq::BN, signs, blob, static_cast<cudaStream_t>(stream)));
 }
 
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, const uint32_t *signs, int8_t *qx, void *qop,
-                        float *sx, uint32_t flags, void *stream) {
+size_t hq_act_operand_bytes(int32_t M, int32_t K, int32_t group) {
+    if (M < 0 || M > HQ_MAX_M || K <= 0 || K % 32 != 0 || K > hq::MAX_K || !group_ok(K, group)) return 0;
+    if (M == 0) return 0;
+    return hq::act_operand_bytes(M, K, group);
+}
+
+int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+                        int32_t *gsum, void *qop, float *sx, uint32_t flags, void *stream) {
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if (K <= 0 || K % 32 != 0) return HQ_ERR_INVALID_ARG;
+    if (K <= 0 || K % 32 != 0 || !group_ok(K, group)) return HQ_ERR_INVALID_ARG;
     if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
-    if (!X || !signs || !sx || (!qx && !qop)) return HQ_ERR_INVALID_ARG;
+    if (!X || !signs || !sx || (!qx && !qop && !gsum)) return HQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(sx, 4) || !aligned(signs, 4) || (qx && !aligned(qx, 4)) ||
-        (qop && !aligned(qop, 16)))
+        (gsum && !aligned(gsum, 4)) || (qop && !aligned(qop, 16)))
         return HQ_ERR_INVALID_ARG;
-    if (K > 65536) return HQ_ERR_UNSUPPORTED;
-    return cuda_status(hq::launch_rotate_quant_act(X, M, K, signs, qx, static_cast<uint8_t *>(qop), sx,
+    if (K > hq::MAX_K) return HQ_ERR_UNSUPPORTED;
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, group, signs, qx, gsum, static_cast<uint8_t *>(qop), sx,
                                                    (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
 }
 
@@ -196,7 +222,7 @@ int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream) {
     if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if ((flags & ~(HQ_LAUNCH_PDL | HQ_LAUNCH_DETERMINISTIC)) != 0) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~(HQ_LAUNCH_PDL | HQ_LAUNCH_DETERMINISTIC | HQ_LAUNCH_EXACT_ORDER)) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
     if (!blob || !qop || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
     if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
@@ -204,8 +230,7 @@ int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop,
         return HQ_ERR_INVALID_ARG;
     const Geom g = geom_of(desc);
     return cuda_status(hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, partials, workspace,
-                                              (flags & HQ_LAUNCH_PDL) != 0, (flags & HQ_LAUNCH_DETERMINISTIC) != 0,
-                                              static_cast<cudaStream_t>(stream)));
+                                              flags, static_cast<cudaStream_t>(stream)));
 }
 
 int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
@@ -228,6 +253,21 @@ int hq_workspace_status(void *workspace, void *stream) {
     const int zero = 0;
     if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return HQ_ERR_CUDA;
     return HQ_ERR_TIMEOUT;
+}
+
+int hq_selftest_gemm_wait_timeout(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
+                                  int32_t M, float *Y, void *workspace, int64_t limit_ns, void *stream) {
+    if (!desc_ok(desc) || M <= 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
+    if (limit_ns < 1000 || limit_ns > 100000000) return HQ_ERR_INVALID_ARG;
+    if (!blob || !qop || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(qop, 16) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16))
+        return HQ_ERR_INVALID_ARG;
+    const Geom g = geom_of(desc);
+    // the deterministic mode waits for one arrival more than there are
+    // contributors: every wait between thread blocks runs out after limit_ns
+    return cuda_status(hq::launch_verify_gemm(g, blob, static_cast<const uint8_t *>(qop), sx, M, Y, nullptr, workspace,
+                                              HQ_LAUNCH_DETERMINISTIC, static_cast<cudaStream_t>(stream), 1,
+                                              (long long)limit_ns));
 }
 
 int hq_selftest_wait_timeout(void *workspace, int64_t limit_ns, void *stream) {

@@ -16,29 +16,28 @@ namespace hq {
 // The weights of a layer are cut into tiles of BN = 128 output channels by
 // KT input features (KT = max(128, group)).  Tiles are stored n-block major,
 // K minor, so the tiles one thread block streams are one contiguous byte
-// range and one bulk copy fetches a whole tile.  Inside a tile:
+// range and one bulk copy fetches a whole tile.  Inside a tile, with
+// channel n = 0..127 and 64-feature chunk c = 0..KT/64-1:
 //
-//   codes   [chunk][ntile 0..7][lane 0..31][16 bytes]
-//           ntile = 16 consecutive channels.  A lane (g = lane/4, t = lane%4)
-//           of the consumer warp that owns the ntile holds, for every 32
-//           features f0.., channels g and g+8 at features f0 + 8t .. f0 + 8t + 7:
-//           the operands of two mma.m16n8k16 steps.  A chunk covers 64
-//           features in the 4-bit format (four 32-bit words, one per 16-feature
-//           step, nibble layout in widen_w4 of k_gemm.cuh) and 32 features in
-//           the 8-bit format (four words: channel g features +0..3, channel
-//           g+8 +0..3, channel g +4..7, channel g+8 +4..7).
-//   scales  [group in tile][ntile][16 floats, rows ordered 0,8,1,9,...,7,15]
-//   zeros   [group in tile][ntile][8 bytes, byte r = z[r] | z[r+8] << 4]
-//           (4-bit format only)
+//   codes   4-bit: [c][quarter p 0..1][n][16 bytes]: the 32 features
+//           64c + 32p .. +31 of channel n as four 32-bit words of eight
+//           nibbles; nibble i of word j is feature 8j + 2 (i & 3) + (i >> 2)
+//           (so that the GEMM widens a word into the fp16 pairs (0,1) (2,3)
+//           (4,5) (6,7) with one mask each).
+//           8-bit: [c][quarter p 0..3][n][16 bytes]: features 64c + 16p + e,
+//           e = 0..15, in order.
+//           A GEMM thread owns one channel: it reads 16 contiguous bytes per
+//           quarter and the 32 lanes of a warp read 512 contiguous bytes.
+//   scales  [n][group in tile] fp32
+//   zeros   4-bit only: nibble n * GPT + g (low nibble first), uint4
 //
 // Every region and every tile is a multiple of 16 bytes, and the byte count
 // of a tile equals its algorithmic size: BN*KT*(bits/8) for the codes plus
 // 4 bytes (and half a byte for the zero point) per (channel, group).
 // N and K are padded up to whole tiles with zero codes and zero scales.
 // ---------------------------------------------------------------------------
-constexpr int BN = 128;           // output channels per tile (8 mma row tiles)
-constexpr int NTILES = BN / 16;   // mma row tiles per tile
-constexpr int MAX_CTAS = 512;     // upper bound on GEMM thread blocks (workspace sizing)
+constexpr int BN = 128;           // output channels per tile (= TMEM lanes)
+constexpr int MAX_CTAS = 160;     // upper bound on GEMM thread blocks (one per SM; workspace sizing)
 constexpr int MAX_M = HQ_MAX_M;
 
 struct Geom {
@@ -53,7 +52,6 @@ struct Geom {
     int scale_bytes; // per tile
     int zero_bytes;  // per tile
     int tile_bytes;
-    int chunk_k;     // features covered by one 16-byte lane chunk: 64 (4-bit) or 32 (8-bit)
 };
 
 __host__ __device__ inline bool desc_valid(int K, int N, int G, int fmt) {
@@ -63,6 +61,23 @@ __host__ __device__ inline bool desc_valid(int K, int N, int G, int fmt) {
     if (K % G != 0) return false;
     if (fmt != HQ_W4_ASYM && fmt != HQ_W8_SYM) return false;
     return true;
+}
+
+// Largest K a layer may have: the activation operand's limit (a row of X is
+// rotated and quantized by one thread block), and far below the int range of
+// the tile arithmetic (K + KT - 1 stays positive).
+constexpr int MAX_K = 65536;
+
+// A valid layer whose tile count fits the kernels' int tile indices (at most
+// 2^30 tiles of 128 channels x max(128, group) features) and whose K is at
+// most MAX_K.  Every entry point that takes a layer descriptor checks this
+// before computing any geometry.
+inline bool desc_ok(const hq_layer_desc *d) {
+    if (!d || !desc_valid(d->K, d->N, d->group, d->format)) return false;
+    if (d->K > MAX_K) return false;
+    const long long kt = d->group > 128 ? d->group : 128;
+    const long long tiles = ((long long)d->N + BN - 1) / BN * (((long long)d->K + kt - 1) / kt);
+    return tiles <= (1LL << 30);
 }
 
 __host__ __device__ inline Geom make_geom(int K, int N, int G, int fmt) {
@@ -81,7 +96,6 @@ __host__ __device__ inline Geom make_geom(int K, int N, int G, int fmt) {
     g.scale_bytes = g.GPT * BN * 4;
     g.zero_bytes = fmt == HQ_W4_ASYM ? g.GPT * BN / 2 : 0;
     g.tile_bytes = g.code_bytes + g.scale_bytes + g.zero_bytes;
-    g.chunk_k = fmt == HQ_W4_ASYM ? 64 : 32;
     return g;
 }
 
@@ -90,14 +104,11 @@ __host__ __device__ inline size_t blob_bytes(const Geom &g) {
 }
 
 // Workspace: [0, 16) error word; then the partial-sum slots, two per thread
-// block, BN x MAX_M_LAUNCH floats each (a launch fills its first M rows);
-// then two counters per n-block (arrivals [NB], then finished reductions
-// [NB]).  Every offset is independent of the layer and of M, so one
-// workspace, large enough for each call, serves calls of any shape in turn.
-// The GEMM handles at most MAX_M_LAUNCH rows per launch (larger batches are
-// run as consecutive launches that reuse the workspace).
-constexpr int MAX_M_LAUNCH = 32;
-__host__ __device__ inline size_t ws_slot_floats() { return (size_t)BN * (size_t)MAX_M_LAUNCH; }
+// block, BN x MAX_M floats each (a call fills its first M rows); then two
+// counters per n-block (arrivals [NB], then finished reductions [NB]).
+// Every offset is independent of the layer and of M, so one workspace, large
+// enough for each call, serves calls of any shape in turn.
+__host__ __device__ inline size_t ws_slot_floats() { return (size_t)BN * (size_t)MAX_M; }
 __host__ __device__ inline size_t ws_partial_offset() { return 16; }
 __host__ __device__ inline size_t ws_counter_offset() {
     return ws_partial_offset() + (size_t)MAX_CTAS * 2 * ws_slot_floats() * 4;
@@ -105,13 +116,25 @@ __host__ __device__ inline size_t ws_counter_offset() {
 __host__ __device__ inline size_t ws_counter_bytes(const Geom &g) { return ((size_t)g.NB * 8 + 15) / 16 * 16; }
 __host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_offset() + ws_counter_bytes(g); }
 
-// Activation operand of the GEMM: fp16 codes in blocks of 128 features,
-// [ceil(K/128)][M][128]; inside a 256-byte row the 16-byte chunk q of token
-// row t is stored at chunk q ^ (4 * (t & 1)) (bank-conflict-free reads of
-// the mma B operands); features past K are zero.
+// Activation operand of the GEMM (private to the library).  Rows are padded
+// to MT = 16, 32, 64 or 128 (the MMA's N); rows past M and features past K
+// are zero.
+//   codes      [ceil(K/128) blocks][16 chunks of 8 features][MT rows][8 fp16]:
+//              a block is the B operand of the tile's MMAs as 8-row x
+//              16-byte core matrices (K-major, no swizzle).
+//   group sums [groups][MT] fp32: S[g][m] = sum of the int8 codes of row m
+//              over group g; the groups are counted per 128-feature block
+//              (128 / G per block for G <= 128), so that every tile finds its
+//              own, zero past K.
 constexpr int ACT_BLOCK = 128;
-__host__ __device__ inline size_t act_operand_bytes(int M, int K) {
-    return (size_t)M * (size_t)((K + ACT_BLOCK - 1) / ACT_BLOCK) * ACT_BLOCK * 2;
+__host__ __device__ inline int act_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+__host__ __device__ inline int act_blocks(int K) { return (K + ACT_BLOCK - 1) / ACT_BLOCK; }
+__host__ __device__ inline int act_groups(int K, int G) { return G <= ACT_BLOCK ? act_blocks(K) * (ACT_BLOCK / G) : K / G; }
+__host__ __device__ inline size_t act_code_bytes(int M, int K) {
+    return (size_t)act_blocks(K) * (size_t)act_rows(M) * ACT_BLOCK * 2;
+}
+__host__ __device__ inline size_t act_operand_bytes(int M, int K, int G) {
+    return act_code_bytes(M, K) + (size_t)act_groups(K, G) * (size_t)act_rows(M) * 4;
 }
 
 // Device error codes written to the workspace error word.
@@ -167,17 +190,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase (no suspension): the fast path of a wait
+// whose phase has usually completed already.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with parity `parity` of barrier `bar` to complete, for
 // at most `limit_ns`.  On time-out, records DEV_ERR_TIMEOUT in *err (if not
 // NULL) and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int *err,
                                                   unsigned long long limit_ns = WAIT_LIMIT_NS) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     uint32_t it = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++it & 15u) == 0u && global_timer_ns() - t0 > limit_ns) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// The same wait for a warp whose waiting must not take issue slots from the
+// warps it shares a scheduler with: between polls it sleeps about sleep_ns.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int *err, uint32_t sleep_ns,
+                                                unsigned long long limit_ns = WAIT_LIMIT_NS) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
             if (err) atomicExch(err, DEV_ERR_TIMEOUT);
             return false;
         }
@@ -221,13 +274,14 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 // Wait until *p >= target (acquire), for at most WAIT_LIMIT_NS; polls with a
 // short sleep in between.  On time-out records DEV_ERR_TIMEOUT in *err and
 // returns false.
-__device__ __forceinline__ bool wait_count_bounded(const int *p, int target, int *err) {
+__device__ __forceinline__ bool wait_count_bounded(const int *p, int target, int *err,
+                                                   unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (ld_acquire_gpu(p) >= target) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         __nanosleep(100);
         if (ld_acquire_gpu(p) >= target) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             if (err) atomicExch(err, DEV_ERR_TIMEOUT);
             return false;
         }
@@ -276,12 +330,13 @@ __device__ __forceinline__ bool wait_flag_bounded(uint32_t addr, int *err) {
 // reset, which happens only after the mark was added), for at most
 // WAIT_LIMIT_NS; acquire.  On time-out records DEV_ERR_TIMEOUT in *err and
 // returns false.
-__device__ __forceinline__ bool wait_mark_bounded(const int *p, int mark, int own, int *err) {
+__device__ __forceinline__ bool wait_mark_bounded(const int *p, int mark, int own, int *err,
+                                                  unsigned long long limit_ns = WAIT_LIMIT_NS) {
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         const int v = ld_acquire_gpu(p);
         if (v >= mark || v < own) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             if (err) atomicExch(err, DEV_ERR_TIMEOUT);
             return false;
         }
@@ -298,13 +353,18 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 
 // Launchers (defined in the kernel translation units).
 namespace hq {
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop,
-                                    float *sx, bool pdl, cudaStream_t s);
-cudaError_t launch_pack(const Geom &g, const float *W, const uint32_t *signs, void *blob, cudaStream_t s);
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx,
+                                    int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s);
+// rows of W -> n-blocks nb0.. of the blob of layer g
+cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,
+                        cudaStream_t s);
 cudaError_t launch_unpack(const Geom &g, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
                           cudaStream_t s);
+// flags: HQ_LAUNCH_* of hq_verify_gemm; wait_extra / wait_ns: the bounded-wait
+// self-test (0 / 0 = normal call).
 cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *qop, const float *sx, int M, float *Y,
-                               int32_t *partials, void *workspace, bool pdl, bool det, cudaStream_t s);
+                               int32_t *partials, void *workspace, uint32_t flags, cudaStream_t s,
+                               int wait_extra = 0, long long wait_ns = 0);
 cudaError_t launch_wait_selftest(void *workspace, long long limit_ns, cudaStream_t s);
 // Draft-tree acceptance: ACCEPT_CHUNK logits per thread block of the argmax.
 constexpr int ACCEPT_CHUNK = 8192;

@@ -13,7 +13,10 @@
 // IEEE-rounded fp32 operation in the order 1, 2, 4, 8, 16, so the rotated
 // values are bit-identical to a scalar implementation of the same order.
 // The codes are written as int8 and/or as the GEMM's operand: fp16 (exact
-// for |q| <= 127) in 128-feature blocks, laid out for its tensor-core steps.
+// for |q| <= 127) in 128-feature blocks laid out as the MMA's B operand, plus
+// the per-group sums of the codes (the Medium identity's correction term).
+// The grid has one block per operand row: rows past M (padding up to the
+// MMA's N) only write zeros.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -34,16 +37,39 @@ __device__ __forceinline__ float bfly_x(float v, int lane_bit, bool upper) {
 }
 
 template <int V, int T>
-__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K,
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G,
                                                         const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
-                                                        uint8_t *__restrict__ qop, float *__restrict__ sx) {
+                                                        int32_t *__restrict__ gsum, uint8_t *__restrict__ qop,
+                                                        float *__restrict__ sx) {
     __shared__ float s_red[T / 32];
+    __shared__ int s_gs[MAX_K / 16];  // group sums of this row
     pdl_wait();
 
     const int row = blockIdx.x;
+    const int MT = gridDim.x;  // operand rows
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int n4 = K >> 2;  // float4s per row
+    const int n4pad = act_blocks(K) * (ACT_BLOCK / 4);
+    const int ngk = K / G, ngp = act_groups(K, G);
+    float *op_s = qop ? reinterpret_cast<float *>(qop + act_code_bytes(M, K)) : nullptr;
+    // byte offset of the 4 features 4*idx .. 4*idx+3 of this row in the operand
+    auto op_off = [&](int idx) -> size_t {
+        const int f = idx * 4;
+        return ((size_t)(f / 8) * MT + row) * 16 + (size_t)(f % 8) * 2;
+    };
+
+    if (row >= M) {
+        // padding row of the operand: zero codes, zero group sums
+        if (qop) {
+            for (int idx = tid; idx < n4pad; idx += T) *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(0u, 0u);
+            for (int g = tid; g < ngp; g += T) op_s[(size_t)g * MT + row] = 0.0f;
+        }
+        pdl_launch_dependents();
+        return;
+    }
+    for (int g = tid; g < ngk; g += T) s_gs[g] = 0;
+
     const float c = __int_as_float((int)HADAMARD_SCALE_BITS);
     const float4 *xr = reinterpret_cast<const float4 *>(X + (size_t)row * K);
 
@@ -89,12 +115,11 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     }
 
     // The dependent GEMM may launch now that this block's reads of X are in:
-    // its blocks' weight prefetch then no longer delays those reads (pass 1.848
-    // -> 1.811 ms against a launch at the start; at the end, 1.984 ms).
+    // its blocks' weight prefetch then no longer delays those reads.
     pdl_launch_dependents();
 
     // row absmax: warp, then every warp reduces the warps' maxima itself
-    // (one block barrier)
+    // (one block barrier; it also orders the zeroing of s_gs before the adds)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) s_red[tid >> 5] = amax;
@@ -106,9 +131,11 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     if (tid == 0) sx[row] = s;
 
     // outputs: int8 codes and/or the GEMM operand (the same codes as fp16,
-    // exact), 4 features per thread; the operand's padding past K is zeroed
+    // exact), 4 features per thread; the operand's padding past K is zeroed.
+    // Group sums: the G/4 consecutive threads of a group (within a warp for
+    // G <= 128) reduce by shuffles, one lane adds into shared memory.
     char4 *qr = qx ? reinterpret_cast<char4 *>(qx + (size_t)row * K) : nullptr;
-    const int n4pad = ((K + ACT_BLOCK - 1) / ACT_BLOCK) * (ACT_BLOCK / 4);
+    const int width = G / 4 < 32 ? G / 4 : 32;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int idx = tid + j * T;
@@ -123,21 +150,28 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
         if (qop && idx < n4pad) {
             const uint32_t h0 = __half_as_ushort(__int2half_rn(q0)), h1 = __half_as_ushort(__int2half_rn(q1));
             const uint32_t h2 = __half_as_ushort(__int2half_rn(q2)), h3 = __half_as_ushort(__int2half_rn(q3));
-            const int f = idx * 4;                      // first feature
-            const int kb = f / ACT_BLOCK;               // 128-feature block
-            const int q = (f % ACT_BLOCK) / 8;          // 16-byte chunk in the row
-            const int qs = q ^ ((row & 1) << 2);        // swizzled chunk
-            uint8_t *dst = qop + ((size_t)kb * M + row) * (ACT_BLOCK * 2) + qs * 16 + (f % 8) * 2;
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+            *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
         }
+        // every thread of the warp takes part in the shuffles (lanes past the
+        // row's end add zeros); a group's G/4 threads are consecutive lanes
+        int gs = q0 + q1 + q2 + q3;
+        for (int o = width / 2; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+        if (idx < n4 && (lane & (width - 1)) == 0) atomicAdd(&s_gs[(idx * 4) / G], gs);
+    }
+    __syncthreads();
+    for (int g = tid; g < ngp; g += T) {
+        const int v2 = g < ngk ? s_gs[g] : 0;
+        if (gsum && g < ngk) gsum[(size_t)row * ngk + g] = v2;
+        if (op_s) op_s[(size_t)g * MT + row] = (float)v2;
     }
 }
 
 template <int V, int T>
-cudaError_t launch_act_t(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop, float *sx,
-                         bool pdl, cudaStream_t s) {
+cudaError_t launch_act_t(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, int32_t *gsum,
+                         uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)M);
+    // one block per operand row (rows past M write the operand's zero padding)
+    cfg.gridDim = dim3((unsigned)(qop ? act_rows(M) : M));
     cfg.blockDim = dim3(T);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -146,25 +180,25 @@ cudaError_t launch_act_t(const float *X, int M, int K, const uint32_t *signs, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, signs, qx, qop, sx);
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, signs, qx, gsum, qop, sx);
 }
 
 }  // namespace
 
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, const uint32_t *signs, int8_t *qx, uint8_t *qop,
-                                    float *sx, bool pdl, cudaStream_t s) {
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx,
+                                    int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     // As many threads per row as the row has float4s, up to 1024: the kernel
     // is latency-bound (one block per row), so the shortest chain per thread
     // wins (256 threads x 4 float4s at K = 4096 made the pass 4% slower).
     const int n4 = K / 4;
-    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
-    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, signs, qx, qop, sx, pdl, s);
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -3,7 +3,5 @@
 #include "k_gemm.cuh"
 
 namespace hq {
-cudaError_t launch_gemm_w4(const GemmArgs &a, int G, bool pdl, cudaStream_t s) {
-    return launch_gemm_fmt<HQ_W4_ASYM>(a, G, pdl, s);
-}
+cudaError_t launch_gemm_w4(const GemmArgs &a, bool pdl, cudaStream_t s) { return launch_gemm_fmt<HQ_W4_ASYM>(a, pdl, s); }
 }  // namespace hq

@@ -3,7 +3,5 @@
 #include "k_gemm.cuh"
 
 namespace hq {
-cudaError_t launch_gemm_w8(const GemmArgs &a, int G, bool pdl, cudaStream_t s) {
-    return launch_gemm_fmt<HQ_W8_SYM>(a, G, pdl, s);
-}
+cudaError_t launch_gemm_w8(const GemmArgs &a, bool pdl, cudaStream_t s) { return launch_gemm_fmt<HQ_W8_SYM>(a, pdl, s); }
 }  // namespace hq

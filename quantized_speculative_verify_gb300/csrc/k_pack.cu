@@ -11,8 +11,8 @@
 // One thread block per blob tile (128 channels x KT features).  Phase 1: each
 // warp rotates rows of the tile, one 32-block per warp instruction (lane j
 // holds feature j; butterfly stride h = lane exchange xor h), and quantizes
-// each (channel, group).  Phase 2: the tile is written in the lane-fragment
-// order the GEMM consumes (layout described in hq_internal.cuh).
+// each (channel, group).  Phase 2: the tile is written in the channel-per-
+// thread order the GEMM consumes (layout described in hq_internal.cuh).
 #include <cuda_runtime.h>
 
 #include "hq_internal.cuh"
@@ -37,8 +37,10 @@ __device__ __forceinline__ float warp_max(float v, int width) {
 }
 
 template <int KT>
-__global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ W, const uint32_t *__restrict__ signs,
-                                              uint8_t *__restrict__ blob) {
+// Packs `rows` rows of W into the n-blocks nb0, nb0 + 1, ... of the blob of
+// layer g (rows past `rows` are zero).
+__global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ W, int rows, int nb0,
+                                              const uint32_t *__restrict__ signs, uint8_t *__restrict__ blob) {
     constexpr int NBLK = KT / 32;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *codes_s = smem;                                    // [BN][KT]
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
         for (int blk = 0; blk < NBLK; ++blk) {
             const int k = kt * KT + blk * 32 + lane;
             float v = 0.0f;
-            if (n < g.N && k < g.K) {
+            if (n < rows && k < g.K) {
                 v = __ldg(W + (size_t)n * g.K + k);
                 const uint32_t sb = (__ldg(signs + (k >> 5)) >> lane) & 1u;
                 v = __int_as_float(__float_as_int(v) ^ (int)(sb << 31));
@@ -128,56 +130,38 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
     }
     __syncthreads();
 
-    uint8_t *tile = blob + ((size_t)b * g.KTILES + kt) * (size_t)g.tile_bytes;
+    uint8_t *tile = blob + ((size_t)(nb0 + b) * g.KTILES + kt) * (size_t)g.tile_bytes;
     const int nchunks = g.code_bytes / 16;
     for (int q = threadIdx.x; q < nchunks; q += blockDim.x) {
-        const int ch = q >> 8, j = (q >> 5) & 7, t = q & 31;
-        const int r0 = j * 16 + (t >> 2), r1 = r0 + 8, tig = t & 3;
-        uint8_t out[16];
+        const int cp = q / BN, r = q % BN;  // 16-byte run cp of channel r
+        const uint8_t *src = codes_s + r * KT;
+        uint32_t wv[4];
         if (w4) {
-            // word (c2, s2): features b = ch*64 + c2*32 + tig*8 + 4*s2 .. b+3;
-            // nibbles n0..n7 = (r0,b) (r1,b) (r0,b+2) (r1,b+2) (r0,b+1) (r1,b+1) (r0,b+3) (r1,b+3)
+            // word j: features 32 cp + 8 j + e; nibble i = feature 2 (i & 3) + (i >> 2)
 #pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-                const int b = ch * 64 + (wd >> 1) * 32 + tig * 8 + 4 * (wd & 1);
-                const uint8_t *p0 = codes_s + r0 * KT + b, *p1 = codes_s + r1 * KT + b;
-                const uint32_t word = (uint32_t)p0[0] | ((uint32_t)p1[0] << 4) | ((uint32_t)p0[2] << 8) |
-                                      ((uint32_t)p1[2] << 12) | ((uint32_t)p0[1] << 16) | ((uint32_t)p1[1] << 20) |
-                                      ((uint32_t)p0[3] << 24) | ((uint32_t)p1[3] << 28);
-                out[4 * wd + 0] = (uint8_t)word;
-                out[4 * wd + 1] = (uint8_t)(word >> 8);
-                out[4 * wd + 2] = (uint8_t)(word >> 16);
-                out[4 * wd + 3] = (uint8_t)(word >> 24);
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t *p8 = src + cp * 32 + j * 8;
+                uint32_t word = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) word |= (uint32_t)(p8[2 * (i & 3) + (i >> 2)] & 15u) << (4 * i);
+                wv[j] = word;
             }
         } else {
-            const int kb = ch * 32 + tig * 8;
+            // features 16 cp + e, e = 0..15, in order
+            const uint8_t *p8 = src + cp * 16;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                out[e] = codes_s[r0 * KT + kb + e];
-                out[4 + e] = codes_s[r1 * KT + kb + e];
-                out[8 + e] = codes_s[r0 * KT + kb + 4 + e];
-                out[12 + e] = codes_s[r1 * KT + kb + 4 + e];
-            }
+            for (int j = 0; j < 4; ++j)
+                wv[j] = (uint32_t)p8[4 * j] | ((uint32_t)p8[4 * j + 1] << 8) | ((uint32_t)p8[4 * j + 2] << 16) |
+                        ((uint32_t)p8[4 * j + 3] << 24);
         }
-        uint4 w;
-        w.x = out[0] | (out[1] << 8) | (out[2] << 16) | ((uint32_t)out[3] << 24);
-        w.y = out[4] | (out[5] << 8) | (out[6] << 16) | ((uint32_t)out[7] << 24);
-        w.z = out[8] | (out[9] << 8) | (out[10] << 16) | ((uint32_t)out[11] << 24);
-        w.w = out[12] | (out[13] << 8) | (out[14] << 16) | ((uint32_t)out[15] << 24);
-        reinterpret_cast<uint4 *>(tile)[q] = w;
+        reinterpret_cast<uint4 *>(tile)[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
     float *sc = reinterpret_cast<float *>(tile + g.code_bytes);
-    for (int q = threadIdx.x; q < g.GPT * BN; q += blockDim.x) {
-        const int gl = q / BN, rem = q % BN, j = rem / 16, pos = rem % 16;
-        const int r = j * 16 + (pos >> 1) + 8 * (pos & 1);
-        sc[q] = scales_s[r * g.GPT + gl];
-    }
+    for (int q = threadIdx.x; q < g.GPT * BN; q += blockDim.x) sc[q] = scales_s[q];  // [channel][group]
     if (w4) {
         uint8_t *zp = tile + g.code_bytes + g.scale_bytes;
-        for (int q = threadIdx.x; q < g.GPT * BN / 2; q += blockDim.x) {
-            const int gl = q / (BN / 2), rem = q % (BN / 2), j = rem / 8, rr = rem % 8;
-            zp[q] = (uint8_t)(zeros_s[(j * 16 + rr) * g.GPT + gl] | (zeros_s[(j * 16 + rr + 8) * g.GPT + gl] << 4));
-        }
+        // nibble i = (channel i / GPT, group i % GPT), low nibble first
+        for (int q = threadIdx.x; q < g.GPT * BN / 2; q += blockDim.x) zp[q] = (uint8_t)(zeros_s[2 * q] | (zeros_s[2 * q + 1] << 4));
     }
 }
 
@@ -188,69 +172,56 @@ __global__ void __launch_bounds__(256) k_unpack(Geom g, const uint8_t *__restric
     const bool w4 = g.fmt == HQ_W4_ASYM;
     const int nchunks = g.code_bytes / 16;
     for (int q = threadIdx.x; q < nchunks; q += blockDim.x) {
-        const int ch = q >> 8, j = (q >> 5) & 7, t = q & 31;
-        const int r0 = j * 16 + (t >> 2), r1 = r0 + 8, tig = t & 3;
-        const uint8_t *in = tile + (size_t)q * 16;
-        const int n0 = b * BN + r0, n1 = b * BN + r1;
-        for (int e = 0; e < 16; ++e) {
-            int k;
+        const int cp = q / BN, r = q % BN;
+        const int n = b * BN + r;
+        const uint4 u = reinterpret_cast<const uint4 *>(tile)[q];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+        if (n >= g.N) continue;
+        for (int j = 0; j < 4; ++j) {
             if (w4) {
-                if (e >= 4) continue;  // one 32-bit word per iteration
-                const int wd = e;
-                const uint32_t word = (uint32_t)in[4 * wd] | ((uint32_t)in[4 * wd + 1] << 8) |
-                                      ((uint32_t)in[4 * wd + 2] << 16) | ((uint32_t)in[4 * wd + 3] << 24);
-                const int b = kt * g.KT + ch * 64 + (wd >> 1) * 32 + tig * 8 + 4 * (wd & 1);
-                // nibble i -> (row, feature offset)
-                const int rowsel[8] = {0, 1, 0, 1, 0, 1, 0, 1};
-                const int foff[8] = {0, 0, 2, 2, 1, 1, 3, 3};
-                for (int nb = 0; nb < 8; ++nb) {
-                    const int kk = b + foff[nb];
-                    const int n = rowsel[nb] ? n1 : n0;
-                    if (kk < g.K && n < g.N) codes[(size_t)n * g.K + kk] = (uint8_t)((word >> (4 * nb)) & 15u);
+                for (int i = 0; i < 8; ++i) {
+                    const int k = kt * g.KT + cp * 32 + j * 8 + 2 * (i & 3) + (i >> 2);
+                    if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
                 }
             } else {
-                const int quarter = e / 4, off = e % 4;
-                k = kt * g.KT + ch * 32 + tig * 8 + (quarter >= 2 ? 4 : 0) + off;
-                const int n = (quarter & 1) ? n1 : n0;
-                if (k < g.K && n < g.N) codes[(size_t)n * g.K + k] = in[e];
+                for (int e = 0; e < 4; ++e) {
+                    const int k = kt * g.KT + cp * 16 + j * 4 + e;
+                    if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)(wv[j] >> (8 * e));
+                }
             }
         }
     }
     const float *sc = reinterpret_cast<const float *>(tile + g.code_bytes);
     for (int q = threadIdx.x; q < g.GPT * BN; q += blockDim.x) {
-        const int gl = q / BN, rem = q % BN, j = rem / 16, pos = rem % 16;
-        const int n = b * BN + j * 16 + (pos >> 1) + 8 * (pos & 1);
-        const int gg = kt * g.GPT + gl;
+        const int n = b * BN + q / g.GPT, gg = kt * g.GPT + q % g.GPT;
         if (n < g.N && gg < g.NGK) scales[(size_t)n * g.NGK + gg] = sc[q];
     }
     if (w4 && zeros) {
         const uint8_t *zp = tile + g.code_bytes + g.scale_bytes;
-        for (int q = threadIdx.x; q < g.GPT * BN / 2; q += blockDim.x) {
-            const int gl = q / (BN / 2), rem = q % (BN / 2), j = rem / 8, rr = rem % 8;
-            const int gg = kt * g.GPT + gl;
-            const int n0 = b * BN + j * 16 + rr, n1 = n0 + 8;
-            if (gg < g.NGK) {
-                if (n0 < g.N) zeros[(size_t)n0 * g.NGK + gg] = zp[q] & 15;
-                if (n1 < g.N) zeros[(size_t)n1 * g.NGK + gg] = zp[q] >> 4;
-            }
+        for (int i = threadIdx.x; i < g.GPT * BN; i += blockDim.x) {
+            const int n = b * BN + i / g.GPT, gg = kt * g.GPT + i % g.GPT;
+            if (n < g.N && gg < g.NGK) zeros[(size_t)n * g.NGK + gg] = (zp[i >> 1] >> (4 * (i & 1))) & 15;
         }
     }
 }
 
 template <int KT>
-cudaError_t launch_pack_t(const Geom &g, const float *W, const uint32_t *signs, void *blob, cudaStream_t s) {
+cudaError_t launch_pack_t(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,
+                          cudaStream_t s) {
     const size_t smem = (size_t)BN * KT + (size_t)BN * g.GPT * 5;
     cudaError_t e = cudaFuncSetAttribute(k_pack<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_pack<KT><<<dim3(g.KTILES, g.NB), 256, smem, s>>>(g, W, signs, static_cast<uint8_t *>(blob));
+    k_pack<KT><<<dim3(g.KTILES, (rows + BN - 1) / BN), 256, smem, s>>>(g, W, rows, nb0, signs,
+                                                                       static_cast<uint8_t *>(blob));
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_pack(const Geom &g, const float *W, const uint32_t *signs, void *blob, cudaStream_t s) {
-    if (g.KT == 128) return launch_pack_t<128>(g, W, signs, blob, s);
-    if (g.KT == 256) return launch_pack_t<256>(g, W, signs, blob, s);
+cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,
+                        cudaStream_t s) {
+    if (g.KT == 128) return launch_pack_t<128>(g, W, rows, nb0, signs, blob, s);
+    if (g.KT == 256) return launch_pack_t<256>(g, W, rows, nb0, signs, blob, s);
     return cudaErrorInvalidValue;
 }
 

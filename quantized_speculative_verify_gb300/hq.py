@@ -26,6 +26,7 @@ HQ_W8_SYM = 1
 HQ_LAUNCH_DEFAULT = 0
 HQ_LAUNCH_PDL = 1
 HQ_LAUNCH_DETERMINISTIC = 2
+HQ_LAUNCH_EXACT_ORDER = 4
 HQ_MAX_M = 128
 
 FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
@@ -33,8 +34,9 @@ FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 # Every symbol include/hq.h declares.
 EXPORTS = ("hq_tree_accept_workspace_bytes", "hq_tree_accept", "hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
            "hq_make_signs",
-           "hq_pack_weights", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
-           "hq_selftest_wait_timeout", "hq_verify_gemm_noalloc", "hq_tree_attention_workspace_bytes",
+           "hq_pack_weights", "hq_pack_weights_at", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
+           "hq_selftest_wait_timeout", "hq_selftest_gemm_wait_timeout", "hq_verify_gemm_noalloc", "hq_noalloc_status",
+           "hq_tree_attention_workspace_bytes",
            "hq_tree_attention", "hq_tree_commit_kv", "hq_delta_tree", "hq_delta_commit")
 
 HQ_ATTN_HEAD_DIM = 128
@@ -75,15 +77,18 @@ def load() -> ctypes.CDLL:
         "hq_version": (I32, []),
         "hq_packed_bytes": (SZ, [D]),
         "hq_workspace_bytes": (SZ, [D, I32]),
-        "hq_act_operand_bytes": (SZ, [I32, I32]),
+        "hq_act_operand_bytes": (SZ, [I32, I32, I32]),
         "hq_make_signs": (ctypes.c_int, [U64, I32, P]),
         "hq_pack_weights": (ctypes.c_int, [D, P, P, P, P]),
-        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, P, P, P, P, U32, P]),
+        "hq_pack_weights_at": (ctypes.c_int, [D, I32, I32, P, P, P, P]),
+        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, I32, P, P, P, P, P, U32, P]),
         "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, I32, P, P, P, U32, P]),
         "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
         "hq_workspace_status": (ctypes.c_int, [P, P]),
         "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
+        "hq_selftest_gemm_wait_timeout": (ctypes.c_int, [D, P, P, P, I32, P, P, ctypes.c_int64, P]),
         "hq_verify_gemm_noalloc": (ctypes.c_int, [D, P, P, P, I32, P, P, U32, P]),
+        "hq_noalloc_status": (ctypes.c_int, [P]),
         "hq_tree_accept_workspace_bytes": (SZ, [I32, I32]),
         "hq_tree_accept": (ctypes.c_int, [P, I32, I32, P, P, P, P, P, P, P, U32, P]),
         "hq_tree_attention_workspace_bytes": (SZ, [I32]),
@@ -152,8 +157,8 @@ def hq_workspace_bytes(desc: hq_layer_desc, M: int) -> int:
     return int(load().hq_workspace_bytes(ctypes.byref(desc), int(M)))
 
 
-def hq_act_operand_bytes(M: int, K: int) -> int:
-    return int(load().hq_act_operand_bytes(int(M), int(K)))
+def hq_act_operand_bytes(M: int, K: int, group: int) -> int:
+    return int(load().hq_act_operand_bytes(int(M), int(K), int(group)))
 
 
 def hq_make_signs(seed: int, K: int) -> np.ndarray:
@@ -167,9 +172,14 @@ def hq_pack_weights(desc, W, signs, blob, stream=None) -> None:
            "hq_pack_weights")
 
 
-def hq_rotate_quant_act(X, M: int, K: int, signs, qx, qop, sx, flags: int = 0, stream=None) -> None:
-    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), _ptr(signs), _ptr(qx), _ptr(qop), _ptr(sx),
-                                      int(flags), _stream(stream)), "hq_rotate_quant_act")
+def hq_pack_weights_at(desc, n0: int, rows: int, W, signs, blob, stream=None) -> None:
+    _check(load().hq_pack_weights_at(ctypes.byref(desc), int(n0), int(rows), _ptr(W), _ptr(signs), _ptr(blob),
+                                     _stream(stream)), "hq_pack_weights_at")
+
+
+def hq_rotate_quant_act(X, M: int, K: int, group: int, signs, qx, gsum, qop, sx, flags: int = 0, stream=None) -> None:
+    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), int(group), _ptr(signs), _ptr(qx), _ptr(gsum),
+                                      _ptr(qop), _ptr(sx), int(flags), _stream(stream)), "hq_rotate_quant_act")
 
 
 def hq_verify_gemm(desc, blob, qop, sx, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
@@ -191,7 +201,13 @@ def hq_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
            "hq_selftest_wait_timeout")
 
 
-HQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 128 * 1024
+def hq_selftest_gemm_wait_timeout(desc, blob, qop, sx, M: int, Y, workspace, limit_ns: int, stream=None) -> None:
+    _check(load().hq_selftest_gemm_wait_timeout(ctypes.byref(desc), _ptr(blob), _ptr(qop), _ptr(sx), int(M), _ptr(Y),
+                                                _ptr(workspace), int(limit_ns), _stream(stream)),
+           "hq_selftest_gemm_wait_timeout")
+
+
+HQ_NOALLOC_SCRATCH_BYTES = 20 * 1024 * 1024 + 128 * 1024
 
 
 def hq_verify_gemm_noalloc(desc, blob, qop, sx, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:
@@ -203,6 +219,11 @@ def hq_verify_gemm_noalloc(desc, blob, qop, sx, M: int, Y, partials=None, flags:
         raise HQError(rc, f"hq_verify_gemm_noalloc: this call needs {need} bytes of scratch, more than the "
                           f"library's fixed {HQ_NOALLOC_SCRATCH_BYTES}-byte array")
     _check(rc, "hq_verify_gemm_noalloc")
+
+
+def hq_noalloc_status(stream=None) -> int:
+    """HQ_ERR_TIMEOUT if an allocation-free call on the current device timed out since the last status call."""
+    return int(load().hq_noalloc_status(_stream(stream)))
 
 
 # ------------------------------------------------------- tensor helpers ---
@@ -243,23 +264,46 @@ def pack_layer(W: torch.Tensor, group: int, fmt, signs_host: np.ndarray, stream=
     return PackedLayer(desc, blob, signs)
 
 
-def act_buffers(M: int, K: int, device, int8_codes: bool = True) -> tuple:
-    """(qx int8 [M][K] or None, GEMM activation operand (uint8 bytes), sx fp32 [M])."""
+@dataclass
+class FusedLayer:
+    """Several layers that read the same activations, packed into one blob:
+    one GEMM computes all of them; `split(Y)` gives each part's outputs as
+    views of Y's columns."""
+    layer: PackedLayer
+    widths: list
+    offsets: list
+
+    def split(self, Y: torch.Tensor) -> list:
+        return [Y[:, o:o + w] for o, w in zip(self.offsets, self.widths)]
+
+
+def pack_fused(Ws: list, group: int, fmt, signs_host: np.ndarray, stream=None) -> FusedLayer:
+    """Pack the parts Ws (fp32 [N_i][K] on the device, same K) into one blob;
+    every part but the last must have a multiple of 128 rows."""
+    K = Ws[0].shape[1]
+    widths = [int(w.shape[0]) for w in Ws]
+    if any(w.shape[1] != K for w in Ws) or any(n % 128 for n in widths[:-1]):
+        raise HQError(HQ_ERR_INVALID_ARG, "pack_fused: parts need the same K and widths that are multiples of 128")
+    offsets = [sum(widths[:i]) for i in range(len(widths))]
+    desc = make_desc(K, sum(widths), group, fmt)
+    nbytes = hq_packed_bytes(desc)
+    if nbytes == 0:
+        raise HQError(HQ_ERR_INVALID_ARG, "hq_packed_bytes")
+    dev = Ws[0].device
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    signs = torch.from_numpy(signs_host.astype(np.int32, copy=False).view(np.int32)).to(dev)
+    for W, o in zip(Ws, offsets):
+        hq_pack_weights_at(desc, o, W.shape[0], W.contiguous(), signs, blob, stream)
+    return FusedLayer(PackedLayer(desc, blob, signs), widths, offsets)
+
+
+def act_buffers(M: int, K: int, group: int, device, int8_codes: bool = True, group_sums: bool = False) -> tuple:
+    """(qx int8 [M][K] or None, gsum int32 [M][K/group] or None, GEMM activation operand (opaque bytes), sx fp32 [M])."""
     qx = torch.empty((M, K), dtype=torch.int8, device=device) if int8_codes else None
-    qop = torch.empty(hq_act_operand_bytes(M, K), dtype=torch.uint8, device=device)
+    gsum = torch.empty((M, K // group), dtype=torch.int32, device=device) if group_sums else None
+    qop = torch.empty(hq_act_operand_bytes(M, K, group), dtype=torch.uint8, device=device)
     sx = torch.empty(M, dtype=torch.float32, device=device)
-    return qx, qop, sx
-
-
-def decode_act_operand(qop: np.ndarray, M: int, K: int) -> np.ndarray:
-    """The GEMM activation operand as fp16 codes [M][K] (layout in include/hq.h)."""
-    nb = (K + 127) // 128
-    a = np.asarray(qop, dtype=np.uint8).view(np.float16).reshape(nb, M, 16, 8)
-    out = np.empty((M, nb * 128), dtype=np.float16)
-    for m in range(M):
-        chunks = np.arange(16) ^ (4 * (m & 1))
-        out[m] = a[:, m, chunks, :].reshape(nb * 128)
-    return out[:, :K]
+    return qx, gsum, qop, sx
 
 
 def workspace(desc: hq_layer_desc, M: int, device) -> torch.Tensor:
@@ -284,11 +328,11 @@ def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torc
     """Y = dequant(int GEMM(quant(rotate(X)), packed W)): the two kernels in sequence."""
     M, K = X.shape
     if bufs is None:
-        bufs = act_buffers(M, K, X.device, int8_codes=False)
-    qx, qop, sx = bufs
+        bufs = act_buffers(M, K, layer.group, X.device, int8_codes=False)
+    qx, gsum, qop, sx = bufs
     if Y is None:
         Y = torch.empty((M, layer.N), dtype=torch.float32, device=X.device)
-    hq_rotate_quant_act(X, M, K, layer.signs, qx, qop, sx, flags & HQ_LAUNCH_PDL, stream)
+    hq_rotate_quant_act(X, M, K, layer.group, layer.signs, qx, gsum, qop, sx, flags & HQ_LAUNCH_PDL, stream)
     hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, partials, ws, flags, stream)
     return Y
 

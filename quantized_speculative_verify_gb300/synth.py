@@ -90,6 +90,28 @@ def decoder_linears(cfg=DECODER_9B, fuse_qkv: bool = False):
     return out
 
 
+def decoder_gemms(cfg=DECODER_9B, fuse_qkv: bool = True):
+    """The GEMMs of one verify pass in launch order: (name, K, parts) with
+    parts = [(part name, N, weight seed index)].  q, k and v read the same
+    activations and, with fuse_qkv, run as one GEMM over their three weight
+    matrices; gate and up always run as one GEMM over their two.  The seed
+    index of a part is its position in the unfused list of matrices."""
+    h, kv, f = cfg["hidden"], cfg["kv"], cfg["ffn"]
+    out, idx = [], 0
+    for l in range(cfg["n_layers"]):
+        qkv = [(f"l{l}.q", h, idx), (f"l{l}.k", kv, idx + 1), (f"l{l}.v", kv, idx + 2)]
+        if fuse_qkv:
+            out.append((f"l{l}.qkv", h, qkv))
+        else:
+            out += [(name, h, [(name, n, i)]) for name, n, i in qkv]
+        out.append((f"l{l}.o", h, [(f"l{l}.o", h, idx + 3)]))
+        out.append((f"l{l}.gate_up", h, [(f"l{l}.gate", f, idx + 4), (f"l{l}.up", f, idx + 5)]))
+        out.append((f"l{l}.down", f, [(f"l{l}.down", h, idx + 6)]))
+        idx += 7
+    out.append(("lm_head", h, [("lm_head", cfg["vocab"], idx)]))
+    return out
+
+
 def decoder_weight_count(cfg=DECODER_9B) -> int:
     return sum(K * N for _, K, N in decoder_linears(cfg))
 

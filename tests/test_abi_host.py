@@ -46,7 +46,7 @@ def test_status_strings_and_version():
     assert hq.status_string(hq.HQ_OK) == "HQ_OK"
     assert hq.status_string(hq.HQ_ERR_TIMEOUT) == "HQ_ERR_TIMEOUT"
     assert hq.status_string(99) == "HQ_ERR_UNKNOWN"
-    assert hq.hq_version() >> 16 == 1
+    assert hq.hq_version() >> 16 == 2  # 2.x: opaque activation operand with group sums, one GEMM launch up to 128 rows
 
 
 @pytest.mark.parametrize("seed,K", [(0, 32), (1, 4096), (2, 12288), (1234567, 256), (2 ** 63 + 5, 8192)])
@@ -88,9 +88,9 @@ def test_invalid_desc_has_no_size(K, N, G, fmt):
 
 def test_tile_count_bound():
     # the kernels index tiles with ints: at most 2^30 tiles (128 channels x 128 features each) per layer
-    at_bound = hq.hq_layer_desc(1 << 24, 1 << 20, 64, hq.HQ_W4_ASYM)  # 2^13 x 2^17 tiles
+    at_bound = hq.hq_layer_desc(1 << 16, 1 << 28, 64, hq.HQ_W4_ASYM)  # 2^21 x 2^9 tiles
     assert hq.hq_packed_bytes(at_bound) == (1 << 30) * (128 * 128 // 2 + 2 * 128 * 4 + 2 * 128 // 2)
-    beyond = hq.hq_layer_desc(1 << 24, (1 << 20) + 128, 64, hq.HQ_W4_ASYM)
+    beyond = hq.hq_layer_desc(1 << 16, (1 << 28) + 128, 64, hq.HQ_W4_ASYM)
     assert hq.hq_packed_bytes(beyond) == 0 and hq.hq_workspace_bytes(beyond, 16) == 0
     lib = hq.load()
     fake = 0x10000  # never dereferenced: the descriptor is rejected first
@@ -99,18 +99,37 @@ def test_tile_count_bound():
     assert lib.hq_pack_weights(ctypes.byref(beyond), fake, fake, fake, None) == hq.HQ_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("K", [65536 + 64, 1 << 24, 2 ** 31 - 64])
+def test_K_above_the_activation_limit_is_invalid(K):
+    # K is bounded by what one activation row may hold (65536), far below
+    # where the tile arithmetic (K + 127 in int) could overflow
+    d = hq.hq_layer_desc(K, 128, 64, hq.HQ_W4_ASYM)
+    assert hq.hq_packed_bytes(d) == 0 and hq.hq_workspace_bytes(d, 16) == 0
+    ok = hq.hq_layer_desc(65536, 128, 64, hq.HQ_W4_ASYM)
+    assert hq.hq_packed_bytes(ok) > 0
+    lib = hq.load()
+    fake = 0x10000
+    assert lib.hq_verify_gemm(ctypes.byref(d), fake, fake, fake, 16, fake, None, fake, 0, None) == \
+        hq.HQ_ERR_INVALID_ARG
+
+
 def test_act_operand_bytes():
-    assert hq.hq_act_operand_bytes(16, 4096) == 16 * 32 * 256
-    assert hq.hq_act_operand_bytes(3, 96) == 3 * 1 * 256  # padded to a 128-feature block
-    assert hq.hq_act_operand_bytes(0, 4096) == 0
-    assert hq.hq_act_operand_bytes(129, 4096) == 0 and hq.hq_act_operand_bytes(4, 100) == 0
+    # opaque, but its size follows from the rows padded to the MMA's N (16, 32,
+    # 64, 128), 128-feature blocks of fp16 codes and one fp32 sum per group and row
+    assert hq.hq_act_operand_bytes(16, 4096, 64) == 32 * 16 * 256 + 64 * 16 * 4
+    assert hq.hq_act_operand_bytes(3, 96, 32) == 1 * 16 * 256 + 4 * 16 * 4  # one padded block, its four groups
+    assert hq.hq_act_operand_bytes(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4
+    assert hq.hq_act_operand_bytes(128, 4096, 16) == 32 * 128 * 256 + 256 * 128 * 4
+    assert hq.hq_act_operand_bytes(0, 4096, 64) == 0
+    assert hq.hq_act_operand_bytes(129, 4096, 64) == 0 and hq.hq_act_operand_bytes(4, 100, 32) == 0
+    assert hq.hq_act_operand_bytes(4, 96, 64) == 0 and hq.hq_act_operand_bytes(4, 256, 48) == 0  # bad group
 
 
 def test_workspace_bytes():
     d = hq.make_desc(4096, 4096, 64, "w4")
-    assert hq.hq_workspace_bytes(d, 16) == hq.hq_workspace_bytes(d, 1) > 16 * 1024 * 1024
+    assert hq.hq_workspace_bytes(d, 16) == hq.hq_workspace_bytes(d, 1) > 20 * 1024 * 1024
     assert hq.hq_workspace_bytes(d, 129) == 0 and hq.hq_workspace_bytes(d, -1) == 0
-    assert hq.hq_workspace_bytes(d, 128) == hq.hq_workspace_bytes(d, 32)  # at most 32 rows per launch
+    assert hq.hq_workspace_bytes(d, 128) == hq.hq_workspace_bytes(d, 1)  # one launch for every M
     assert hq.hq_workspace_bytes(d, 16) % 16 == 0
     # a wider layer needs more counters, at the same offsets: a workspace sized
     # for the widest layer serves every layer
@@ -132,15 +151,18 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert lib.hq_pack_weights(ctypes.byref(bad), FAKE, FAKE, FAKE, None) == E
     assert lib.hq_pack_weights(D, None, FAKE, FAKE, None) == E
     assert lib.hq_pack_weights(D, FAKE, FAKE, FAKE + 8, None) == E  # blob must be 16-byte aligned
-    # activations
-    assert lib.hq_rotate_quant_act(FAKE, 129, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, -1, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 100, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(None, 4, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, None, None, FAKE, 0, None) == E  # no output at all
-    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, FAKE, FAKE, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, FAKE, FAKE + 8, FAKE, 0, None) == E  # operand alignment
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, FAKE, FAKE, FAKE, FAKE, 2, None) == E
+    # activations: (X, M, K, group, signs, qx, gsum, qop, sx, flags, stream)
+    assert lib.hq_rotate_quant_act(FAKE, 129, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, -1, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 100, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 48, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E  # group
+    assert lib.hq_rotate_quant_act(FAKE, 4, 96, 64, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E  # K % group
+    assert lib.hq_rotate_quant_act(None, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, None, None, None, FAKE, 0, None) == E  # no output
+    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, None, FAKE + 8, FAKE, 0, None) == E  # operand
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 0, None) == E  # gsum
+    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 2, None) == E
     # gemm
     assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 129, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, None, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
@@ -149,20 +171,23 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert lib.hq_verify_gemm(D, FAKE + 8, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, FAKE, FAKE + 8, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 8, None) == E
-    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 4, None) == E  # unknown flag bit
+    assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 16, None) == E  # unknown flag bit
     assert lib.hq_verify_gemm(ctypes.byref(bad), FAKE, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
     # unpack / status / self-test
     assert lib.hq_unpack_codes(D, FAKE, FAKE, FAKE, None, None) == E  # W4 needs zeros
     assert lib.hq_workspace_status(None, None) == E
     assert lib.hq_selftest_wait_timeout(FAKE, 10, None) == E
     assert lib.hq_selftest_wait_timeout(None, 10 ** 6, None) == E
+    assert lib.hq_selftest_gemm_wait_timeout(D, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, None) == E
+    assert lib.hq_selftest_gemm_wait_timeout(D, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 10 ** 6, None) == E
+    assert lib.hq_selftest_gemm_wait_timeout(D, FAKE, FAKE, FAKE, 4, FAKE, None, 10 ** 6, None) == E
 
 
 def test_empty_batch_is_a_no_op():
     lib = hq.load()
     d = hq.make_desc(256, 256, 32, "w4")
     # M = 0: nothing to do, nothing launched, pointers never touched
-    assert lib.hq_rotate_quant_act(None, 0, 256, None, None, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_rotate_quant_act(None, 0, 256, 32, None, None, None, None, None, 0, None) == hq.HQ_OK
     assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK
 
 
@@ -239,7 +264,7 @@ def test_binding_refuses_host_buffers_as_device_pointers():
     import torch
     d = hq.make_desc(256, 256, 32, "w4")
     with pytest.raises(TypeError, match="CPU tensor"):
-        hq.hq_rotate_quant_act(torch.zeros((1, 256)), 1, 256, None, None, None, None)
+        hq.hq_rotate_quant_act(torch.zeros((1, 256)), 1, 256, 32, None, None, None, None, None)
     with pytest.raises(TypeError, match="ndarray"):
         hq.hq_verify_gemm(d, np.zeros(16, dtype=np.uint8), None, None, 1, None, None, None)
     with pytest.raises(TypeError, match="CPU tensor"):

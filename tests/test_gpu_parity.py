@@ -14,14 +14,12 @@ import torch
 
 import oracle
 from quantized_speculative_verify_gb300 import hq, synth
+from guard import Guarded
+from tolerance import ATOL, RTOL, assert_close, strict_fraction  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
-ATOL, RTOL = 1e-6, 1e-5
 DEV = "cuda"
-# Fraction of outputs that must also meet |dY| <= ATOL + RTOL |Y| with the
-# relative part taken against |Y| itself (see assert_close).
-STRICT_FRACTION = 0.99
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,56 +29,22 @@ def _need_gpu():
     hq.load()
 
 
-def sum_magnitude(ref):
-    """sx[m] * sum_g |scale[n][g] * P[m][n][g]|: the size of the fp32 sum that forms Y[m][n]."""
-    terms = np.abs(ref["scales"].astype(np.float64)[None] * ref["P"].astype(np.float64)).sum(-1)
-    return np.abs(ref["sx"].astype(np.float64))[:, None] * terms
-
-
-def assert_close(y, ref_out):
-    """fp32 outputs within 1e-6 absolute + 1e-5 relative of the oracle.
-
-    The fp32 sum over quantization groups is formed in ascending group order
-    by the oracle and by every thread block that owns a 128-channel block's
-    whole K range (those outputs are bit-identical, see
-    test_gemm_unsplit_blocks_are_bit_exact); where K is split between thread
-    blocks the partial sums are added in ascending K order, which rounds
-    differently.  Any two summation orders of the same fp32 terms differ by
-    a few ulp of the partial sums, so the relative part is taken against the
-    magnitude of the sum being formed, sx * sum_g |scale * P|; in addition at
-    least STRICT_FRACTION of the outputs must meet the tolerance relative to
-    |Y| itself.  In the default (accumulating) mode each thread block adds
-    sx * (its partial sum) into Y in whatever order the blocks finish: one
-    more rounding per block, of the same size, well inside the bound."""
-    y = np.asarray(y, dtype=np.float64)
-    ref = np.asarray(ref_out["Y"], dtype=np.float64)
-    err = np.abs(y - ref)
-    mag = np.maximum(np.abs(ref), sum_magnitude(ref_out))
-    lim = ATOL + RTOL * mag
-    bad = err > lim
-    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance; worst {np.max(err - lim):.3e}"
-    strict = err <= ATOL + RTOL * np.abs(ref)
-    assert strict.mean() >= STRICT_FRACTION, f"only {strict.mean():.5f} within the elementwise tolerance"
-
-
-def gpu_act(X, signs_dev):
+def gpu_act(X, signs_dev, G):
     M, K = X.shape
-    qx, qop, sx = hq.act_buffers(M, K, DEV)
-    qop.fill_(0xFF)  # padding must be written, not left over
-    hq.hq_rotate_quant_act(X, M, K, signs_dev, qx, qop, sx)
+    qx = Guarded((M, K), torch.int8, DEV)
+    gsum = Guarded((M, K // G), torch.int32, DEV)
+    qop = Guarded((hq.hq_act_operand_bytes(M, K, G),), torch.uint8, DEV, fill=0xFF)  # padding must be written
+    sx = Guarded((M,), torch.float32, DEV)
+    hq.hq_rotate_quant_act(X, M, K, G, signs_dev, qx.t, gsum.t, qop.t, sx.t)
     torch.cuda.synchronize()
-    return qx, qop, sx
+    for name, g in (("qx", qx), ("gsum", gsum), ("operand", qop), ("sx", sx)):
+        g.check(name)
+    return qx.t, gsum.t, qop.t, sx.t
 
 
-def check_act(qx, qop, sx, rq, rs):
-    M, K = rq.shape
+def check_act(qx, gsum, sx, rq, rs, rg):
     assert np.array_equal(qx.cpu().numpy(), rq)
-    # the GEMM operand holds the same integers as fp16, exactly, and zeros past K
-    op = qop.cpu().numpy()
-    assert np.array_equal(hq.decode_act_operand(op, M, K).astype(np.float64), rq.astype(np.float64))
-    nb = (K + 127) // 128
-    full = hq.decode_act_operand(op, M, nb * 128)
-    assert not full[:, K:].astype(np.float64).any()
+    assert np.array_equal(gsum.cpu().numpy(), rg)
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
 
 
@@ -99,9 +63,9 @@ ACT_CASES = [(1, 32, 32), (3, 64, 16), (16, 256, 32), (17, 256, 64), (16, 4096, 
 def test_rotate_quant_act_bit_exact(M, K, G):
     X = synth.activations(M, K, seed=M * 7 + K, outlier_channels=min(2, K), heavy_frac=0.01)
     s_host, s_dev = signs_pair(M + K, K)
-    qx, qop, sx = gpu_act(X.to(DEV), s_dev)
-    rq, rs, _ = oracle.quant_act(X.numpy(), G, s_host)
-    check_act(qx, qop, sx, rq, rs)
+    qx, gsum, qop, sx = gpu_act(X.to(DEV), s_dev, G)
+    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
+    check_act(qx, gsum, sx, rq, rs, rg)
 
 
 def test_rotate_quant_act_degenerate_rows():
@@ -114,9 +78,9 @@ def test_rotate_quant_act_degenerate_rows():
     X[4, :32] = 3.0                  # constant block
     X[5] = 1e30                      # huge values
     s_host, s_dev = signs_pair(9, K)
-    qx, qop, sx = gpu_act(X.to(DEV), s_dev)
-    rq, rs, _ = oracle.quant_act(X.numpy(), G, s_host)
-    check_act(qx, qop, sx, rq, rs)
+    qx, gsum, qop, sx = gpu_act(X.to(DEV), s_dev, G)
+    rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
+    check_act(qx, gsum, sx, rq, rs, rg)
     assert sx[1].item() == 0.0 and not qx[1].any()
 
 
@@ -126,7 +90,7 @@ def test_rotate_quant_act_nan_does_not_crash():
     X[0, 3] = float("nan")
     X[1, 9] = float("inf")
     _, s_dev = signs_pair(1, K)
-    gpu_act(X.to(DEV), s_dev)  # values unspecified; it must return
+    gpu_act(X.to(DEV), s_dev, G)  # values unspecified; it must return
 
 
 # ----------------------------------------------------------- packing ---
@@ -161,8 +125,8 @@ def test_pack_bit_exact(fmt, K, N, G):
 
 
 # ---------------------------------------------------------------- GEMM ---
-# workspace: 16-byte error word, 512 blocks x 2 slots x 128 x 32 fp32 partial sums, counters
-COUNTER_OFFSET = 16 + 512 * 2 * 128 * 32 * 4
+# workspace: 16-byte error word, 160 blocks x 2 slots x 128 x 128 fp32 partial sums, counters
+COUNTER_OFFSET = 16 + 160 * 2 * 128 * 128 * 4
 
 
 def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
@@ -170,18 +134,22 @@ def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     if layer is None:
         layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
     ws = hq.workspace(layer.desc, M, DEV)
-    bufs = hq.act_buffers(M, K, DEV)
-    P = torch.empty((M, layer.N, K // G), dtype=torch.int32, device=DEV) if check else None
+    bufs = hq.act_buffers(M, K, G, DEV)
+    P = Guarded((M, layer.N, K // G), torch.int32, DEV) if check else None
     # Y starts as NaN: an output the kernel fails to write (or to zero before
-    # accumulating into it) stays NaN and fails the comparison
-    Y = torch.full((M, layer.N), float("nan"), dtype=torch.float32, device=DEV)
-    hq.verify_linear(layer, X.to(DEV), ws, Y=Y, bufs=bufs, partials=P, flags=flags)
+    # accumulating into it) stays NaN and fails the comparison; both live
+    # between guard bands
+    Y = Guarded((M, layer.N), torch.float32, DEV, fill=float("nan"))
+    hq.verify_linear(layer, X.to(DEV), ws, Y=Y.t, bufs=bufs, partials=None if P is None else P.t, flags=flags)
     assert hq.hq_workspace_status(ws) == hq.HQ_OK
     torch.cuda.synchronize()
-    # every call leaves the error word and the n-block counters (after 16 MiB
-    # of partial-sum slots) at zero
+    Y.check("Y")
+    if P is not None:
+        P.check("partials")
+    # every call leaves the error word and the n-block counters (after the
+    # partial-sum slots) at zero
     assert not ws[:16].any() and not ws[COUNTER_OFFSET:].any()
-    return dict(Y=Y.cpu().numpy(), P=None if P is None else P.cpu().numpy(), layer=layer, ws=ws)
+    return dict(Y=Y.t.cpu().numpy(), P=None if P is None else P.t.cpu().numpy(), layer=layer, ws=ws)
 
 
 GEMM_CASES = [("w4", 1, 256, 256, 32), ("w4", 16, 256, 256, 32), ("w4", 3, 512, 200, 64), ("w8", 17, 384, 136, 128),
@@ -200,6 +168,41 @@ def test_gemm_partials_bit_exact_and_output_close(fmt, M, K, N, G, flags):
     ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
     assert np.array_equal(r["P"], ref["P"])
     assert_close(r["Y"], ref)
+
+
+@pytest.mark.parametrize("fmt,M,K,N,G", GEMM_CASES)
+def test_gemm_exact_order_is_bit_exact(fmt, M, K, N, G):
+    # HQ_LAUNCH_EXACT_ORDER: every output summed over its groups in ascending
+    # order by one thread block -> the oracle's sequential fp32 sum, bit for bit
+    X = synth.activations(M, K, seed=M + K, outlier_channels=2)
+    W = synth.weights(N, K, seed=N + K + 1, outlier_frac=0.005)
+    s_host, _ = signs_pair(M * N + K, K)
+    r = run_layer(X, W, G, fmt, s_host, check=True, flags=hq.HQ_LAUNCH_EXACT_ORDER | hq.HQ_LAUNCH_PDL)
+    ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+    assert np.array_equal(r["P"], ref["P"])
+    assert np.array_equal(r["Y"].view(np.uint32), ref["Y"].view(np.uint32))
+
+
+def test_gemm_wait_timeout_selftest_reports_error_and_recovers():
+    # a GEMM whose waits between thread blocks ask for one arrival too many:
+    # each runs out after 1 ms, the call reports HQ_ERR_TIMEOUT, no hang
+    M, K, N, G = 16, 4096, 1024, 64  # 256 tiles over at most 152 blocks: split outputs
+    X = synth.activations(M, K, seed=41, outlier_channels=2)
+    W = synth.weights(N, K, seed=42)
+    s_host, s_dev = signs_pair(43, K)
+    layer = hq.pack_layer(W.to(DEV), G, "w4", s_host)
+    _, _, qop, sx = hq.act_buffers(M, K, G, DEV, int8_codes=False)
+    hq.hq_rotate_quant_act(X.to(DEV), M, K, G, layer.signs, None, None, qop, sx)
+    ws = hq.workspace(layer.desc, M, DEV)
+    Y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    hq.hq_selftest_gemm_wait_timeout(layer.desc, layer.blob, qop, sx, M, Y, ws, 1_000_000)
+    assert hq.hq_workspace_status(ws) == hq.HQ_ERR_TIMEOUT
+    # the context is still usable and a clean workspace gives the right outputs
+    ws.zero_()
+    hq.hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, None, ws, hq.HQ_LAUNCH_EXACT_ORDER)
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    ref = oracle.verify_linear(X.numpy(), W.numpy(), G, "w4", s_host)
+    assert np.array_equal(Y.cpu().numpy().view(np.uint32), ref["Y"].view(np.uint32))
 
 
 def test_gemm_unsplit_blocks_are_bit_exact():
