@@ -328,8 +328,9 @@ class VerifyPass:
             if not name.endswith((".k", ".v")):  # a new activation input
                 s_host = hq.hq_make_signs(synth.layer_seed(seed, 500 + li), K)
                 X = synth.activations(self.M, K, seed=synth.layer_seed(seed, 2000 + li), device=device, **cfg["x"])
-                _, _, qop, sx = hq.act_buffers(self.M, K, self.G, device, int8_codes=False)
-                self.inputs.append([name, K, X, qop, sx, None, s_host])
+                adesc = hq.make_desc(K, 128, self.G, self.fmt)  # the layers that read this input
+                _, _, qop, sx = hq.act_buffers(adesc, self.M, device, int8_codes=False)
+                self.inputs.append([name, K, X, qop, sx, None, s_host, adesc])
             Ws = [synth.weights(n, K, seed=synth.layer_seed(seed, wi), device=device, **cfg["w"])
                   for _, n, wi in parts]
             fused = hq.pack_fused(Ws, self.G, self.fmt, s_host)
@@ -380,9 +381,9 @@ class VerifyPass:
         hq = self.hq
         done = set()
         for ii, li in self.plan:
-            name, K, X, qop, sx, signs, _ = self.inputs[ii]
+            name, K, X, qop, sx, signs, _, adesc = self.inputs[ii]
             if act and ii not in done:
-                hq.hq_rotate_quant_act(X, self.M, K, self.G, signs, None, None, qop, sx, self.flags)
+                hq.hq_rotate_quant_act(adesc, X, self.M, signs, None, None, qop, sx, self.flags)
                 done.add(ii)
             if gemm:
                 layer = self.layers[li]
@@ -612,7 +613,7 @@ def measure_sweep(torch, hq, synth, device, stream, args, peak):
         t1 = None
         for M in c["Ms"]:
             X = synth.activations(M, K, seed=c["seed"] + M, device=device)
-            bufs = hq.act_buffers(M, K, c["G"], device, int8_codes=False)
+            bufs = hq.act_buffers(layers[0].desc, M, device, int8_codes=False)
             Y = torch.empty((M, N), dtype=torch.float32, device=device)
             ws = hq.workspace(layers[0].desc, M, device)
             for i in range(copies * 2):
@@ -661,7 +662,7 @@ def measure_layers(torch, hq, synth, device, stream, peak):
         rows = []
         for M in c["Ms"]:
             X = synth.activations(M, K, seed=c["seed"] + 1, device=device, **c["x"])
-            bufs = hq.act_buffers(M, K, c["G"], device, int8_codes=False)
+            bufs = hq.act_buffers(first.desc, M, device, int8_codes=False)
             Y = torch.empty((M, N), dtype=torch.float32, device=device)
             ws = hq.workspace(first.desc, M, device)
             for i in range(2 * copies):
@@ -886,8 +887,8 @@ def run_one_gemm(args) -> int:
     layer = hq.pack_layer(W, G, fmt, hq.hq_make_signs(3, K))
     del W
     X = synth.activations(M, K, seed=2, device=dev)
-    _, _, qop, sx = hq.act_buffers(M, K, G, dev, int8_codes=False)
-    hq.hq_rotate_quant_act(X, M, K, G, layer.signs, None, None, qop, sx)
+    _, _, qop, sx = hq.act_buffers(layer.desc, M, dev, int8_codes=False)
+    hq.hq_rotate_quant_act(layer.desc, X, M, layer.signs, None, None, qop, sx)
     ws = hq.workspace(layer.desc, M, dev)
     Y = torch.empty((M, N), dtype=torch.float32, device=dev)
     for _ in range(max(args.warmup, 1)):

@@ -164,41 +164,43 @@ int hq_pack_weights(const hq_layer_desc *desc, const float *W, const uint32_t *s
 int hq_pack_weights_at(const hq_layer_desc *desc, int32_t n0, int32_t rows, const float *W, const uint32_t *signs,
                        void *blob, void *stream);
 
-/* Size in bytes of the GEMM's activation operand for M rows, K features and
- * quantization group `group` (0 if the arguments are invalid or M = 0).  The
- * operand is an opaque buffer written by hq_rotate_quant_act and read by
- * hq_verify_gemm; its layout is private to this version of the library. */
-size_t hq_act_operand_bytes(int32_t M, int32_t K, int32_t group);
+/* Size in bytes of the GEMM's activation operand for M rows of the
+ * activations of layers like `desc` (its K, group and format; N is not used),
+ * 0 if the arguments are invalid or M = 0.  The operand is an opaque buffer
+ * written by hq_rotate_quant_act and read by hq_verify_gemm of layers with the
+ * same K, group and format; its layout is private to this version of the
+ * library (it depends on the format and on M). */
+size_t hq_act_operand_bytes(const hq_layer_desc *desc, int32_t M);
 
 /* Verify pass, step 1: rotate and quantize the activations of M rows
  * (section "How Uzu optimizes bytes and tokens per pass": activations
  * quantized to 8 bits on the fly, after the same randomized Hadamard
  * transform as the weights).
- *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op),
- *         K a positive multiple of 32, at most 65536
- *   group quantization group of the layers that read these activations
- *         (16, 32, 64, 128 or 256, dividing K)
+ *   desc  the layers that read these activations: K (a multiple of 32, at
+ *         most 65536), group (16, 32, 64, 128 or 256, dividing K) and format
+ *         choose the operand's encoding; N is not used
+ *   X     fp32 [M][K], 16-byte aligned, 0 <= M <= HQ_MAX_M (M = 0: no-op)
  *   signs uint32 [K/32]
  *   qx    int8 [M][K] (4-byte aligned) or NULL: clamp(rint(x' / sx), -127, 127)
  *   gsum  int32 [M][K/group] (4-byte aligned) or NULL: the sum of the codes
  *         qx over each group (the correction term of the Medium format:
  *         sum qx (q - z) = sum qx q - z * gsum)
- *   qop   the GEMM's activation operand (hq_act_operand_bytes(M, K, group)
+ *   qop   the GEMM's activation operand (hq_act_operand_bytes(desc, M)
  *         bytes, 16-byte aligned, opaque) or NULL
  *   sx    fp32 [M]:  max_k |x'[m][k]| / 127  (0 for an all-zero row)
  * At least one of qx, gsum, qop must be given.  x' is the rotated row: per
  * 32-block, sign flip, unnormalized Walsh-Hadamard butterfly at strides 1, 2,
  * 4, 8, 16 in fp32 without fused multiply-add, then multiplication by
  * fp32(1/sqrt(32)).  flags: HQ_LAUNCH_DEFAULT or HQ_LAUNCH_PDL. */
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, const uint32_t *signs, int8_t *qx,
                         int32_t *gsum, void *qop, float *sx, uint32_t flags, void *stream);
 
 /* Verify pass, step 2: integer GEMM of the quantized activations against the
  * packed weights with the per-group dequantization epilogue (section "How
  * Uzu optimizes bytes and tokens per pass": both matmul operands integers).
  *   blob      packed by hq_pack_weights for the same desc (16-byte aligned)
- *   qop, sx   from hq_rotate_quant_act with the same M, K, group (= desc's)
- *             and signs
+ *   qop, sx   from hq_rotate_quant_act with the same M, a descriptor of the
+ *             same K, group and format, and the same signs
  *   M         0..HQ_MAX_M (0: no-op); one launch for every M
  *   Y         fp32 [M][N]:
  *               Y[m][n] = sx[m] * sum_g ( scale[n][g] * P[m][n][g] )
@@ -208,9 +210,10 @@ int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, con
  *             exactly (slower; for verification)
  *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
  *             before its first use
- * The integer sums P are exact: the codes are multiplied on the fp16 tensor
- * cores (tcgen05) with fp32 accumulation, exact for these ranges, and the
- * Medium zero point enters through the group sums.  The fp32 sum
+ * The integer sums P are exact: the codes are multiplied on the tensor cores
+ * (tcgen05, e4m3 or fp16 operands) with fp32 accumulation, exact for these
+ * ranges, and the Medium zero point enters through the group sums.  The fp32
+ * sum
  * over groups is taken in ascending group order.  An output whose K range is
  * split across thread blocks is the sum of the blocks' partial sums: by
  * default each block adds sx[m] * (its partial sum) into Y with an fp32

@@ -90,26 +90,42 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.code_bytes = g.code_bytes;
     a.scale_bytes = g.scale_bytes;
     const int MT = act_rows(M);
-    a.act_off = (g.tile_bytes + 127) / 128 * 128;
+    const bool e4 = act_e4(g.fmt, M, g.G);
+    const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
+    const int acols = e4 ? g.KT / 4 : g.KT / 2;  // TMEM columns of one tile's widened weights
+    // Pipeline unit: two tiles up to 32 rows (every barrier wait then serves
+    // two tiles), one above.  Tensor memory (512 columns): two A buffers of a
+    // unit, then accumulator units of V groups (as many as fit twice, up to
+    // a unit's groups), up to MAX_ND of them.
+    int U = MT <= 32 ? 2 : 1, V = 1, nd = 0;
+    const int na = 2;
+    for (;;) {
+        const int rem = TMEM_COLS - na * U * acols;
+        V = U * g.GPT;
+        while (V > 1 && 2 * V * dc > rem) V /= 2;
+        nd = rem / (V * dc);
+        if (nd >= 2 || U == 1) break;
+        U = 1;
+    }
+    if (nd > MAX_ND) nd = MAX_ND;
+    a.U = U;
+    a.V = V;
+    a.na = na;
+    a.nd = nd;
     a.act_bytes = (g.KT / ACT_BLOCK) * MT * ACT_BLOCK * 2;
     a.s_bytes = g.GPT * MT * 4;
-    a.stage_bytes = (a.act_off + a.act_bytes + a.s_bytes + 127) / 128 * 128;
+    a.act_off = (U * g.tile_bytes + 127) / 128 * 128;
+    a.s_off = a.act_off + U * a.act_bytes;
+    a.stage_bytes = (a.s_off + U * a.s_bytes + 127) / 128 * 128;
     a.op_s_offset = (long long)act_code_bytes(M, g.K);
-    // Stage ring: as many stages as fit in ~200 KB of shared memory.
+    // Stage ring: as many units as fit in ~200 KB of shared memory.
     int stages = (200 * 1024) / a.stage_bytes;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
     if (stages < 2) stages = 2;
     a.stages = stages;
-    // Tensor memory (512 columns): accumulator slots of MT columns (up to 16,
-    // at least 2) and A buffers of KT/2 columns (up to 4) in what is left.
-    int nd = 256 / MT;
-    if (nd > MAX_ND) nd = MAX_ND;
-    if (nd < 2) nd = 2;
-    int na = (TMEM_COLS - nd * MT) / (g.KT / 2);
-    if (na > MAX_NA) na = MAX_NA;
-    a.na = na;
-    a.nd = nd;
-    if (na < 2 || 2048 + (size_t)stages * a.stage_bytes > (size_t)GEMM_SMEM_LIMIT) return cudaErrorInvalidConfiguration;
+    if (nd < 2 || na * U * acols + nd * V * dc > TMEM_COLS ||
+        2048 + (size_t)stages * a.stage_bytes > (size_t)GEMM_SMEM_LIMIT)
+        return cudaErrorInvalidConfiguration;
     return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, pdl, s) : launch_gemm_w8(a, pdl, s);
 }
 
@@ -120,11 +136,6 @@ using hq::Geom;
 namespace {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// A quantization group the operand can be laid out for: 16..256, dividing K.
-bool group_ok(int32_t K, int32_t G) {
-    return (G == 16 || G == 32 || G == 64 || G == 128 || G == 256) && K > 0 && K % G == 0;
-}
 
 using hq::desc_ok;
 
@@ -197,25 +208,25 @@ int hq_pack_weights_at(const hq_layer_desc *desc, int32_t n0, int32_t rows, cons
     return cuda_status(hq::launch_pack(g, W, rows, n0 / hq::BN, signs, blob, static_cast<cudaStream_t>(stream)));
 }
 
-size_t hq_act_operand_bytes(int32_t M, int32_t K, int32_t group) {
-    if (M < 0 || M > HQ_MAX_M || K <= 0 || K % 32 != 0 || K > hq::MAX_K || !group_ok(K, group)) return 0;
-    if (M == 0) return 0;
-    return hq::act_operand_bytes(M, K, group);
+size_t hq_act_operand_bytes(const hq_layer_desc *desc, int32_t M) {
+    if (!desc_ok(desc) || M <= 0 || M > HQ_MAX_M) return 0;
+    return hq::act_operand_bytes(M, desc->K, desc->group);
 }
 
-int hq_rotate_quant_act(const float *X, int32_t M, int32_t K, int32_t group, const uint32_t *signs, int8_t *qx,
+int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, const uint32_t *signs, int8_t *qx,
                         int32_t *gsum, void *qop, float *sx, uint32_t flags, void *stream) {
+    if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
     if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
-    if (K <= 0 || K % 32 != 0 || !group_ok(K, group)) return HQ_ERR_INVALID_ARG;
     if ((flags & ~HQ_LAUNCH_PDL) != 0) return HQ_ERR_INVALID_ARG;
     if (M == 0) return HQ_OK;
     if (!X || !signs || !sx || (!qx && !qop && !gsum)) return HQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(sx, 4) || !aligned(signs, 4) || (qx && !aligned(qx, 4)) ||
         (gsum && !aligned(gsum, 4)) || (qop && !aligned(qop, 16)))
         return HQ_ERR_INVALID_ARG;
-    if (K > hq::MAX_K) return HQ_ERR_UNSUPPORTED;
-    return cuda_status(hq::launch_rotate_quant_act(X, M, K, group, signs, qx, gsum, static_cast<uint8_t *>(qop), sx,
-                                                   (flags & HQ_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream)));
+    const int K = desc->K, G = desc->group;
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, G, hq::act_e4(desc->format, M, G), signs, qx, gsum,
+                                                   static_cast<uint8_t *>(qop), sx, (flags & HQ_LAUNCH_PDL) != 0,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,

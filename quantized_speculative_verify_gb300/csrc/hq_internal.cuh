@@ -21,9 +21,10 @@ namespace hq {
 //
 //   codes   4-bit: [c][quarter p 0..1][n][16 bytes]: the 32 features
 //           64c + 32p .. +31 of channel n as four 32-bit words of eight
-//           nibbles; nibble i of word j is feature 8j + 2 (i & 3) + (i >> 2)
-//           (so that the GEMM widens a word into the fp16 pairs (0,1) (2,3)
-//           (4,5) (6,7) with one mask each).
+//           nibbles; byte b of word j holds feature 8j + b in its low nibble
+//           and feature 8j + 4 + b in its high nibble (so that one mask gives
+//           the four codes 8j..8j+3 as bytes, and a shift and a mask the next
+//           four).
 //           8-bit: [c][quarter p 0..3][n][16 bytes]: features 64c + 16p + e,
 //           e = 0..15, in order.
 //           A GEMM thread owns one channel: it reads 16 contiguous bytes per
@@ -118,16 +119,28 @@ __host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_of
 
 // Activation operand of the GEMM (private to the library).  Rows are padded
 // to MT = 16, 32, 64 or 128 (the MMA's N); rows past M and features past K
-// are zero.
-//   codes      [ceil(K/128) blocks][16 chunks of 8 features][MT rows][8 fp16]:
-//              a block is the B operand of the tile's MMAs as 8-row x
-//              16-byte core matrices (K-major, no swizzle).
+// are zero.  Two encodings of the int8 codes, chosen by the layers that read
+// the operand (act_e4):
+//   fp16:   [ceil(K/128) blocks][16 chunks of 8 features][MT rows][8 fp16]
+//           (exact for |q| <= 127), the B operand of kind::f16 MMAs;
+//   digits: [ceil(K/128) blocks][8 chunks of 16 features][2 MT rows][16 e4m3]:
+//           q = 16 h + l with l in [-8, 7], h in [-8, 8], both exact in e4m3;
+//           row r < MT holds the l of token r, row MT + r its h: the B
+//           operand of kind::f8f6f4 MMAs whose N covers both digits.
+// Either way a block is the B operand of a tile's MMAs as 8-row x 16-byte
+// core matrices (K-major, no swizzle), MT * 256 bytes.  Then
 //   group sums [groups][MT] fp32: S[g][m] = sum of the int8 codes of row m
 //              over group g; the groups are counted per 128-feature block
 //              (128 / G per block for G <= 128), so that every tile finds its
 //              own, zero past K.
 constexpr int ACT_BLOCK = 128;
 __host__ __device__ inline int act_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+// The digit encoding: 4-bit weights (their codes are e4m3 bytes as they are),
+// rows that fit an MMA of N = 2 MT <= 128, and groups of at least 32 features
+// (one f8f6f4 MMA covers 32).
+__host__ __device__ inline bool act_e4(int fmt, int M, int G) {
+    return fmt == HQ_W4_ASYM && act_rows(M) <= 64 && G >= 32;
+}
 __host__ __device__ inline int act_blocks(int K) { return (K + ACT_BLOCK - 1) / ACT_BLOCK; }
 __host__ __device__ inline int act_groups(int K, int G) { return G <= ACT_BLOCK ? act_blocks(K) * (ACT_BLOCK / G) : K / G; }
 __host__ __device__ inline size_t act_code_bytes(int M, int K) {
@@ -175,17 +188,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Test the phase; a thread whose phase is not complete may be suspended by
-// the hardware until it completes (or for at most ~1 ms, the hint), instead
-// of spinning.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Test the phase; a thread whose phase is not complete is suspended by the
+// hardware until the phase completes or about `hint_ns` elapse, so a waiting
+// warp issues no instructions (polling would take issue slots from the warps
+// that do the work).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -215,22 +229,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++it & 15u) == 0u && global_timer_ns() - t0 > limit_ns) {
-            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// The same wait for a warp whose waiting must not take issue slots from the
-// warps it shares a scheduler with: between polls it sleeps about sleep_ns.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int *err, uint32_t sleep_ns,
-                                                unsigned long long limit_ns = WAIT_LIMIT_NS) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        __nanosleep(sleep_ns);
-        if (mbar_test_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) {
             if (err) atomicExch(err, DEV_ERR_TIMEOUT);
             return false;
         }
@@ -353,7 +351,7 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 
 // Launchers (defined in the kernel translation units).
 namespace hq {
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx,
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
                                     int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s);
 // rows of W -> n-blocks nb0.. of the blob of layer g
 cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,

@@ -51,8 +51,45 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d, uint32_t a, uint64_t b
         : "memory");
 }
 
-// Instruction descriptor of kind::f16: fp16 A and B (both K-major), fp32 D,
-// M rows, N columns.
+// D[128 x N] (+)= A[128 x 32] * B[32 x N], kind::f8f6f4 with e4m3 A (TMEM,
+// column c = elements 4c .. 4c+3) and e4m3 B (shared memory), fp32 D.
+__device__ __forceinline__ void tc_mma_e4m3_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// The same MMAs issued from converged warp code: every lane executes the
+// instruction, only the lane with `leader` set issues it (the operands stay
+// warp-uniform and no branch is taken around each MMA).
+__device__ __forceinline__ void tc_mma_f16_ts_if(uint32_t leader, uint32_t d, uint32_t a, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(acc), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_e4m3_ts_if(uint32_t leader, uint32_t d, uint32_t a, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(acc), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_if(uint32_t leader, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(leader)
+        : "memory");
+}
+
+// Instruction descriptor: M rows, N columns, fp32 D, A and B K-major of type
+// code 0 (fp16 for kind::f16, e4m3 for kind::f8f6f4).
 __host__ __device__ constexpr uint32_t tc_idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

@@ -13,8 +13,9 @@
 // IEEE-rounded fp32 operation in the order 1, 2, 4, 8, 16, so the rotated
 // values are bit-identical to a scalar implementation of the same order.
 // The codes are written as int8 and/or as the GEMM's operand: fp16 (exact
-// for |q| <= 127) in 128-feature blocks laid out as the MMA's B operand, plus
-// the per-group sums of the codes (the Medium identity's correction term).
+// for |q| <= 127) or two e4m3 digits (q = 16 h + l), in 128-feature blocks
+// laid out as the MMA's B operand, plus the per-group sums of the codes (the
+// Medium identity's correction term).
 // The grid has one block per operand row: rows past M (padding up to the
 // MMA's N) only write zeros.
 #include <cuda_fp16.h>
@@ -36,8 +37,29 @@ __device__ __forceinline__ float bfly_x(float v, int lane_bit, bool upper) {
     return upper ? __fsub_rn(p, v) : __fadd_rn(v, p);
 }
 
+// e4m3 byte of an integer v in [-8, 8] (exact): 1..8 are 2^e * (1 + m/8).
+__device__ __forceinline__ uint32_t e4m3_small(int v) {
+    const uint32_t a = (uint32_t)(v < 0 ? -v : v);
+    if (a == 0) return 0u;
+    const uint32_t e = 31u - __clz(a);          // 0..3
+    const uint32_t m = ((a << 3) >> e) & 7u;    // mantissa bits
+    return ((e + 7u) << 3) | m | (v < 0 ? 0x80u : 0u);
+}
+// Low and high e4m3 digits of four codes, one byte each.
+__device__ __forceinline__ void digits4(int q0, int q1, int q2, int q3, uint32_t &lo, uint32_t &hi) {
+    const int q[4] = {q0, q1, q2, q3};
+    lo = hi = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int l = ((q[i] + 8) & 15) - 8;
+        const int h = (q[i] - l) / 16;
+        lo |= e4m3_small(l) << (8 * i);
+        hi |= e4m3_small(h) << (8 * i);
+    }
+}
+
 template <int V, int T>
-__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G,
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G, int e4,
                                                         const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
                                                         int32_t *__restrict__ gsum, uint8_t *__restrict__ qop,
                                                         float *__restrict__ sx) {
@@ -53,16 +75,29 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const int n4pad = act_blocks(K) * (ACT_BLOCK / 4);
     const int ngk = K / G, ngp = act_groups(K, G);
     float *op_s = qop ? reinterpret_cast<float *>(qop + act_code_bytes(M, K)) : nullptr;
-    // byte offset of the 4 features 4*idx .. 4*idx+3 of this row in the operand
+    // byte offset of the 4 features 4*idx .. 4*idx+3 of this row in the
+    // operand: fp16, 8 bytes; digits, 4 bytes of low digits (the high digits
+    // are MT rows further)
     auto op_off = [&](int idx) -> size_t {
         const int f = idx * 4;
+        if (e4) {
+            const int kb = f / ACT_BLOCK, c = (f % ACT_BLOCK) / 16;
+            return (size_t)kb * MT * 256 + ((size_t)c * 2 * MT + row) * 16 + (size_t)(f % 16);
+        }
         return ((size_t)(f / 8) * MT + row) * 16 + (size_t)(f % 8) * 2;
     };
 
     if (row >= M) {
         // padding row of the operand: zero codes, zero group sums
         if (qop) {
-            for (int idx = tid; idx < n4pad; idx += T) *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(0u, 0u);
+            for (int idx = tid; idx < n4pad; idx += T) {
+                if (e4) {
+                    *reinterpret_cast<uint32_t *>(qop + op_off(idx)) = 0u;
+                    *reinterpret_cast<uint32_t *>(qop + op_off(idx) + (size_t)MT * 16) = 0u;
+                } else {
+                    *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(0u, 0u);
+                }
+            }
             for (int g = tid; g < ngp; g += T) op_s[(size_t)g * MT + row] = 0.0f;
         }
         pdl_launch_dependents();
@@ -148,9 +183,16 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
         }
         if (qr && idx < n4) qr[idx] = make_char4((signed char)q0, (signed char)q1, (signed char)q2, (signed char)q3);
         if (qop && idx < n4pad) {
-            const uint32_t h0 = __half_as_ushort(__int2half_rn(q0)), h1 = __half_as_ushort(__int2half_rn(q1));
-            const uint32_t h2 = __half_as_ushort(__int2half_rn(q2)), h3 = __half_as_ushort(__int2half_rn(q3));
-            *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+            if (e4) {
+                uint32_t lo, hi;
+                digits4(q0, q1, q2, q3, lo, hi);
+                *reinterpret_cast<uint32_t *>(qop + op_off(idx)) = lo;
+                *reinterpret_cast<uint32_t *>(qop + op_off(idx) + (size_t)MT * 16) = hi;
+            } else {
+                const uint32_t h0 = __half_as_ushort(__int2half_rn(q0)), h1 = __half_as_ushort(__int2half_rn(q1));
+                const uint32_t h2 = __half_as_ushort(__int2half_rn(q2)), h3 = __half_as_ushort(__int2half_rn(q3));
+                *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+            }
         }
         // every thread of the warp takes part in the shuffles (lanes past the
         // row's end add zeros); a group's G/4 threads are consecutive lanes
@@ -167,8 +209,8 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
 }
 
 template <int V, int T>
-cudaError_t launch_act_t(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx, int32_t *gsum,
-                         uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
+cudaError_t launch_act_t(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
+                         int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     // one block per operand row (rows past M write the operand's zero padding)
     cfg.gridDim = dim3((unsigned)(qop ? act_rows(M) : M));
@@ -180,25 +222,25 @@ cudaError_t launch_act_t(const float *X, int M, int K, int G, const uint32_t *si
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, signs, qx, gsum, qop, sx);
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, e4 ? 1 : 0, signs, qx, gsum, qop, sx);
 }
 
 }  // namespace
 
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, const uint32_t *signs, int8_t *qx,
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
                                     int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     // As many threads per row as the row has float4s, up to 1024: the kernel
     // is latency-bound (one block per row), so the shortest chain per thread
     // wins (256 threads x 4 float4s at K = 4096 made the pass 4% slower).
     const int n4 = K / 4;
-    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
     return cudaErrorInvalidValue;
 }
 

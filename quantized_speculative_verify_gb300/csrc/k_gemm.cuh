@@ -9,22 +9,24 @@
 // memory-bound" (the pass streams every weight once, so the kernel is bound by
 // memory bandwidth, not arithmetic).
 //
-// Integer arithmetic on fp16 tensor cores.  The integer MMA of this GPU is
-// far slower than its fp16 MMA, so the contraction runs as an exact fp16
-// tcgen05.mma with fp32 accumulation in tensor memory (TMEM):
-//  - 8-bit codes q (|q| <= 127) are widened to fp16 q exactly (magic-number
-//    conversion: (1152 + q) - 1152);
-//  - 4-bit codes q are widened to fp16 64 + q (the nibble placed under the
-//    exponent of 64, whose ulp is 1/16: two bitwise operations for two codes),
-//    and the zero point z is applied after the MMA through the group sums of
-//    the activation codes, S = sum_{k in g} qx[k]:
-//        P = sum qx (q - z) = sum qx (64 + q) - (64 + z) S
-//    (the Medium identity of the method); |sum qx (64 + q)| <= 127 * 79 * 256
-//    < 2^24, so every partial sum is an exact fp32 integer and one fused
-//    multiply-add gives P exactly.
-// Activation codes (fp16, exact) are the B operand in shared memory, the
-// widened weights the A operand in TMEM (128 channels = 128 TMEM lanes), and
-// each quantization group's P lands in its own TMEM accumulator slot.
+// Integer arithmetic on floating-point tensor cores.  The integer MMA of this
+// GPU is far slower than its floating-point MMAs, so the contraction runs as
+// exact tcgen05.mma with fp32 accumulation in tensor memory (TMEM), the
+// widened weights as the A operand in TMEM (128 channels = 128 TMEM lanes),
+// the activation codes as the B operand in shared memory, each quantization
+// group's integer sum in its own TMEM accumulator slot:
+//  - 4-bit weights, up to 64 rows, groups of 32 or more: kind::f8f6f4.  A
+//    4-bit code q in a byte is the e4m3 number q * 2^-9 (subnormal up to 7,
+//    then exponent 1), so the codes need only be spread to bytes; an
+//    activation code is split into two exact e4m3 digits, q = 16 h + l, which
+//    the MMA's N covers side by side (N = 2 * rows).  D = 2^-9 sum q l and
+//    2^-9 sum q h, exact; P = 2^9 (D_l + 16 D_h) - z S with the group sum S
+//    (the Medium identity: sum qx (q - z) = sum qx q - z sum qx).
+//  - otherwise kind::f16 with A in fp16: 8-bit codes widened exactly
+//    ((1152 + q) - 1152); 4-bit codes widened to 64 + q (the nibble under the
+//    exponent of 64, whose ulp is 1/16), and P = sum qx (64 + q) - (64 + z) S.
+// Every partial sum is an exact fp32 value (integers, or multiples of 2^-9,
+// below 2^24 units), so the integer P is exact.
 //
 // Epilogue: y += scale * P with separately rounded fp32 multiply and add, in
 // ascending group order, so an output whose whole K range is handled by one
@@ -32,9 +34,11 @@
 // f32x2 multiply and add are not used there: the compiler contracts the pair
 // into a fused multiply-add, which rounds once.)
 //
-// Thread block (one per SM, 14 warps, each role running tiles ahead of the
-// next through rings of shared-memory stages, A buffers and accumulator
-// slots):
+// Thread block (one per SM, 14 warps, each role running ahead of the next
+// through rings of shared-memory stages, A buffers and accumulator slots).
+// The unit of the rings is U consecutive tiles of the block's range (U = 2
+// where tensor memory allows): every barrier wait, which costs about a
+// hundred cycles beside running MMAs, serves U tiles.
 //  - warp 0, one lane: producer.  Per tile, one bulk copy of the weight tile,
 //    one of the activation blocks and one of their group sums into a stage
 //    (mbarrier transaction counts).  The weight copies of the first stages go
@@ -87,11 +91,14 @@ struct GemmArgs {
     long long wait_ns;  // bound of the waits between thread blocks
     int M;    // token rows (the operand is padded to MT rows)
     int N, K, G, KT, GPT, NGK, NB, KTILES, T, grid, stages, na, nd;
+    int U;           // tiles per pipeline unit (stage, A buffer)
+    int V;           // groups per accumulator unit (one wait / commit each)
     int tile_bytes, code_bytes, scale_bytes;
-    int act_off;     // offset of the activation blocks within a stage
-    int act_bytes;   // activation blocks per stage: (KT/128) * MT * 256
-    int s_bytes;     // group sums per stage: GPT * MT * 4
-    int stage_bytes;
+    int act_off;     // offset of the activation blocks within a stage (after U weight tiles)
+    int s_off;       // offset of the group sums within a stage (after U activation blocks)
+    int act_bytes;   // activation blocks of one tile: (KT/128) * MT * 256
+    int s_bytes;     // group sums of one tile: GPT * MT * 4
+    int stage_bytes; // one unit: U weight tiles, their activation blocks and group sums
     long long op_s_offset;  // byte offset of the group sums in the operand
 };
 
@@ -103,18 +110,12 @@ constexpr int ZERO_MARK = 1 << 24;
 // Weight stages a block copies in before waiting for the previous kernel.
 constexpr int PREFETCH_STAGES = 2;
 
-// Back-off of the waits of the roles that are not on the MMA warp's critical
-// path (producer, widening, epilogue): their polling would otherwise take
-// issue slots from the MMA warp on the same scheduler.
-#ifndef HQ_WAIT_SLEEP_NS
-#define HQ_WAIT_SLEEP_NS 64
-#endif
-constexpr uint32_t WAIT_SLEEP_NS = HQ_WAIT_SLEEP_NS;
-
 constexpr int NWID = 4;                       // widening warps
-constexpr int NEPI = 8;                       // epilogue warps
 constexpr int WID0 = 2, EPI0 = WID0 + NWID;   // first warp of each role
-constexpr int GEMM_THREADS = (EPI0 + NEPI) * 32;
+// epilogue warps: one per TMEM lane quarter up to 32 rows, two above (token
+// halves)
+__host__ __device__ constexpr int gemm_nepi(int MT) { return MT <= 32 ? 4 : 8; }
+__host__ __device__ constexpr int gemm_threads(int MT) { return (EPI0 + gemm_nepi(MT)) * 32; }
 constexpr int TMEM_COLS = 512;                // one block per SM owns all of TMEM
 constexpr int MAX_NA = 4;                     // A buffers (widened weight tiles) in TMEM
 constexpr int MAX_ND = 16;                    // accumulator slots in TMEM
@@ -134,16 +135,25 @@ __device__ __forceinline__ int cta_of_tile(int t, int T, int grid) {
     return (int)((((long long)t + 1) * grid - 1) / T);
 }
 
-// Eight 4-bit codes -> four fp16x2 (64 + q).  Nibble i of w holds feature
-// 2 * (i & 3) + (i >> 2) of an 8-feature run, so that the four results are
-// the features (0,1) (2,3) (4,5) (6,7): a code at bits 4..7 of a 16-bit half
+// Eight 4-bit codes (byte b: features b and b + 4) -> the e4m3 bytes of
+// features 0..3 and 4..7.
+__device__ __forceinline__ void widen_w4_e4(uint32_t w, uint32_t *o) {
+    o[0] = w & 0x0F0F0F0Fu;
+    o[1] = (w >> 4) & 0x0F0F0F0Fu;
+}
+
+// Eight 4-bit codes (byte b: features b and b + 4) -> four fp16x2 (64 + q),
+// features (0,1) (2,3) (4,5) (6,7): a code at bits 4..7 of a 16-bit half
 // under the exponent bits 0x5400 (fp16 64, ulp 1/16) reads 64 + q.
-__device__ __forceinline__ void widen_w4(uint32_t w, uint32_t *o) {
+__device__ __forceinline__ void widen_w4_f16(uint32_t w, uint32_t *o) {
     constexpr uint32_t M4 = 0x00F000F0u, E64 = 0x54005400u;
-    o[0] = ((w << 4) & M4) | E64;
-    o[1] = (w & M4) | E64;
-    o[2] = ((w >> 4) & M4) | E64;
-    o[3] = ((w >> 8) & M4) | E64;
+    uint32_t y01, y23;  // bytes (0, -, 1, -) and (2, -, 3, -)
+    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(y01) : "r"(w));
+    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(y23) : "r"(w));
+    o[0] = ((y01 << 4) & M4) | E64;  // features 0, 1
+    o[1] = ((y23 << 4) & M4) | E64;  // 2, 3
+    o[2] = (y01 & M4) | E64;         // 4, 5
+    o[3] = (y23 & M4) | E64;         // 6, 7
 }
 
 // Four int8 codes -> two fp16x2 q: bias to unsigned, place under the fp16
@@ -170,39 +180,20 @@ struct RingPos {
     }
 };
 
-// The KS MMAs (K = 16 each) of one quantization group, from one unrolled
-// sequence: A advances 8 TMEM columns per step, B 32 * MT bytes (two core
-// matrices of 8 features x MT rows).
-template <int KS, int MT>
-__device__ __forceinline__ void issue_group(uint32_t d_tm, uint32_t a_tm, uint64_t bdesc, uint32_t idesc) {
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-        tc_mma_f16_ts(d_tm, a_tm + (uint32_t)(ks * 8), bdesc + (uint64_t)((ks * 32 * MT) >> 4), idesc, ks > 0 ? 1u : 0u);
-}
-
-template <int MH>
-__device__ __forceinline__ void tmem_ld_tokens(uint32_t taddr, float *v) {
-    if constexpr (MH == 8) {
-        tmem_ld8(taddr, v);
-    } else if constexpr (MH == 16) {
-        tmem_ld16(taddr, v);
-    } else if constexpr (MH == 32) {
-        tmem_ld32(taddr, v);
-    } else {
-        tmem_ld32(taddr, v);
-        tmem_ld32(taddr + 32, v + 32);
-    }
-}
-
-// CHECK: also write the exact integer partial sums (check mode).
-template <int FMT, int MT, bool CHECK>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs a) {
-    constexpr int MH = MT / 2;          // tokens per epilogue thread
-    constexpr int CH = MH < 32 ? MH : 32;  // tokens per tensor-memory load
+// E4: the kind::f8f6f4 path (4-bit weights, digit-encoded operand); CHECK:
+// also write the exact integer partial sums (check mode).
+template <int FMT, int MT, bool E4, bool CHECK>
+__global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmArgs a) {
+    constexpr int NEPI = gemm_nepi(MT);
+    constexpr int MH = NEPI == 4 ? MT : MT / 2;  // tokens per epilogue thread
+    constexpr int CH = MH < 32 ? MH : 32;        // tokens per tensor-memory load
+    constexpr int BROWS = E4 ? 2 * MT : MT;      // rows of the B operand (the MMA's N)
+    constexpr int DC = BROWS;                    // TMEM columns of one group's accumulator
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    const int S = a.stages, NA = a.na, ND = a.nd;
+    const int S = a.stages, NA = a.na, ND = a.nd, U = a.U, V = a.V;
+    const int vmask = V - 1;  // V is a power of two
     const int KT = a.KT, GPT = a.GPT, G = a.G;
-    const int KSTEPS_G = G / 16;  // MMAs per group
+    const int KSTEPS_G = E4 ? G / 32 : G / 16;  // MMAs per group
     // barriers and flags first, the stage ring after
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
     uint64_t *empty = full + MAX_STAGES;
@@ -220,8 +211,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
     const int t0 = range_begin(a, blockIdx.x);
     const int t1 = range_begin(a, blockIdx.x + 1);
     const int ntl = t1 - t0;
+    const int nunits = (ntl + U - 1) / U;
+    const int ngroups = ntl * GPT;  // groups of the block, in the order they are computed
     int *err = reinterpret_cast<int *>(a.ws);
-    const uint32_t tx_bytes = (uint32_t)(a.tile_bytes + a.act_bytes + a.s_bytes);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -255,10 +247,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
     const int zb = (t1 - 1) / KTILES;
     const bool zeroer = !det && ntl > 0 && zb * KTILES >= t0 && (zb + 1) * KTILES > t1;
     int *ctr = reinterpret_cast<int *>(a.ws + ws_counter_offset());
-    const int acols = KT / 2;          // TMEM columns of one A buffer
-    const int dcol0 = NA * acols;      // first accumulator column
-    const int quarter = warp & 3;      // TMEM lanes 32 * quarter .. (widening and epilogue warps)
-    const int n = quarter * 32 + lane; // channel within the tile
+    const int acols = E4 ? KT / 4 : KT / 2;  // TMEM columns of one tile's A operand
+    const int dcol0 = NA * U * acols;         // first accumulator column
+    const int quarter = warp & 3;             // TMEM lanes 32 * quarter .. (widening and epilogue warps)
+    const int n = quarter * 32 + lane;        // channel within the tile
     const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
 
     if (warp == 0) {
@@ -266,14 +258,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
-            auto copy_acts = [&](int i, int st) {
-                const int kt = (t0 + i) % KTILES;
+            auto unit_tiles = [&](int u) { return ntl - u * U < U ? ntl - u * U : U; };
+            auto copy_weights = [&](int u, int st) {
+                const uint32_t fb = smem_addr(&full[st]);
+                const int nt = unit_tiles(u);
+                mbar_arrive_expect_tx(fb, (uint32_t)(nt * (a.tile_bytes + a.act_bytes + a.s_bytes)));
+                // the unit's tiles are consecutive in the blob
+                bulk_copy_g2s(smem_addr(ring + (size_t)st * a.stage_bytes),
+                              a.blob + (size_t)(t0 + u * U) * (size_t)a.tile_bytes, (uint32_t)(nt * a.tile_bytes), fb,
+                              pol_w);
+            };
+            auto copy_acts = [&](int u, int st) {
                 uint8_t *stage = ring + (size_t)st * a.stage_bytes;
                 const uint32_t fb = smem_addr(&full[st]);
-                bulk_copy_g2s(smem_addr(stage + a.act_off), a.qop + (size_t)kt * a.act_bytes, (uint32_t)a.act_bytes,
-                              fb, pol_a);
-                bulk_copy_g2s(smem_addr(stage + a.act_off + a.act_bytes),
-                              a.qop + a.op_s_offset + (size_t)kt * a.s_bytes, (uint32_t)a.s_bytes, fb, pol_a);
+                for (int j = 0; j < unit_tiles(u); ++j) {
+                    const int kt = (t0 + u * U + j) % KTILES;
+                    bulk_copy_g2s(smem_addr(stage + a.act_off + j * a.act_bytes), a.qop + (size_t)kt * a.act_bytes,
+                                  (uint32_t)a.act_bytes, fb, pol_a);
+                    bulk_copy_g2s(smem_addr(stage + a.s_off + j * a.s_bytes),
+                                  a.qop + a.op_s_offset + (size_t)kt * a.s_bytes, (uint32_t)a.s_bytes, fb, pol_a);
+                }
             };
             // Accumulating mode: after the copies of a tile that ends a split
             // segment, count this block into the n-block's counter (acquire),
@@ -300,122 +304,151 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
                 st_release_cta_shared(smem_addr(&sflag[nsplit]), 1);
                 ++nsplit;
             };
-            int i = 0;
-            for (; i < ntl && i < S && i < PREFETCH_STAGES; ++i) {
-                const uint32_t fb = smem_addr(&full[i]);
-                mbar_arrive_expect_tx(fb, tx_bytes);
-                bulk_copy_g2s(smem_addr(ring + (size_t)i * a.stage_bytes),
-                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
-            }
+            auto check_unit = [&](int u) {
+                for (int j = 0; j < unit_tiles(u); ++j) check(u * U + j);
+            };
+            int u = 0;
+            for (; u < nunits && u < S && u < PREFETCH_STAGES; ++u) copy_weights(u, u);
             pdl_wait();
-            for (int j = 0; j < i; ++j) copy_acts(j, j);
+            for (int j = 0; j < u; ++j) copy_acts(j, j);
             if (!det)
-                for (int j = 0; j < i; ++j) check(j);
-            RingPos ps{i % S, (uint32_t)((i / S) & 1)};
-            for (; i < ntl; ++i) {
+                for (int j = 0; j < u; ++j) check_unit(j);
+            RingPos ps{u % S, (uint32_t)((u / S) & 1)};
+            for (; u < nunits; ++u) {
                 const int st = ps.slot;
-                if (!mbar_wait_sleep(smem_addr(&empty[st]), ps.phase ^ 1u, err, WAIT_SLEEP_NS)) break;
-                const uint32_t fb = smem_addr(&full[st]);
-                mbar_arrive_expect_tx(fb, tx_bytes);
-                bulk_copy_g2s(smem_addr(ring + (size_t)st * a.stage_bytes),
-                              a.blob + (size_t)(t0 + i) * (size_t)a.tile_bytes, (uint32_t)a.tile_bytes, fb, pol_w);
-                copy_acts(i, st);
-                if (!det) check(i);
+                if (!mbar_wait_bounded(smem_addr(&empty[st]), ps.phase ^ 1u, err)) break;
+                copy_weights(u, st);
+                copy_acts(u, st);
+                if (!det) check_unit(u);
                 ps.next(S);
             }
             // No copy may still be landing in shared memory when the block exits.
-            const int issued = i;
+            const int issued = u;
             for (int j = issued > S ? issued - S : 0; j < issued; ++j)
                 mbar_wait_bounded(smem_addr(&full[j % S]), (uint32_t)((j / S) & 1), err);
         }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer ---
-        const uint32_t idesc = tc_idesc_f16(128, MT);
+        const uint32_t idesc = tc_idesc_f16(128, BROWS);
         // descriptor of the first stage's activation blocks; stage st adds
         // st * stage_bytes (the start address field counts 16-byte units)
-        const uint64_t bdesc_ring = tc_smem_desc(smem_addr(ring + a.act_off), 16u * MT, 128u);
+        const uint64_t bdesc_ring = tc_smem_desc(smem_addr(ring + a.act_off), 16u * BROWS, 128u);
         const uint32_t stage_units = (uint32_t)(a.stage_bytes >> 4);
-        // One elected lane waits and issues; the other lanes only keep the
-        // warp's ring positions in step.
+        const uint32_t tile_act_units = (uint32_t)(a.act_bytes >> 4);
+        const uint32_t group_b_units = (uint32_t)((KSTEPS_G * 32 * BROWS) >> 4);
+        // The whole warp runs the loop (all values warp-uniform) and waits;
+        // one elected lane issues each MMA and commit through a predicate.
+        // The unit's stage needs no wait of its own: its A buffer is widened
+        // only after the stage has landed.
+        __syncwarp();
+        const uint32_t leader = elect_one() ? 1u : 0u;
         bool ok = true;
         RingPos ps{0, 0u}, pa{0, 0u}, pd{0, 0u};
-        for (int i = 0; i < ntl; ++i) {
-            const uint32_t a_tm = tbase + (uint32_t)(pa.slot * acols);
+        int g = 0;  // groups issued so far
+        for (int u = 0; u < nunits; ++u) {
+            const int nt = ntl - u * U < U ? ntl - u * U : U;
+            const uint32_t a_tm = tbase + (uint32_t)(pa.slot * U * acols);
             const uint64_t bdesc = bdesc_ring + (uint64_t)(ps.slot * stage_units);
-            __syncwarp();
-            if (elect_one()) {
-                if (ok) ok = mbar_wait_bounded(smem_addr(&full[ps.slot]), ps.phase, err);
-                if (ok) ok = mbar_wait_bounded(smem_addr(&a_full[pa.slot]), pa.phase, err);
-                RingPos pg = pd;
-                for (int gl = 0; gl < GPT; ++gl) {
-                    if (ok) ok = mbar_wait_bounded(smem_addr(&d_empty[pg.slot]), pg.phase ^ 1u, err);
-                    tc_fence_after();
-                    const uint32_t d_tm = tbase + (uint32_t)(dcol0 + pg.slot * MT);
-                    const uint32_t a_g = a_tm + (uint32_t)(gl * KSTEPS_G * 8);
-                    const uint64_t b_g = bdesc + (uint64_t)((gl * KSTEPS_G * 32 * MT) >> 4);
-                    switch (KSTEPS_G) {
-                        case 1: issue_group<1, MT>(d_tm, a_g, b_g, idesc); break;
-                        case 2: issue_group<2, MT>(d_tm, a_g, b_g, idesc); break;
-                        case 4: issue_group<4, MT>(d_tm, a_g, b_g, idesc); break;
-                        case 8: issue_group<8, MT>(d_tm, a_g, b_g, idesc); break;
-                        default: issue_group<16, MT>(d_tm, a_g, b_g, idesc); break;
+            if (ok) ok = mbar_wait_bounded(smem_addr(&a_full[pa.slot]), pa.phase, err);
+            tc_fence_after();
+            for (int j = 0; j < nt; ++j) {
+                for (int gl = 0; gl < GPT; ++gl, ++g) {
+                    const int r = g & vmask;
+                    if (r == 0) {
+                        if (ok) ok = mbar_wait_bounded(smem_addr(&d_empty[pd.slot]), pd.phase ^ 1u, err);
+                        tc_fence_after();
                     }
-                    tc_commit(smem_addr(&d_full[pg.slot]));
-                    pg.next(ND);
+                    const uint32_t d_tm = tbase + (uint32_t)(dcol0 + (pd.slot * V + r) * DC);
+                    const uint32_t a_g = a_tm + (uint32_t)(j * acols + gl * KSTEPS_G * 8);
+                    uint64_t b_g = bdesc + (uint64_t)(j * tile_act_units + gl * group_b_units);
+                    for (int ks = 0; ks < KSTEPS_G; ++ks) {
+                        if (E4)
+                            tc_mma_e4m3_ts_if(leader, d_tm, a_g + (uint32_t)(ks * 8), b_g, idesc, ks > 0 ? 1u : 0u);
+                        else
+                            tc_mma_f16_ts_if(leader, d_tm, a_g + (uint32_t)(ks * 8), b_g, idesc, ks > 0 ? 1u : 0u);
+                        b_g += (uint64_t)((32 * BROWS) >> 4);
+                    }
+                    if (r == vmask || g == ngroups - 1) {
+                        tc_commit_if(leader, smem_addr(&d_full[pd.slot]));
+                        pd.next(ND);
+                    }
                 }
-                tc_commit(smem_addr(&a_empty[pa.slot]));
-                tc_commit(smem_addr(&empty[ps.slot]));
             }
-            __syncwarp();
-            for (int gl = 0; gl < GPT; ++gl) pd.next(ND);
+            tc_commit_if(leader, smem_addr(&a_empty[pa.slot]));
+            tc_commit_if(leader, smem_addr(&empty[ps.slot]));
             ps.next(S);
             pa.next(NA);
         }
         // every MMA has completed before the block frees TMEM
-        __syncwarp();
-        if (elect_one()) tc_commit(smem_addr(done_bar));
-        __syncwarp();
+        tc_commit_if(leader, smem_addr(done_bar));
         mbar_wait_bounded(smem_addr(done_bar), 0u, err);
     } else if (warp < EPI0) {
         // ----------------------------------------------------- widening ---
         const int KC = KT / 64;  // 64-feature chunks per tile
         bool ok = true;
         RingPos ps{0, 0u}, pa{0, 0u};
-        for (int i = 0; i < ntl; ++i) {
+        for (int u = 0; u < nunits; ++u) {
+            const int nt = ntl - u * U < U ? ntl - u * U : U;
             const int st = ps.slot, ab = pa.slot;
-            if (ok) ok = mbar_wait_sleep(smem_addr(&full[st]), ps.phase, err, WAIT_SLEEP_NS);
-            if (ok) ok = mbar_wait_sleep(smem_addr(&a_empty[ab]), pa.phase ^ 1u, err, WAIT_SLEEP_NS);
+            if (ok) ok = mbar_wait_bounded(smem_addr(&full[st]), ps.phase, err);
+            if (ok) ok = mbar_wait_bounded(smem_addr(&a_empty[ab]), pa.phase ^ 1u, err);
             __syncwarp();
             tc_fence_after();
-            const uint8_t *tile = ring + (size_t)st * a.stage_bytes;
-            for (int c = 0; c < KC; ++c) {
-                uint32_t v[32];
-                if (FMT == HQ_W4_ASYM) {
-                    uint4 u[2];
+            for (int j = 0; j < nt; ++j) {
+                const uint8_t *tile = ring + (size_t)st * a.stage_bytes + (size_t)j * a.tile_bytes;
+                const uint32_t a_col = (uint32_t)((ab * U + j) * acols);
+                if (E4) {
+                    // 64 features -> 16 columns of e4m3 bytes; one store per 128 features
+                    for (int c = 0; c < KC; c += 2) {
+                        uint32_t v[32];
 #pragma unroll
-                    for (int p = 0; p < 2; ++p)
-                        u[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 2 + p) * BN + n) * 16);
+                        for (int cc = 0; cc < 2; ++cc) {
+                            uint4 uu[2];
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        widen_w4(u[p].x, v + 16 * p + 0);
-                        widen_w4(u[p].y, v + 16 * p + 4);
-                        widen_w4(u[p].z, v + 16 * p + 8);
-                        widen_w4(u[p].w, v + 16 * p + 12);
+                            for (int p = 0; p < 2; ++p)
+                                uu[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)((c + cc) * 2 + p) * BN + n) * 16);
+#pragma unroll
+                            for (int p = 0; p < 2; ++p) {
+                                uint32_t *o = v + 16 * cc + 8 * p;
+                                widen_w4_e4(uu[p].x, o + 0);
+                                widen_w4_e4(uu[p].y, o + 2);
+                                widen_w4_e4(uu[p].z, o + 4);
+                                widen_w4_e4(uu[p].w, o + 6);
+                            }
+                        }
+                        tmem_st32(tbase + lane_field + a_col + (uint32_t)(c * 16), v);
                     }
                 } else {
-                    uint4 u[4];
+                    for (int c = 0; c < KC; ++c) {
+                        uint32_t v[32];
+                        if (FMT == HQ_W4_ASYM) {
+                            uint4 uu[2];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        u[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 4 + p) * BN + n) * 16);
+                            for (int p = 0; p < 2; ++p)
+                                uu[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 2 + p) * BN + n) * 16);
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        widen_i8(u[p].x, v + 8 * p + 0);
-                        widen_i8(u[p].y, v + 8 * p + 2);
-                        widen_i8(u[p].z, v + 8 * p + 4);
-                        widen_i8(u[p].w, v + 8 * p + 6);
+                            for (int p = 0; p < 2; ++p) {
+                                widen_w4_f16(uu[p].x, v + 16 * p + 0);
+                                widen_w4_f16(uu[p].y, v + 16 * p + 4);
+                                widen_w4_f16(uu[p].z, v + 16 * p + 8);
+                                widen_w4_f16(uu[p].w, v + 16 * p + 12);
+                            }
+                        } else {
+                            uint4 uu[4];
+#pragma unroll
+                            for (int p = 0; p < 4; ++p)
+                                uu[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 4 + p) * BN + n) * 16);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                widen_i8(uu[p].x, v + 8 * p + 0);
+                                widen_i8(uu[p].y, v + 8 * p + 2);
+                                widen_i8(uu[p].z, v + 8 * p + 4);
+                                widen_i8(uu[p].w, v + 8 * p + 6);
+                            }
+                        }
+                        tmem_st32(tbase + lane_field + a_col + (uint32_t)(c * 32), v);
                     }
                 }
-                tmem_st32(tbase + lane_field + (uint32_t)(ab * acols + c * 32), v);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -430,7 +463,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
     } else {
         // ----------------------------------------------------- epilogue ---
         pdl_wait();
-        const int mt = threadIdx.x - EPI0 * 32;  // epilogue thread 0..255
+        const int mt = threadIdx.x - EPI0 * 32;  // epilogue thread 0..NEPI*32-1
         const int h = (warp - EPI0) >> 2;        // token half
         const int M = a.M, N = a.N;
         float *wsp = reinterpret_cast<float *>(a.ws + ws_partial_offset());
@@ -450,118 +483,143 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
         }
 
         RingPos ps{0, 0u}, pd{0, 0u};
+        int g = 0;  // groups folded so far
         // position of the tile being folded: n-block eb, K tile ekt
         int eb = t0 / KTILES, ekt = t0 - eb * KTILES, seg_k0 = ekt;
-        for (int i = 0; i < ntl; ++i) {
+        for (int u = 0; u < nunits; ++u) {
+            const int nt = ntl - u * U < U ? ntl - u * U : U;
             const int st = ps.slot;
-            if (i == 0 || ekt == 0) {
-                seg_k0 = ekt;
-#pragma unroll
-                for (int t = 0; t < MH; ++t) y[t] = 0.0f;
-            }
             // the stage's scales, zero points and group sums are read below
-            if (ok) ok = mbar_wait_sleep(smem_addr(&full[st]), ps.phase, err, WAIT_SLEEP_NS);
-            const uint8_t *tile = ring + (size_t)st * a.stage_bytes;
-            const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes) + (size_t)n * GPT;
-            const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;
-            const float *tS = reinterpret_cast<const float *>(tile + a.act_off + a.act_bytes);
-            for (int gl = 0; gl < GPT; ++gl) {
-                const int slot = pd.slot;
-                if (ok) ok = mbar_wait_sleep(smem_addr(&d_full[slot]), pd.phase, err, WAIT_SLEEP_NS);
-                __syncwarp();
-                tc_fence_after();
-                const float sc = tsc[gl];
-                float nz = 0.0f;
-                if (FMT == HQ_W4_ASYM) {
-                    const int zi = n * GPT + gl;
-                    const uint32_t zb8 = tzp[zi >> 1];
-                    nz = -(float)(64u + ((zi & 1) ? (zb8 >> 4) : (zb8 & 15u)));
+            if (ok) ok = mbar_wait_bounded(smem_addr(&full[st]), ps.phase, err);
+            for (int j = 0; j < nt; ++j) {
+                const int i = u * U + j;
+                if (i == 0 || ekt == 0) {
+                    seg_k0 = ekt;
+#pragma unroll
+                    for (int t = 0; t < MH; ++t) y[t] = 0.0f;
                 }
-                const f2 nz2 = f2_make(nz, nz);
-                const float *Sg = tS + gl * MT + h * MH;
+                const uint8_t *tile = ring + (size_t)st * a.stage_bytes + (size_t)j * a.tile_bytes;
+                const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes) + (size_t)n * GPT;
+                const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;
+                const float *tS = reinterpret_cast<const float *>(ring + (size_t)st * a.stage_bytes + a.s_off +
+                                                                  (size_t)j * a.s_bytes);
+                for (int gl = 0; gl < GPT; ++gl, ++g) {
+                    const int r = g & vmask;
+                    if (r == 0) {
+                        if (ok) ok = mbar_wait_bounded(smem_addr(&d_full[pd.slot]), pd.phase, err);
+                        __syncwarp();
+                        tc_fence_after();
+                    }
+                    const float sc = tsc[gl];
+                    float nz = 0.0f;
+                    if (FMT == HQ_W4_ASYM) {
+                        const int zi = n * GPT + gl;
+                        const uint32_t zb8 = tzp[zi >> 1];
+                        const float z = (float)((zi & 1) ? (zb8 >> 4) : (zb8 & 15u));
+                        // E4: in units of 2^-9 (the accumulators hold 2^-9 sum q d)
+                        nz = E4 ? -z * (1.0f / 512.0f) : -(64.0f + z);
+                    }
+                    const f2 nz2 = f2_make(nz, nz);
+                    const float scale = E4 ? sc * 512.0f : sc;  // exact: a power-of-two multiple
+                    const float *Sg = tS + gl * MT + h * MH;
 #pragma unroll
-                for (int c0 = 0; c0 < MH; c0 += CH) {
-                    float acc[CH];
-                    const uint32_t taddr = tbase + lane_field + (uint32_t)(dcol0 + slot * MT + h * MH + c0);
-                    if constexpr (CH == 8)
-                        tmem_ld8(taddr, acc);
-                    else if constexpr (CH == 16)
-                        tmem_ld16(taddr, acc);
-                    else
-                        tmem_ld32(taddr, acc);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int p = 0; p < CH / 2; ++p) {
-                        float p0 = acc[2 * p], p1 = acc[2 * p + 1];
-                        if (FMT == HQ_W4_ASYM) {
-                            // exact: P = sum qx (64 + q) - (64 + z) S, integers below 2^24
-                            const float2 sv = *reinterpret_cast<const float2 *>(Sg + c0 + 2 * p);
-                            f2_split(f2_fma(nz2, f2_make(sv.x, sv.y), f2_make(p0, p1)), p0, p1);
+                    for (int c0 = 0; c0 < MH; c0 += CH) {
+                        float acc[CH], acc_h[E4 ? CH : 1];
+                        const uint32_t taddr =
+                            tbase + lane_field + (uint32_t)(dcol0 + (pd.slot * V + r) * DC + h * MH + c0);
+                        if constexpr (CH == 8) {
+                            tmem_ld8(taddr, acc);
+                            if constexpr (E4) tmem_ld8(taddr + MT, acc_h);
+                        } else if constexpr (CH == 16) {
+                            tmem_ld16(taddr, acc);
+                            if constexpr (E4) tmem_ld16(taddr + MT, acc_h);
+                        } else {
+                            tmem_ld32(taddr, acc);
+                            if constexpr (E4) tmem_ld32(taddr + MT, acc_h);
                         }
-                        const int tok = h * MH + c0 + 2 * p;
-                        if (CHECK) {
-                            const int gg = ekt * GPT + gl;
-                            const int nn = eb * BN + n;
-                            if (gg < a.NGK && nn < N) {
-                                if (tok < M) a.partials[((size_t)tok * N + nn) * a.NGK + gg] = __float2int_rn(p0);
-                                if (tok + 1 < M) a.partials[((size_t)(tok + 1) * N + nn) * a.NGK + gg] = __float2int_rn(p1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int p = 0; p < CH / 2; ++p) {
+                            f2 P2 = f2_make(acc[2 * p], acc[2 * p + 1]);
+                            if constexpr (E4)  // low digit + 16 x high digit (exact)
+                                P2 = f2_fma(f2_make(16.0f, 16.0f), f2_make(acc_h[2 * p], acc_h[2 * p + 1]), P2);
+                            if (FMT == HQ_W4_ASYM) {
+                                // exact: P = sum qx q' - (z or 64 + z) S, below 2^24 units
+                                const float2 sv = *reinterpret_cast<const float2 *>(Sg + c0 + 2 * p);
+                                P2 = f2_fma(nz2, f2_make(sv.x, sv.y), P2);
                             }
+                            float p0, p1;
+                            f2_split(P2, p0, p1);
+                            const int tok = h * MH + c0 + 2 * p;
+                            if (CHECK) {
+                                const int gq = ekt * GPT + gl;
+                                const int nn = eb * BN + n;
+                                const float uu = E4 ? 512.0f : 1.0f;
+                                if (gq < a.NGK && nn < N) {
+                                    if (tok < M) a.partials[((size_t)tok * N + nn) * a.NGK + gq] = __float2int_rn(p0 * uu);
+                                    if (tok + 1 < M)
+                                        a.partials[((size_t)(tok + 1) * N + nn) * a.NGK + gq] = __float2int_rn(p1 * uu);
+                                }
+                            }
+                            // y += scale * P: product rounded, then sum rounded
+                            y[c0 + 2 * p] = __fadd_rn(y[c0 + 2 * p], __fmul_rn(scale, p0));
+                            y[c0 + 2 * p + 1] = __fadd_rn(y[c0 + 2 * p + 1], __fmul_rn(scale, p1));
                         }
-                        // y += scale * P: product rounded, then sum rounded
-                        y[c0 + 2 * p] = __fadd_rn(y[c0 + 2 * p], __fmul_rn(sc, p0));
-                        y[c0 + 2 * p + 1] = __fadd_rn(y[c0 + 2 * p + 1], __fmul_rn(sc, p1));
+                    }
+                    if (r == vmask || g == ngroups - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_addr(&d_empty[pd.slot]));
+                        pd.next(ND);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&d_empty[slot]));
-                pd.next(ND);
+
+                // end of an n-block segment?
+                if (ekt == KTILES - 1 || i == ntl - 1) {
+                    const int nn = eb * BN + n;
+                    if (seg_k0 == 0 && ekt == KTILES - 1) {
+                        // the whole K range of the n-block: write Y
+#pragma unroll
+                        for (int t = 0; t < MH; ++t) {
+                            const int tok = h * MH + t;
+                            if (tok < M && nn < N) a.Y[(size_t)tok * N + nn] = __fmul_rn(__ldg(a.sx + tok), y[t]);
+                        }
+                    } else if (det) {
+                        // part of the K range: publish the partial sums now,
+                        // count the arrival once this block's tiles are all done
+                        const int slot = eb == first_b ? 0 : 1;
+                        float *mys = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats();
+#pragma unroll
+                        for (int t = 0; t < MH; ++t) {
+                            const int tok = h * MH + t;
+                            if (tok < M) __stcg(mys + (size_t)tok * BN + n, y[t]);
+                        }
+                        if (slot == 0)
+                            pend0 = eb;
+                        else
+                            pend1 = eb;
+                    } else {
+                        // part of the K range, accumulating mode: once the
+                        // zeroing is visible (the segment's flag), add sx *
+                        // (this block's sum) into Y
+                        if (ok) ok = wait_flag_bounded(smem_addr(&sflag[nsplit]), err);
+                        ++nsplit;
+#pragma unroll
+                        for (int t = 0; t < MH; ++t) {
+                            const int tok = h * MH + t;
+                            if (tok < M && nn < N)
+                                atomicAdd(a.Y + (size_t)tok * N + nn, __fmul_rn(__ldg(a.sx + tok), y[t]));
+                        }
+                    }
+                }
+                if (++ekt == KTILES) {
+                    ekt = 0;
+                    ++eb;
+                }
             }
             // this warp no longer reads the stage
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-
-            // end of an n-block segment?
-            if (ekt == KTILES - 1 || i == ntl - 1) {
-                const int nn = eb * BN + n;
-                if (seg_k0 == 0 && ekt == KTILES - 1) {
-                    // the whole K range of the n-block: write Y
-#pragma unroll
-                    for (int t = 0; t < MH; ++t) {
-                        const int tok = h * MH + t;
-                        if (tok < M && nn < N) a.Y[(size_t)tok * N + nn] = __fmul_rn(__ldg(a.sx + tok), y[t]);
-                    }
-                } else if (det) {
-                    // part of the K range: publish the partial sums now, count
-                    // the arrival once this block's tiles are all done
-                    const int slot = eb == first_b ? 0 : 1;
-                    float *mys = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats();
-#pragma unroll
-                    for (int t = 0; t < MH; ++t) {
-                        const int tok = h * MH + t;
-                        if (tok < M) __stcg(mys + (size_t)tok * BN + n, y[t]);
-                    }
-                    if (slot == 0)
-                        pend0 = eb;
-                    else
-                        pend1 = eb;
-                } else {
-                    // part of the K range, accumulating mode: once the zeroing
-                    // is visible (the segment's flag), add sx * (this block's
-                    // sum) into Y
-                    if (ok) ok = wait_flag_bounded(smem_addr(&sflag[nsplit]), err);
-                    ++nsplit;
-#pragma unroll
-                    for (int t = 0; t < MH; ++t) {
-                        const int tok = h * MH + t;
-                        if (tok < M && nn < N) atomicAdd(a.Y + (size_t)tok * N + nn, __fmul_rn(__ldg(a.sx + tok), y[t]));
-                    }
-                }
-            }
-            if (++ekt == KTILES) {
-                ekt = 0;
-                ++eb;
-            }
             ps.next(S);
         }
 
@@ -572,6 +630,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
             const int nc = cta_of_tile(zb * KTILES + KTILES - 1, a.T, a.grid) - cta_of_tile(zb * KTILES, a.T, a.grid) + 1;
             if (mark_old == nc - 1) atomicExch(&ctr[zb], 0);
         }
+
         // Split n-blocks, deterministic mode: every contributor arrives,
         // waits until all contributors of the n-block have arrived, then sums
         // its 1/nc share of the n-block's outputs over all contributors'
@@ -702,9 +761,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_verify_gemm(const GemmArgs 
 }
 
 // Launch one instance.
-template <int FMT, int MT, bool CHECK>
+template <int FMT, int MT, bool E4, bool CHECK>
 cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
-    auto kern = k_verify_gemm<FMT, MT, CHECK>;
+    auto kern = k_verify_gemm<FMT, MT, E4, CHECK>;
     size_t smem = 2048 + (size_t)a.stages * (size_t)a.stage_bytes;
     if (smem < (size_t)MIN_GEMM_SMEM) smem = MIN_GEMM_SMEM;
     int dev = 0;
@@ -719,7 +778,7 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.grid);
-    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.blockDim = dim3(gemm_threads(MT));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -730,23 +789,29 @@ cudaError_t launch_gemm_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int FMT>
-cudaError_t launch_gemm_fmt(const GemmArgs &a, bool pdl, cudaStream_t s) {
+template <int FMT, bool CHECK>
+cudaError_t launch_gemm_check(const GemmArgs &a, bool pdl, cudaStream_t s) {
     const int mt = act_rows(a.M);
-    if (a.partials) {
-        switch (mt) {
-            case 16: return launch_gemm_instance<FMT, 16, true>(a, pdl, s);
-            case 32: return launch_gemm_instance<FMT, 32, true>(a, pdl, s);
-            case 64: return launch_gemm_instance<FMT, 64, true>(a, pdl, s);
-            default: return launch_gemm_instance<FMT, 128, true>(a, pdl, s);
+    if constexpr (FMT == HQ_W4_ASYM) {
+        if (act_e4(FMT, a.M, a.G)) {
+            switch (mt) {
+                case 16: return launch_gemm_instance<FMT, 16, true, CHECK>(a, pdl, s);
+                case 32: return launch_gemm_instance<FMT, 32, true, CHECK>(a, pdl, s);
+                default: return launch_gemm_instance<FMT, 64, true, CHECK>(a, pdl, s);
+            }
         }
     }
     switch (mt) {
-        case 16: return launch_gemm_instance<FMT, 16, false>(a, pdl, s);
-        case 32: return launch_gemm_instance<FMT, 32, false>(a, pdl, s);
-        case 64: return launch_gemm_instance<FMT, 64, false>(a, pdl, s);
-        default: return launch_gemm_instance<FMT, 128, false>(a, pdl, s);
+        case 16: return launch_gemm_instance<FMT, 16, false, CHECK>(a, pdl, s);
+        case 32: return launch_gemm_instance<FMT, 32, false, CHECK>(a, pdl, s);
+        case 64: return launch_gemm_instance<FMT, 64, false, CHECK>(a, pdl, s);
+        default: return launch_gemm_instance<FMT, 128, false, CHECK>(a, pdl, s);
     }
+}
+
+template <int FMT>
+cudaError_t launch_gemm_fmt(const GemmArgs &a, bool pdl, cudaStream_t s) {
+    return a.partials ? launch_gemm_check<FMT, true>(a, pdl, s) : launch_gemm_check<FMT, false>(a, pdl, s);
 }
 
 cudaError_t launch_gemm_w4(const GemmArgs &a, bool pdl, cudaStream_t s);

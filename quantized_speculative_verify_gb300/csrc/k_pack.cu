@@ -137,13 +137,13 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
         const uint8_t *src = codes_s + r * KT;
         uint32_t wv[4];
         if (w4) {
-            // word j: features 32 cp + 8 j + e; nibble i = feature 2 (i & 3) + (i >> 2)
+            // word j: features 32 cp + 8 j + e; byte b = feature b | feature b + 4 << 4
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint8_t *p8 = src + cp * 32 + j * 8;
                 uint32_t word = 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) word |= (uint32_t)(p8[2 * (i & 3) + (i >> 2)] & 15u) << (4 * i);
+                for (int b = 0; b < 4; ++b) word |= ((uint32_t)(p8[b] & 15u) | ((uint32_t)(p8[b + 4] & 15u) << 4)) << (8 * b);
                 wv[j] = word;
             }
         } else {
@@ -179,8 +179,8 @@ __global__ void __launch_bounds__(256) k_unpack(Geom g, const uint8_t *__restric
         if (n >= g.N) continue;
         for (int j = 0; j < 4; ++j) {
             if (w4) {
-                for (int i = 0; i < 8; ++i) {
-                    const int k = kt * g.KT + cp * 32 + j * 8 + 2 * (i & 3) + (i >> 2);
+                for (int i = 0; i < 8; ++i) {  // nibble i: byte i / 2, feature (i / 2) + 4 (i % 2)
+                    const int k = kt * g.KT + cp * 32 + j * 8 + (i >> 1) + 4 * (i & 1);
                     if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
                 }
             } else {

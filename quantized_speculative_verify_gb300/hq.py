@@ -77,11 +77,11 @@ def load() -> ctypes.CDLL:
         "hq_version": (I32, []),
         "hq_packed_bytes": (SZ, [D]),
         "hq_workspace_bytes": (SZ, [D, I32]),
-        "hq_act_operand_bytes": (SZ, [I32, I32, I32]),
+        "hq_act_operand_bytes": (SZ, [D, I32]),
         "hq_make_signs": (ctypes.c_int, [U64, I32, P]),
         "hq_pack_weights": (ctypes.c_int, [D, P, P, P, P]),
         "hq_pack_weights_at": (ctypes.c_int, [D, I32, I32, P, P, P, P]),
-        "hq_rotate_quant_act": (ctypes.c_int, [P, I32, I32, I32, P, P, P, P, P, U32, P]),
+        "hq_rotate_quant_act": (ctypes.c_int, [D, P, I32, P, P, P, P, P, U32, P]),
         "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, I32, P, P, P, U32, P]),
         "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
         "hq_workspace_status": (ctypes.c_int, [P, P]),
@@ -157,8 +157,8 @@ def hq_workspace_bytes(desc: hq_layer_desc, M: int) -> int:
     return int(load().hq_workspace_bytes(ctypes.byref(desc), int(M)))
 
 
-def hq_act_operand_bytes(M: int, K: int, group: int) -> int:
-    return int(load().hq_act_operand_bytes(int(M), int(K), int(group)))
+def hq_act_operand_bytes(desc: hq_layer_desc, M: int) -> int:
+    return int(load().hq_act_operand_bytes(ctypes.byref(desc), int(M)))
 
 
 def hq_make_signs(seed: int, K: int) -> np.ndarray:
@@ -177,8 +177,8 @@ def hq_pack_weights_at(desc, n0: int, rows: int, W, signs, blob, stream=None) ->
                                      _stream(stream)), "hq_pack_weights_at")
 
 
-def hq_rotate_quant_act(X, M: int, K: int, group: int, signs, qx, gsum, qop, sx, flags: int = 0, stream=None) -> None:
-    _check(load().hq_rotate_quant_act(_ptr(X), int(M), int(K), int(group), _ptr(signs), _ptr(qx), _ptr(gsum),
+def hq_rotate_quant_act(desc, X, M: int, signs, qx, gsum, qop, sx, flags: int = 0, stream=None) -> None:
+    _check(load().hq_rotate_quant_act(ctypes.byref(desc), _ptr(X), int(M), _ptr(signs), _ptr(qx), _ptr(gsum),
                                       _ptr(qop), _ptr(sx), int(flags), _stream(stream)), "hq_rotate_quant_act")
 
 
@@ -297,11 +297,13 @@ def pack_fused(Ws: list, group: int, fmt, signs_host: np.ndarray, stream=None) -
     return FusedLayer(PackedLayer(desc, blob, signs), widths, offsets)
 
 
-def act_buffers(M: int, K: int, group: int, device, int8_codes: bool = True, group_sums: bool = False) -> tuple:
-    """(qx int8 [M][K] or None, gsum int32 [M][K/group] or None, GEMM activation operand (opaque bytes), sx fp32 [M])."""
+def act_buffers(desc: hq_layer_desc, M: int, device, int8_codes: bool = True, group_sums: bool = False) -> tuple:
+    """Buffers of hq_rotate_quant_act for M rows of the activations of layers like `desc`:
+    (qx int8 [M][K] or None, gsum int32 [M][K/group] or None, GEMM activation operand (opaque bytes), sx fp32 [M])."""
+    K, group = desc.K, desc.group
     qx = torch.empty((M, K), dtype=torch.int8, device=device) if int8_codes else None
     gsum = torch.empty((M, K // group), dtype=torch.int32, device=device) if group_sums else None
-    qop = torch.empty(hq_act_operand_bytes(M, K, group), dtype=torch.uint8, device=device)
+    qop = torch.empty(hq_act_operand_bytes(desc, M), dtype=torch.uint8, device=device)
     sx = torch.empty(M, dtype=torch.float32, device=device)
     return qx, gsum, qop, sx
 
@@ -328,11 +330,11 @@ def verify_linear(layer: PackedLayer, X: torch.Tensor, ws: torch.Tensor, Y: torc
     """Y = dequant(int GEMM(quant(rotate(X)), packed W)): the two kernels in sequence."""
     M, K = X.shape
     if bufs is None:
-        bufs = act_buffers(M, K, layer.group, X.device, int8_codes=False)
+        bufs = act_buffers(layer.desc, M, X.device, int8_codes=False)
     qx, gsum, qop, sx = bufs
     if Y is None:
         Y = torch.empty((M, layer.N), dtype=torch.float32, device=X.device)
-    hq_rotate_quant_act(X, M, K, layer.group, layer.signs, qx, gsum, qop, sx, flags & HQ_LAUNCH_PDL, stream)
+    hq_rotate_quant_act(layer.desc, X, M, layer.signs, qx, gsum, qop, sx, flags & HQ_LAUNCH_PDL, stream)
     hq_verify_gemm(layer.desc, layer.blob, qop, sx, M, Y, partials, ws, flags, stream)
     return Y
 

@@ -115,14 +115,18 @@ def test_K_above_the_activation_limit_is_invalid(K):
 
 def test_act_operand_bytes():
     # opaque, but its size follows from the rows padded to the MMA's N (16, 32,
-    # 64, 128), 128-feature blocks of fp16 codes and one fp32 sum per group and row
-    assert hq.hq_act_operand_bytes(16, 4096, 64) == 32 * 16 * 256 + 64 * 16 * 4
-    assert hq.hq_act_operand_bytes(3, 96, 32) == 1 * 16 * 256 + 4 * 16 * 4  # one padded block, its four groups
-    assert hq.hq_act_operand_bytes(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4
-    assert hq.hq_act_operand_bytes(128, 4096, 16) == 32 * 128 * 256 + 256 * 128 * 4
-    assert hq.hq_act_operand_bytes(0, 4096, 64) == 0
-    assert hq.hq_act_operand_bytes(129, 4096, 64) == 0 and hq.hq_act_operand_bytes(4, 100, 32) == 0
-    assert hq.hq_act_operand_bytes(4, 96, 64) == 0 and hq.hq_act_operand_bytes(4, 256, 48) == 0  # bad group
+    # 64, 128), 128-feature blocks of 2 bytes per code (fp16, or two e4m3
+    # digits) and one fp32 sum per group and row
+    def size(M, K, G, fmt="w4"):
+        return hq.hq_act_operand_bytes(hq.make_desc(K, 128, G, fmt), M)
+    assert size(16, 4096, 64) == 32 * 16 * 256 + 64 * 16 * 4
+    assert size(16, 4096, 64, "w8") == size(16, 4096, 64)  # both encodings have the same size
+    assert size(3, 96, 32) == 1 * 16 * 256 + 4 * 16 * 4  # one padded block, its four groups
+    assert size(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4
+    assert size(128, 4096, 16) == 32 * 128 * 256 + 256 * 128 * 4
+    assert size(0, 4096, 64) == 0 and size(129, 4096, 64) == 0
+    for bad in (hq.hq_layer_desc(100, 128, 32, 0), hq.hq_layer_desc(96, 128, 64, 0), hq.hq_layer_desc(256, 128, 48, 0)):
+        assert hq.hq_act_operand_bytes(bad, 4) == 0
 
 
 def test_workspace_bytes():
@@ -151,18 +155,17 @@ def test_invalid_arguments_are_rejected_before_launch():
     assert lib.hq_pack_weights(ctypes.byref(bad), FAKE, FAKE, FAKE, None) == E
     assert lib.hq_pack_weights(D, None, FAKE, FAKE, None) == E
     assert lib.hq_pack_weights(D, FAKE, FAKE, FAKE + 8, None) == E  # blob must be 16-byte aligned
-    # activations: (X, M, K, group, signs, qx, gsum, qop, sx, flags, stream)
-    assert lib.hq_rotate_quant_act(FAKE, 129, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, -1, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 100, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 48, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E  # group
-    assert lib.hq_rotate_quant_act(FAKE, 4, 96, 64, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E  # K % group
-    assert lib.hq_rotate_quant_act(None, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, None, None, None, FAKE, 0, None) == E  # no output
-    assert lib.hq_rotate_quant_act(FAKE + 4, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, None, FAKE + 8, FAKE, 0, None) == E  # operand
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 0, None) == E  # gsum
-    assert lib.hq_rotate_quant_act(FAKE, 4, 256, 32, FAKE, FAKE, None, FAKE, FAKE, 2, None) == E
+    # activations: (desc, X, M, signs, qx, gsum, qop, sx, flags, stream)
+    assert lib.hq_rotate_quant_act(D, FAKE, 129, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(D, FAKE, -1, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(ctypes.byref(bad), FAKE, 4, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(None, FAKE, 4, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(D, None, 4, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(D, FAKE, 4, FAKE, None, None, None, FAKE, 0, None) == E  # no output
+    assert lib.hq_rotate_quant_act(D, FAKE + 4, 4, FAKE, FAKE, None, FAKE, FAKE, 0, None) == E
+    assert lib.hq_rotate_quant_act(D, FAKE, 4, FAKE, FAKE, None, FAKE + 8, FAKE, 0, None) == E  # operand
+    assert lib.hq_rotate_quant_act(D, FAKE, 4, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 0, None) == E  # gsum
+    assert lib.hq_rotate_quant_act(D, FAKE, 4, FAKE, FAKE, None, FAKE, FAKE, 2, None) == E
     # gemm
     assert lib.hq_verify_gemm(D, FAKE, FAKE, FAKE, 129, FAKE, None, FAKE, 0, None) == E
     assert lib.hq_verify_gemm(D, None, FAKE, FAKE, 4, FAKE, None, FAKE, 0, None) == E
@@ -187,7 +190,7 @@ def test_empty_batch_is_a_no_op():
     lib = hq.load()
     d = hq.make_desc(256, 256, 32, "w4")
     # M = 0: nothing to do, nothing launched, pointers never touched
-    assert lib.hq_rotate_quant_act(None, 0, 256, 32, None, None, None, None, None, 0, None) == hq.HQ_OK
+    assert lib.hq_rotate_quant_act(ctypes.byref(d), None, 0, None, None, None, None, None, 0, None) == hq.HQ_OK
     assert lib.hq_verify_gemm(ctypes.byref(d), None, None, None, 0, None, None, None, 0, None) == hq.HQ_OK
 
 
@@ -264,7 +267,7 @@ def test_binding_refuses_host_buffers_as_device_pointers():
     import torch
     d = hq.make_desc(256, 256, 32, "w4")
     with pytest.raises(TypeError, match="CPU tensor"):
-        hq.hq_rotate_quant_act(torch.zeros((1, 256)), 1, 256, 32, None, None, None, None, None)
+        hq.hq_rotate_quant_act(d, torch.zeros((1, 256)), 1, None, None, None, None, None)
     with pytest.raises(TypeError, match="ndarray"):
         hq.hq_verify_gemm(d, np.zeros(16, dtype=np.uint8), None, None, 1, None, None, None)
     with pytest.raises(TypeError, match="CPU tensor"):

@@ -29,13 +29,14 @@ def _need_gpu():
     hq.load()
 
 
-def gpu_act(X, signs_dev, G):
+def gpu_act(X, signs_dev, G, fmt="w4"):
     M, K = X.shape
+    desc = hq.make_desc(K, 128, G, fmt)
     qx = Guarded((M, K), torch.int8, DEV)
     gsum = Guarded((M, K // G), torch.int32, DEV)
-    qop = Guarded((hq.hq_act_operand_bytes(M, K, G),), torch.uint8, DEV, fill=0xFF)  # padding must be written
+    qop = Guarded((hq.hq_act_operand_bytes(desc, M),), torch.uint8, DEV, fill=0xFF)  # padding must be written
     sx = Guarded((M,), torch.float32, DEV)
-    hq.hq_rotate_quant_act(X, M, K, G, signs_dev, qx.t, gsum.t, qop.t, sx.t)
+    hq.hq_rotate_quant_act(desc, X, M, signs_dev, qx.t, gsum.t, qop.t, sx.t)
     torch.cuda.synchronize()
     for name, g in (("qx", qx), ("gsum", gsum), ("operand", qop), ("sx", sx)):
         g.check(name)
@@ -63,9 +64,10 @@ ACT_CASES = [(1, 32, 32), (3, 64, 16), (16, 256, 32), (17, 256, 64), (16, 4096, 
 def test_rotate_quant_act_bit_exact(M, K, G):
     X = synth.activations(M, K, seed=M * 7 + K, outlier_channels=min(2, K), heavy_frac=0.01)
     s_host, s_dev = signs_pair(M + K, K)
-    qx, gsum, qop, sx = gpu_act(X.to(DEV), s_dev, G)
     rq, rs, rg = oracle.quant_act(X.numpy(), G, s_host)
-    check_act(qx, gsum, sx, rq, rs, rg)
+    for fmt in ("w4", "w8"):  # the two operand encodings
+        qx, gsum, qop, sx = gpu_act(X.to(DEV), s_dev, G, fmt)
+        check_act(qx, gsum, sx, rq, rs, rg)
 
 
 def test_rotate_quant_act_degenerate_rows():
@@ -134,7 +136,7 @@ def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
     if layer is None:
         layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
     ws = hq.workspace(layer.desc, M, DEV)
-    bufs = hq.act_buffers(M, K, G, DEV)
+    bufs = hq.act_buffers(layer.desc, M, DEV)
     P = Guarded((M, layer.N, K // G), torch.int32, DEV) if check else None
     # Y starts as NaN: an output the kernel fails to write (or to zero before
     # accumulating into it) stays NaN and fails the comparison; both live
@@ -191,8 +193,8 @@ def test_gemm_wait_timeout_selftest_reports_error_and_recovers():
     W = synth.weights(N, K, seed=42)
     s_host, s_dev = signs_pair(43, K)
     layer = hq.pack_layer(W.to(DEV), G, "w4", s_host)
-    _, _, qop, sx = hq.act_buffers(M, K, G, DEV, int8_codes=False)
-    hq.hq_rotate_quant_act(X.to(DEV), M, K, G, layer.signs, None, None, qop, sx)
+    _, _, qop, sx = hq.act_buffers(layer.desc, M, DEV, int8_codes=False)
+    hq.hq_rotate_quant_act(layer.desc, X.to(DEV), M, layer.signs, None, None, qop, sx)
     ws = hq.workspace(layer.desc, M, DEV)
     Y = torch.empty((M, N), dtype=torch.float32, device=DEV)
     hq.hq_selftest_gemm_wait_timeout(layer.desc, layer.blob, qop, sx, M, Y, ws, 1_000_000)

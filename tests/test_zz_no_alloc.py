@@ -54,8 +54,8 @@ def _layer(fmt, M, K, N, G, dev):
     W = synth.weights(N, K, seed=N + 5).to(dev)
     signs = hq.hq_make_signs(17, K)
     layer = hq.pack_layer(W, G, fmt, signs)
-    _, _, qop, sx = hq.act_buffers(M, K, G, dev, int8_codes=False)
-    hq.hq_rotate_quant_act(X, M, K, G, layer.signs, None, None, qop, sx)
+    _, _, qop, sx = hq.act_buffers(layer.desc, M, dev, int8_codes=False)
+    hq.hq_rotate_quant_act(layer.desc, X, M, layer.signs, None, None, qop, sx)
     return layer, qop, sx
 
 
