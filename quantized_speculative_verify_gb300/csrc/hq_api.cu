@@ -91,40 +91,54 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.scale_bytes = g.scale_bytes;
     const int MT = act_rows(M);
     const bool e4 = act_e4(g.fmt, M, g.G);
+    // stage: U weight tiles, then the U activation K tiles (codes, group sums)
+    a.act_bytes = act_tile_code_bytes(M, g.G);
+    a.s_bytes = act_tile_sum_bytes(M, g.G);
+    a.act_tile_bytes = act_tile_bytes(M, g.G);
+    auto stage_layout = [&](int U, int header) {
+        a.U = U;
+        a.act_off = (U * g.tile_bytes + 127) / 128 * 128;
+        a.stage_bytes = (a.act_off + U * a.act_tile_bytes + 127) / 128 * 128;
+        // Stage ring: as many units as fit in shared memory beside the barriers.
+        int stages = (GEMM_SMEM_LIMIT - header) / a.stage_bytes;
+        if (stages > MAX_STAGES) stages = MAX_STAGES;
+        if (stages < 2) stages = 2;
+        a.stages = stages;
+        return header + (size_t)stages * a.stage_bytes <= (size_t)GEMM_SMEM_LIMIT;
+    };
+    if (g.fmt == HQ_W4_ASYM && MT <= 32) {
+        // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows of
+        // 4-bit weights, where the per-group fold of every output is a few
+        // register operations.  Units of four tiles.
+        a.V = a.na = a.nd = 0;
+        if (!stage_layout(4, 1024)) return cudaErrorInvalidConfiguration;
+        return launch_gemm_w4_rs(a, pdl, s);
+    }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
     const int acols = e4 ? g.KT / 4 : g.KT / 2;  // TMEM columns of one tile's widened weights
-    // Pipeline unit: two tiles up to 32 rows (every barrier wait then serves
-    // two tiles), one above.  Tensor memory (512 columns): two A buffers of a
-    // unit, then accumulator units of V groups (as many as fit twice, up to
-    // a unit's groups), up to MAX_ND of them.
-    int U = MT <= 32 ? 2 : 1, V = 1, nd = 0;
+    // Pipeline unit: U consecutive tiles, one weight copy and one
+    // activation copy (fewer, larger copies stream faster); four tiles up to
+    // 32 rows where tensor memory allows, else two, else one.  Tensor memory
+    // (512 columns): two A buffers of a unit, then accumulator units of V
+    // groups (as many as fit twice, up to a unit's groups), up to MAX_ND.
+    int U = MT <= 32 ? 4 : 1, V = 1, nd = 0;
     const int na = 2;
     for (;;) {
         const int rem = TMEM_COLS - na * U * acols;
-        V = U * g.GPT;
-        while (V > 1 && 2 * V * dc > rem) V /= 2;
-        nd = rem / (V * dc);
+        nd = 0;
+        if (rem > 0) {
+            V = U * g.GPT;
+            while (V > 1 && 2 * V * dc > rem) V /= 2;
+            nd = rem / (V * dc);
+        }
         if (nd >= 2 || U == 1) break;
-        U = 1;
+        U /= 2;
     }
     if (nd > MAX_ND) nd = MAX_ND;
-    a.U = U;
     a.V = V;
     a.na = na;
     a.nd = nd;
-    a.act_bytes = (g.KT / ACT_BLOCK) * MT * ACT_BLOCK * 2;
-    a.s_bytes = g.GPT * MT * 4;
-    a.act_off = (U * g.tile_bytes + 127) / 128 * 128;
-    a.s_off = a.act_off + U * a.act_bytes;
-    a.stage_bytes = (a.s_off + U * a.s_bytes + 127) / 128 * 128;
-    a.op_s_offset = (long long)act_code_bytes(M, g.K);
-    // Stage ring: as many units as fit in ~200 KB of shared memory.
-    int stages = (200 * 1024) / a.stage_bytes;
-    if (stages > MAX_STAGES) stages = MAX_STAGES;
-    if (stages < 2) stages = 2;
-    a.stages = stages;
-    if (nd < 2 || na * U * acols + nd * V * dc > TMEM_COLS ||
-        2048 + (size_t)stages * a.stage_bytes > (size_t)GEMM_SMEM_LIMIT)
+    if (!stage_layout(U, 2048) || nd < 2 || na * U * acols + nd * V * dc > TMEM_COLS)
         return cudaErrorInvalidConfiguration;
     return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, pdl, s) : launch_gemm_w8(a, pdl, s);
 }

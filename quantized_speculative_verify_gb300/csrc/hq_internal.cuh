@@ -119,35 +119,39 @@ __host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_of
 
 // Activation operand of the GEMM (private to the library).  Rows are padded
 // to MT = 16, 32, 64 or 128 (the MMA's N); rows past M and features past K
-// are zero.  Two encodings of the int8 codes, chosen by the layers that read
-// the operand (act_e4):
-//   fp16:   [ceil(K/128) blocks][16 chunks of 8 features][MT rows][8 fp16]
-//           (exact for |q| <= 127), the B operand of kind::f16 MMAs;
-//   digits: [ceil(K/128) blocks][8 chunks of 16 features][2 MT rows][16 e4m3]:
-//           q = 16 h + l with l in [-8, 7], h in [-8, 8], both exact in e4m3;
-//           row r < MT holds the l of token r, row MT + r its h: the B
-//           operand of kind::f8f6f4 MMAs whose N covers both digits.
-// Either way a block is the B operand of a tile's MMAs as 8-row x 16-byte
-// core matrices (K-major, no swizzle), MT * 256 bytes.  Then
-//   group sums [groups][MT] fp32: S[g][m] = sum of the int8 codes of row m
-//              over group g; the groups are counted per 128-feature block
-//              (128 / G per block for G <= 128), so that every tile finds its
-//              own, zero past K.
+// are zero.  It is a sequence of K tiles of KT = max(G, 128) features (the
+// weight blob's K tiles), each holding what one weight tile's MMAs and
+// epilogue read, so that a run of consecutive K tiles is one contiguous copy:
+//   codes, KT / 128 blocks of 128 features, in one of two encodings chosen
+//   by the layers that read the operand (act_e4):
+//     fp16:   [16 chunks of 8 features][MT rows][8 fp16] (exact for
+//             |q| <= 127), the B operand of kind::f16 MMAs;
+//     digits: [8 chunks of 16 features][2 MT rows][16 e4m3]: q = 16 h + l
+//             with l in [-8, 7], h in [-8, 8], both exact in e4m3; row r < MT
+//             holds the l of token r, row MT + r its h: the B operand of
+//             kind::f8f6f4 MMAs whose N covers both digits;
+//   either way a block is the B operand of a tile's MMAs as 8-row x 16-byte
+//   core matrices (K-major, no swizzle), MT * 256 bytes; then
+//   group sums [KT / G groups][MT] fp32: S[g][m] = sum of the int8 codes of
+//   row m over the tile's group g (zero past K).
 constexpr int ACT_BLOCK = 128;
 __host__ __device__ inline int act_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
-// The digit encoding: 4-bit weights (their codes are e4m3 bytes as they are),
-// rows that fit an MMA of N = 2 MT <= 128, and groups of at least 32 features
-// (one f8f6f4 MMA covers 32).
+// The digit encoding: 4-bit weights (their codes are e4m3 bytes as they are)
+// on the tensor-memory GEMM, rows that fit an MMA of N = 2 MT <= 128 (33 to
+// 64 rows; up to 32 rows the register-resident GEMM takes the fp16
+// encoding), and groups of at least 32 features (one f8f6f4 MMA covers 32).
 __host__ __device__ inline bool act_e4(int fmt, int M, int G) {
-    return fmt == HQ_W4_ASYM && act_rows(M) <= 64 && G >= 32;
+    return fmt == HQ_W4_ASYM && act_rows(M) > 32 && act_rows(M) <= 64 && G >= 32;
 }
 __host__ __device__ inline int act_blocks(int K) { return (K + ACT_BLOCK - 1) / ACT_BLOCK; }
-__host__ __device__ inline int act_groups(int K, int G) { return G <= ACT_BLOCK ? act_blocks(K) * (ACT_BLOCK / G) : K / G; }
-__host__ __device__ inline size_t act_code_bytes(int M, int K) {
-    return (size_t)act_blocks(K) * (size_t)act_rows(M) * ACT_BLOCK * 2;
-}
+__host__ __device__ inline int act_kt(int G) { return G > ACT_BLOCK ? G : ACT_BLOCK; }
+__host__ __device__ inline int act_ktiles(int K, int G) { return (K + act_kt(G) - 1) / act_kt(G); }
+// bytes of one K tile's codes, of its group sums, and of the whole K tile
+__host__ __device__ inline int act_tile_code_bytes(int M, int G) { return (act_kt(G) / ACT_BLOCK) * act_rows(M) * 256; }
+__host__ __device__ inline int act_tile_sum_bytes(int M, int G) { return (act_kt(G) / G) * act_rows(M) * 4; }
+__host__ __device__ inline int act_tile_bytes(int M, int G) { return act_tile_code_bytes(M, G) + act_tile_sum_bytes(M, G); }
 __host__ __device__ inline size_t act_operand_bytes(int M, int K, int G) {
-    return act_code_bytes(M, K) + (size_t)act_groups(K, G) * (size_t)act_rows(M) * 4;
+    return (size_t)act_ktiles(K, G) * (size_t)act_tile_bytes(M, G);
 }
 
 // Device error codes written to the workspace error word.

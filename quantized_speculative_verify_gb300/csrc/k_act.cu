@@ -73,18 +73,25 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const int lane = tid & 31;
     const int n4 = K >> 2;  // float4s per row
     const int n4pad = act_blocks(K) * (ACT_BLOCK / 4);
-    const int ngk = K / G, ngp = act_groups(K, G);
-    float *op_s = qop ? reinterpret_cast<float *>(qop + act_code_bytes(M, K)) : nullptr;
+    const int ngk = K / G;
+    // operand: K tiles of KT features, each its code blocks then its group sums
+    const int bpt = act_kt(G) / ACT_BLOCK;  // code blocks per K tile
+    const int gpt = act_kt(G) / G;          // groups per K tile
+    const int ngp = act_ktiles(K, G) * gpt; // groups of the operand, padding included
+    const size_t tb = (size_t)bpt * MT * 256 + (size_t)gpt * MT * 4;  // bytes per K tile
+    // operand position of group sum g of this row
+    auto op_s = [&](int g) -> float * {
+        return reinterpret_cast<float *>(qop + (size_t)(g / gpt) * tb + (size_t)bpt * MT * 256) + (size_t)(g % gpt) * MT + row;
+    };
     // byte offset of the 4 features 4*idx .. 4*idx+3 of this row in the
     // operand: fp16, 8 bytes; digits, 4 bytes of low digits (the high digits
     // are MT rows further)
     auto op_off = [&](int idx) -> size_t {
         const int f = idx * 4;
-        if (e4) {
-            const int kb = f / ACT_BLOCK, c = (f % ACT_BLOCK) / 16;
-            return (size_t)kb * MT * 256 + ((size_t)c * 2 * MT + row) * 16 + (size_t)(f % 16);
-        }
-        return ((size_t)(f / 8) * MT + row) * 16 + (size_t)(f % 8) * 2;
+        const int kb = f / ACT_BLOCK, fb = f % ACT_BLOCK;
+        const size_t blk = (size_t)(kb / bpt) * tb + (size_t)(kb % bpt) * MT * 256;
+        if (e4) return blk + ((size_t)(fb / 16) * 2 * MT + row) * 16 + (size_t)(fb % 16);
+        return blk + ((size_t)(fb / 8) * MT + row) * 16 + (size_t)(fb % 8) * 2;
     };
 
     if (row >= M) {
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
                     *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(0u, 0u);
                 }
             }
-            for (int g = tid; g < ngp; g += T) op_s[(size_t)g * MT + row] = 0.0f;
+            for (int g = tid; g < ngp; g += T) *op_s(g) = 0.0f;
         }
         pdl_launch_dependents();
         return;
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     for (int g = tid; g < ngp; g += T) {
         const int v2 = g < ngk ? s_gs[g] : 0;
         if (gsum && g < ngk) gsum[(size_t)row * ngk + g] = v2;
-        if (op_s) op_s[(size_t)g * MT + row] = (float)v2;
+        if (qop) *op_s(g) = (float)v2;
     }
 }
 

@@ -1,0 +1,336 @@
+// k_gemm_rs.cuh -- the verify GEMM for 4-bit weights and up to 32 token rows,
+// with every partial sum in registers: warp-level fp16 MMAs on the weights
+// widened straight from the packed tile, the per-group dequantization folded
+// into the fp32 sums as each group ends.
+//
+// Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling":
+// section "How Uzu optimizes bytes and tokens per pass" (both operands of the
+// verify matmul are integers; Medium weights are 4-bit asymmetric, grouped
+// along K) and section "Producing several tokens from one model pass" (the
+// verify batch: a draft tree of up to 32 tokens shares one weight stream).
+//
+// Exact integer contraction on fp16 MMAs (mma.sync m16n8k16, fp32
+// accumulate): weight codes minus the zero point (|q - z| <= 15) and
+// activation codes (|q| <= 127) are exact in fp16, their products exact in
+// fp32, and a group's sum stays below 2^24, so each group's accumulator holds
+// the integer partial sum P of the Medium identity exactly (with the zero
+// point applied to the weights, no group-sum correction is needed).  With at
+// most 32 rows the kernel is bound by instruction issue, not by the tensor
+// pipe: the fp16 form issues one instruction per MMA and needs no split of
+// the activation codes, where the e4m3 forms on this GPU take several.
+//
+// Channels are the MMA's M (16 per warp), tokens its N (8 per MMA), so the
+// weights are the A operand.  A lane widens its four codes of one MMA step
+// and one channel in three instructions: a byte permute picks the two bytes
+// holding them (the packed layout puts features 8w .. 8w + 3 in the low
+// nibbles of word w, 8w + 4 .. 8w + 7 in its high nibbles), a mask under the
+// fp16 exponent bits of 1024 makes 1024 + q (low nibbles) or 1024 + 16 q
+// (high nibbles), and one fused multiply-add by 1 or 1/16 subtracts 1024 + z
+// or 64 + z, exactly.  The activation codes come from the operand's fp16
+// blocks through ldmatrix.
+//
+// Fold of a group into the running sums, in the oracle's ascending group
+// order: y += scale * P.  Exact-order and check modes round the multiply and
+// the add separately (the oracle's arithmetic; the partial sums P written in
+// check mode); otherwise one fused multiply-add, within the fp32 tolerance of
+// the oracle.
+//
+// Thread block: warp 0 streams the weight tiles, warp 1 the activation K
+// tiles (gemm_common.cuh), warps 2..9 compute.  Consumer warp w owns channels
+// 16 w .. 16 w + 15 of every tile and every token; it needs no other warp
+// between a stage's arrival and its release.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gemm_common.cuh"
+#include "hq_internal.cuh"
+#include "hq_tc.cuh"
+
+namespace hq {
+
+
+constexpr int RS_CONSUMERS = 8;                      // consumer warps, 16 channels each
+constexpr int RS_THREADS = (2 + RS_CONSUMERS) * 32;  // + the two producers
+
+// D (+)= A (16 x 16 fp16, row-major) x B (16 x 8 fp16, column-major).  A
+// function of its registers alone (not volatile): the compiler may move the
+// next step's loads ahead of it.
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], const uint32_t (&A)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(b0), "r"(b1));
+}
+// same with a zero accumulator input (a group's first K step)
+__device__ __forceinline__ void mma_f16_zero(float (&d)[4], const uint32_t (&A)[4], uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(b0), "r"(b1), "f"(z));
+}
+// Two 4-bit codes -> fp16x2 (q - z): the selected bytes' nibbles under the
+// exponent bits of 1024, then x * mul + add with (mul, add) = (1, -(1024 + z))
+// for low nibbles or (1/16, -(64 + z)) for high ones.
+__device__ __forceinline__ uint32_t widen2(uint32_t w, uint32_t sel, uint32_t mask, uint32_t mul, uint32_t add) {
+    uint32_t x, r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
+    x = (x & mask) | 0x64006400u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(mul), "r"(add));
+    return r;
+}
+// four 8 x 16-byte row blocks of shared memory, one row address per lane
+// (a memory read: it stays after the wait for the stage)
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(addr)
+        : "memory");
+}
+
+// MT: token rows (16 or 32); G: quantization group (16 .. 256), fixed at
+// compile time so that a tile's K steps and groups unroll completely.
+template <int MT, int G, bool EXACT>
+__global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs a) {
+    constexpr int NT = MT / 8;             // MMA column tiles of tokens
+    constexpr int KT = G > 128 ? G : 128;  // features per tile
+    constexpr int GPT = KT / G;            // groups per tile
+    constexpr int KS = G / 16;             // K steps of 16 features per group
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
+    uint64_t *empty = full + MAX_STAGES;
+    int *sflag = reinterpret_cast<int *>(empty + MAX_STAGES);  // accumulating mode: two segment flags
+    uint8_t *ring = smem_raw + 1024;
+    const int S = a.stages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const GemmBlock blk = make_gemm_block(a, ring, full, empty, sflag);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_addr(&full[i]), 2);             // the two producers' arrivals
+            mbar_init(smem_addr(&empty[i]), RS_CONSUMERS);  // one per consumer warp
+        }
+        sflag[0] = sflag[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) gemm_weight_producer(a, blk);
+        return;
+    }
+    if (warp == 1) {
+        if (lane == 0) gemm_act_producer(a, blk);
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers ---
+    pdl_wait();
+    const int cw = warp - 2;                  // consumer warp: channels 16 cw .. 16 cw + 15
+    const int ctid = threadIdx.x - 64;        // consumer thread 0 .. RS_CONSUMERS * 32 - 1
+    const int g = lane >> 2, tig = lane & 3;  // MMA lane coordinates
+    const int M = a.M, KTILES = a.KTILES;
+    float *wsp = reinterpret_cast<float *>(a.ws + ws_partial_offset());
+    // widening constants of this lane: features 2 tig, 2 tig + 1 of a word
+    // are bytes 2 (tig & 1), + 1, low nibbles for tig < 2, high for tig >= 2
+    const uint32_t b0 = 2u * (uint32_t)(tig & 1);
+    const uint32_t wsel = b0 | (4u << 4) | ((b0 + 1u) << 8) | (4u << 12);
+    const bool hi_nib = tig >= 2;
+    const uint32_t wmask = hi_nib ? 0x00F000F0u : 0x000F000Fu;
+    const uint32_t wmul = hi_nib ? 0x2C002C00u : 0x3C003C00u;  // fp16x2 1/16 or 1
+    // fp16 bits of -(64 + z) = 0xD400 + 16 z, of -(1024 + z) = 0xE400 + z
+    const uint32_t zbase = hi_nib ? 0xD400u : 0xE400u, zmul = hi_nib ? 16u : 1u;
+
+    bool ok = true;
+    int pend0 = -1, pend1 = -1, nsplit = 0;
+    const int first_b = blk.t0 / KTILES;
+    const int mark_old = gemm_zero_outputs(a, blk, ctid, RS_CONSUMERS * 32, 1);
+
+    // y[n][e]: channel 16 cw + g + 8 (e >> 1), token 8 n + 2 tig + (e & 1)
+    float y[NT][4];
+    int eb = blk.t0 / KTILES, ekt = blk.t0 - eb * KTILES, seg_k0 = ekt;
+    const int ch0 = 16 * cw + g;  // the lane's channels: ch0, ch0 + 8
+
+    // lane's ldmatrix row within a 4-matrix load: matrix (lane >> 3) holds
+    // features +0..7 / +8..15 (bit 0) of tokens +0..7 / +8..15 (bit 1)
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t lrow_off = (uint32_t)(((lm & 1) * MT + (lm >> 1) * 8 + lr) * 16);
+
+    RingPos ps{0, 0u};
+    for (int u = 0; u < blk.nunits; ++u) {
+        const int nt = blk.unit_tiles(u);
+        const int st = ps.slot;
+        if (ok) ok = mbar_wait_bounded(smem_addr(&full[st]), ps.phase, blk.err);
+        const uint8_t *stage = ring + (size_t)st * a.stage_bytes;
+        for (int j = 0; j < nt; ++j) {
+            const int i = u * blk.U + j;
+            if (i == 0 || ekt == 0) {
+                seg_k0 = ekt;
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) y[n][e] = 0.0f;
+            }
+            const uint8_t *tile = stage + (size_t)j * a.tile_bytes;
+            const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);  // scales [channel][GPT]
+            const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;                // zero nibbles [channel * GPT + g]
+            const uint32_t act_s = smem_addr(stage + a.act_off + (size_t)j * a.act_tile_bytes);
+            // the lane's two channels' 32-feature chunks: [KT / 32][BN][16 B]
+            const uint4 *wc0 = reinterpret_cast<const uint4 *>(tile) + ch0;
+            // the current 32-feature chunk of each channel (two 16-feature steps,
+            // which may belong to two groups)
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+#pragma unroll
+            for (int gl = 0; gl < GPT; ++gl) {
+                // zero points -> the widening's additive constants; scales
+                uint32_t zadd[2];
+                float sc[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int zi = (ch0 + 8 * h) * GPT + gl;
+                    const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
+                    zadd[h] = (zbase + z * zmul) * 0x10001u;
+                    sc[h] = tsc[zi];
+                }
+                float acc[NT][4];
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int s = gl * KS + ks;  // 16-feature step of the tile
+                    if ((s & 1) == 0) {
+                        w0 = wc0[(s >> 1) * BN];
+                        w1 = wc0[(s >> 1) * BN + 8];
+                    }
+                    // A: rows g, g + 8 (channels ch0, ch0 + 8), features 2 tig.. and 2 tig + 8..
+                    const uint32_t lo0 = (s & 1) ? w0.z : w0.x, hi0 = (s & 1) ? w0.w : w0.y;
+                    const uint32_t lo1 = (s & 1) ? w1.z : w1.x, hi1 = (s & 1) ? w1.w : w1.y;
+                    uint32_t A[4];
+                    A[0] = widen2(lo0, wsel, wmask, wmul, zadd[0]);
+                    A[1] = widen2(lo1, wsel, wmask, wmul, zadd[1]);
+                    A[2] = widen2(hi0, wsel, wmask, wmul, zadd[0]);
+                    A[3] = widen2(hi1, wsel, wmask, wmul, zadd[1]);
+                    // B: tokens' fp16 codes, features 16 s ..: block s / 8, chunks 2 (s % 8), + 1
+                    const uint32_t b_s = act_s + (uint32_t)((s >> 3) * (MT * 256) + ((s & 7) * 2) * (MT * 16));
+#pragma unroll
+                    for (int n2 = 0; n2 < NT; n2 += 2) {
+                        uint32_t bq[4];
+                        ldmatrix_x4(bq, b_s + lrow_off + (uint32_t)(n2 * 8 * 16));
+                        if (ks == 0) {
+                            mma_f16_zero(acc[n2], A, bq[0], bq[1]);
+                            mma_f16_zero(acc[n2 + 1], A, bq[2], bq[3]);
+                        } else {
+                            mma_f16_acc(acc[n2], A, bq[0], bq[1]);
+                            mma_f16_acc(acc[n2 + 1], A, bq[2], bq[3]);
+                        }
+                    }
+                }
+                // fold the group: y += scale * P (P exact in acc)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float s_ch = sc[e >> 1];
+                        if constexpr (EXACT) {
+                            if (a.partials) {
+                                const int tok = 8 * n + 2 * tig + (e & 1);
+                                const int nn = eb * BN + ch0 + 8 * (e >> 1);
+                                const int gq = ekt * GPT + gl;
+                                if (tok < M && nn < a.N && gq < a.NGK)
+                                    a.partials[((size_t)tok * a.N + nn) * a.NGK + gq] = __float2int_rn(acc[n][e]);
+                            }
+                            // y += scale * P: product rounded, then sum rounded
+                            y[n][e] = __fadd_rn(y[n][e], __fmul_rn(s_ch, acc[n][e]));
+                        } else {
+                            y[n][e] = fmaf(s_ch, acc[n][e], y[n][e]);
+                        }
+                    }
+            }
+            // end of an n-block segment?
+            if (ekt == KTILES - 1 || i == blk.ntl - 1) {
+                int kind;
+                float *slot_base = nullptr;
+                if (seg_k0 == 0 && ekt == KTILES - 1) {
+                    kind = SEG_FULL;  // the whole K range of the n-block
+                } else if (blk.det) {
+                    kind = SEG_PUBLISH;
+                    const int slot = eb == first_b ? 0 : 1;
+                    slot_base = wsp + ((size_t)blockIdx.x * 2 + slot) * ws_slot_floats();
+                    if (slot == 0)
+                        pend0 = eb;
+                    else
+                        pend1 = eb;
+                } else {
+                    kind = SEG_ADD;  // once the zeroing is visible (the segment's flag)
+                    if (ok) ok = wait_flag_bounded(smem_addr(&sflag[nsplit]), blk.err);
+                    ++nsplit;
+                }
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int nl = ch0 + 8 * (e >> 1);
+                        gemm_segment_out(a, kind, slot_base, 8 * n + 2 * tig + (e & 1), nl, eb * BN + nl, y[n][e]);
+                    }
+            }
+            if (++ekt == KTILES) {
+                ekt = 0;
+                ++eb;
+            }
+        }
+        // this warp no longer reads the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+        ps.next(S);
+    }
+
+    gemm_finish(a, blk, ok, pend0, pend1, mark_old, ctid, RS_CONSUMERS * 32, 1);
+}
+
+template <int MT, int G, bool EXACT>
+cudaError_t launch_gemm_rs_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
+    auto kern = k_verify_gemm_rs<MT, G, EXACT>;
+    const size_t smem = 1024 + (size_t)a.stages * (size_t)a.stage_bytes;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::atomic<int> configured[CACHE_DEVICES];
+    int done = 0;
+    e = cached_per_device(configured, dev, &done, [&](int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_LIMIT);
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid);
+    cfg.blockDim = dim3(RS_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int MT, bool EXACT>
+cudaError_t launch_gemm_rs_g(const GemmArgs &a, bool pdl, cudaStream_t s) {
+    switch (a.G) {
+        case 16: return launch_gemm_rs_instance<MT, 16, EXACT>(a, pdl, s);
+        case 32: return launch_gemm_rs_instance<MT, 32, EXACT>(a, pdl, s);
+        case 64: return launch_gemm_rs_instance<MT, 64, EXACT>(a, pdl, s);
+        case 128: return launch_gemm_rs_instance<MT, 128, EXACT>(a, pdl, s);
+        case 256: return launch_gemm_rs_instance<MT, 256, EXACT>(a, pdl, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// 4-bit weights, the fp16-encoded operand, up to 32 rows.
+inline cudaError_t launch_gemm_rs(const GemmArgs &a, bool pdl, cudaStream_t s) {
+    const bool exact = a.partials != nullptr || a.nb_align != 0;
+    if (act_rows(a.M) <= 16) return exact ? launch_gemm_rs_g<16, true>(a, pdl, s) : launch_gemm_rs_g<16, false>(a, pdl, s);
+    return exact ? launch_gemm_rs_g<32, true>(a, pdl, s) : launch_gemm_rs_g<32, false>(a, pdl, s);
+}
+
+}  // namespace hq
