@@ -65,6 +65,7 @@ struct GemmArgs {
 constexpr int ZERO_MARK = 1 << 24;
 
 constexpr int MAX_STAGES = 32;
+constexpr int RS_UNIT = 4;  // tiles per pipeline unit of the register-resident GEMM
 constexpr int GEMM_SMEM_LIMIT = 227 * 1024;   // opt-in maximum of dynamic shared memory per block
 
 __device__ __forceinline__ int tile_begin(int c, int T, int grid) { return (int)(((long long)c * T) / grid); }

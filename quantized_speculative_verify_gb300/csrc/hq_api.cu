@@ -93,8 +93,8 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     const bool e4 = act_e4(g.fmt, M, g.G);
     // stage: U weight tiles, then the U activation K tiles (codes, group sums)
     a.act_bytes = act_tile_code_bytes(M, g.G);
-    a.s_bytes = act_tile_sum_bytes(M, g.G);
-    a.act_tile_bytes = act_tile_bytes(M, g.G);
+    a.s_bytes = act_tile_sum_bytes(M, g.G, g.fmt);
+    a.act_tile_bytes = act_tile_bytes(M, g.G, g.fmt);
     auto stage_layout = [&](int U, int header) {
         a.U = U;
         a.act_off = (U * g.tile_bytes + 127) / 128 * 128;
@@ -111,7 +111,7 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
         // 4-bit weights, where the per-group fold of every output is a few
         // register operations.  Units of four tiles.
         a.V = a.na = a.nd = 0;
-        if (!stage_layout(4, 1024)) return cudaErrorInvalidConfiguration;
+        if (!stage_layout(RS_UNIT, 1024)) return cudaErrorInvalidConfiguration;
         return launch_gemm_w4_rs(a, pdl, s);
     }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
@@ -224,7 +224,7 @@ int hq_pack_weights_at(const hq_layer_desc *desc, int32_t n0, int32_t rows, cons
 
 size_t hq_act_operand_bytes(const hq_layer_desc *desc, int32_t M) {
     if (!desc_ok(desc) || M <= 0 || M > HQ_MAX_M) return 0;
-    return hq::act_operand_bytes(M, desc->K, desc->group);
+    return hq::act_operand_bytes(M, desc->K, desc->group, desc->format);
 }
 
 int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, const uint32_t *signs, int8_t *qx,
@@ -238,7 +238,7 @@ int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, co
         (gsum && !aligned(gsum, 4)) || (qop && !aligned(qop, 16)))
         return HQ_ERR_INVALID_ARG;
     const int K = desc->K, G = desc->group;
-    return cuda_status(hq::launch_rotate_quant_act(X, M, K, G, hq::act_e4(desc->format, M, G), signs, qx, gsum,
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, G, hq::act_e4(desc->format, M, G), hq::act_sums(desc->format, M), signs, qx, gsum,
                                                    static_cast<uint8_t *>(qop), sx, (flags & HQ_LAUNCH_PDL) != 0,
                                                    static_cast<cudaStream_t>(stream)));
 }

@@ -131,7 +131,8 @@ __host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_of
 //             holds the l of token r, row MT + r its h: the B operand of
 //             kind::f8f6f4 MMAs whose N covers both digits;
 //   either way a block is the B operand of a tile's MMAs as 8-row x 16-byte
-//   core matrices (K-major, no swizzle), MT * 256 bytes; then
+//   core matrices (K-major, no swizzle), MT * 256 bytes; then, where the
+//   consuming GEMM needs them (act_sums),
 //   group sums [KT / G groups][MT] fp32: S[g][m] = sum of the int8 codes of
 //   row m over the tile's group g (zero past K).
 constexpr int ACT_BLOCK = 128;
@@ -146,12 +147,21 @@ __host__ __device__ inline bool act_e4(int fmt, int M, int G) {
 __host__ __device__ inline int act_blocks(int K) { return (K + ACT_BLOCK - 1) / ACT_BLOCK; }
 __host__ __device__ inline int act_kt(int G) { return G > ACT_BLOCK ? G : ACT_BLOCK; }
 __host__ __device__ inline int act_ktiles(int K, int G) { return (K + act_kt(G) - 1) / act_kt(G); }
+// Whether the operand carries the group sums: only the GEMM that applies a
+// 4-bit layer's zero point through them (the tensor-memory GEMM, above 32
+// rows).  Up to 32 rows the register-resident GEMM subtracts the zero point
+// while widening the weights; 8-bit weights have none.
+__host__ __device__ inline bool act_sums(int fmt, int M) { return fmt == HQ_W4_ASYM && act_rows(M) > 32; }
 // bytes of one K tile's codes, of its group sums, and of the whole K tile
 __host__ __device__ inline int act_tile_code_bytes(int M, int G) { return (act_kt(G) / ACT_BLOCK) * act_rows(M) * 256; }
-__host__ __device__ inline int act_tile_sum_bytes(int M, int G) { return (act_kt(G) / G) * act_rows(M) * 4; }
-__host__ __device__ inline int act_tile_bytes(int M, int G) { return act_tile_code_bytes(M, G) + act_tile_sum_bytes(M, G); }
-__host__ __device__ inline size_t act_operand_bytes(int M, int K, int G) {
-    return (size_t)act_ktiles(K, G) * (size_t)act_tile_bytes(M, G);
+__host__ __device__ inline int act_tile_sum_bytes(int M, int G, int fmt) {
+    return act_sums(fmt, M) ? (act_kt(G) / G) * act_rows(M) * 4 : 0;
+}
+__host__ __device__ inline int act_tile_bytes(int M, int G, int fmt) {
+    return act_tile_code_bytes(M, G) + act_tile_sum_bytes(M, G, fmt);
+}
+__host__ __device__ inline size_t act_operand_bytes(int M, int K, int G, int fmt) {
+    return (size_t)act_ktiles(K, G) * (size_t)act_tile_bytes(M, G, fmt);
 }
 
 // Device error codes written to the workspace error word.
@@ -355,7 +365,7 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 
 // Launchers (defined in the kernel translation units).
 namespace hq {
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, bool sums, const uint32_t *signs, int8_t *qx,
                                     int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s);
 // rows of W -> n-blocks nb0.. of the blob of layer g
 cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,

@@ -14,8 +14,9 @@
 // values are bit-identical to a scalar implementation of the same order.
 // The codes are written as int8 and/or as the GEMM's operand: fp16 (exact
 // for |q| <= 127) or two e4m3 digits (q = 16 h + l), in 128-feature blocks
-// laid out as the MMA's B operand, plus the per-group sums of the codes (the
-// Medium identity's correction term).
+// laid out as the MMA's B operand, plus, where the GEMM applies a zero point
+// through them, the per-group sums of the codes (the Medium identity's
+// correction term).
 // The grid has one block per operand row: rows past M (padding up to the
 // MMA's N) only write zeros.
 #include <cuda_fp16.h>
@@ -59,7 +60,7 @@ __device__ __forceinline__ void digits4(int q0, int q1, int q2, int q3, uint32_t
 }
 
 template <int V, int T>
-__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G, int e4,
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G, int e4, int sums,
                                                         const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
                                                         int32_t *__restrict__ gsum, uint8_t *__restrict__ qop,
                                                         float *__restrict__ sx) {
@@ -78,7 +79,8 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const int bpt = act_kt(G) / ACT_BLOCK;  // code blocks per K tile
     const int gpt = act_kt(G) / G;          // groups per K tile
     const int ngp = act_ktiles(K, G) * gpt; // groups of the operand, padding included
-    const size_t tb = (size_t)bpt * MT * 256 + (size_t)gpt * MT * 4;  // bytes per K tile
+    // bytes per K tile: codes, then (where the GEMM reads them) group sums
+    const size_t tb = (size_t)bpt * MT * 256 + (sums ? (size_t)gpt * MT * 4 : 0);
     // operand position of group sum g of this row
     auto op_s = [&](int g) -> float * {
         return reinterpret_cast<float *>(qop + (size_t)(g / gpt) * tb + (size_t)bpt * MT * 256) + (size_t)(g % gpt) * MT + row;
@@ -105,12 +107,16 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
                     *reinterpret_cast<uint2 *>(qop + op_off(idx)) = make_uint2(0u, 0u);
                 }
             }
-            for (int g = tid; g < ngp; g += T) *op_s(g) = 0.0f;
+            if (sums)
+                for (int g = tid; g < ngp; g += T) *op_s(g) = 0.0f;
         }
         pdl_launch_dependents();
         return;
     }
-    for (int g = tid; g < ngk; g += T) s_gs[g] = 0;
+    // group sums: for the caller (gsum) or for the operand (sums)
+    const bool need_gs = gsum != nullptr || (qop != nullptr && sums != 0);
+    if (need_gs)
+        for (int g = tid; g < ngk; g += T) s_gs[g] = 0;
 
     const float c = __int_as_float((int)HADAMARD_SCALE_BITS);
     const float4 *xr = reinterpret_cast<const float4 *>(X + (size_t)row * K);
@@ -203,21 +209,24 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
         }
         // every thread of the warp takes part in the shuffles (lanes past the
         // row's end add zeros); a group's G/4 threads are consecutive lanes
-        int gs = q0 + q1 + q2 + q3;
-        for (int o = width / 2; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-        if (idx < n4 && (lane & (width - 1)) == 0) atomicAdd(&s_gs[(idx * 4) / G], gs);
+        if (need_gs) {
+            int gs = q0 + q1 + q2 + q3;
+            for (int o = width / 2; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+            if (idx < n4 && (lane & (width - 1)) == 0) atomicAdd(&s_gs[(idx * 4) / G], gs);
+        }
     }
+    if (!need_gs) return;
     __syncthreads();
     for (int g = tid; g < ngp; g += T) {
         const int v2 = g < ngk ? s_gs[g] : 0;
         if (gsum && g < ngk) gsum[(size_t)row * ngk + g] = v2;
-        if (qop) *op_s(g) = (float)v2;
+        if (qop && sums) *op_s(g) = (float)v2;
     }
 }
 
 template <int V, int T>
 cudaError_t launch_act_t(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
-                         int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
+                         int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s, bool sums) {
     cudaLaunchConfig_t cfg = {};
     // one block per operand row (rows past M write the operand's zero padding)
     cfg.gridDim = dim3((unsigned)(qop ? act_rows(M) : M));
@@ -229,25 +238,26 @@ cudaError_t launch_act_t(const float *X, int M, int K, int G, bool e4, const uin
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, e4 ? 1 : 0, signs, qx, gsum, qop, sx);
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, e4 ? 1 : 0, sums ? 1 : 0, signs, qx, gsum, qop,
+                              sx);
 }
 
 }  // namespace
 
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
-                                    int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, bool sums, const uint32_t *signs,
+                                    int8_t *qx, int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     // As many threads per row as the row has float4s, up to 1024: the kernel
     // is latency-bound (one block per row), so the shortest chain per thread
     // wins (256 threads x 4 float4s at K = 4096 made the pass 4% slower).
     const int n4 = K / 4;
-    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
-    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s);
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
     return cudaErrorInvalidValue;
 }
 

@@ -164,7 +164,9 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
         const int st = ps.slot;
         if (ok) ok = mbar_wait_bounded(smem_addr(&full[st]), ps.phase, blk.err);
         const uint8_t *stage = ring + (size_t)st * a.stage_bytes;
-        for (int j = 0; j < nt; ++j) {
+#pragma unroll
+        for (int j = 0; j < RS_UNIT; ++j) {
+            if (j >= nt) break;
             const int i = u * blk.U + j;
             if (i == 0 || ekt == 0) {
                 seg_k0 = ekt;

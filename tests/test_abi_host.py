@@ -116,13 +116,15 @@ def test_K_above_the_activation_limit_is_invalid(K):
 def test_act_operand_bytes():
     # opaque, but its size follows from the rows padded to the MMA's N (16, 32,
     # 64, 128), 128-feature blocks of 2 bytes per code (fp16, or two e4m3
-    # digits) and one fp32 sum per group and row
+    # digits), and one fp32 sum per group and row where the GEMM applies a
+    # 4-bit zero point through them (above 32 rows)
     def size(M, K, G, fmt="w4"):
         return hq.hq_act_operand_bytes(hq.make_desc(K, 128, G, fmt), M)
-    assert size(16, 4096, 64) == 32 * 16 * 256 + 64 * 16 * 4
-    assert size(16, 4096, 64, "w8") == size(16, 4096, 64)  # both encodings have the same size
-    assert size(3, 96, 32) == 1 * 16 * 256 + 4 * 16 * 4  # one padded block, its four groups
-    assert size(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4
+    assert size(16, 4096, 64) == 32 * 16 * 256  # the zero point is applied to the weights
+    assert size(16, 4096, 64, "w8") == size(16, 4096, 64)
+    assert size(3, 96, 32) == 1 * 16 * 256  # one padded block
+    assert size(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4  # group sums for the 4-bit zero point
+    assert size(33, 512, 256, "w8") == 4 * 64 * 256  # symmetric: no zero point
     assert size(128, 4096, 16) == 32 * 128 * 256 + 256 * 128 * 4
     assert size(0, 4096, 64) == 0 and size(129, 4096, 64) == 0
     for bad in (hq.hq_layer_desc(100, 128, 32, 0), hq.hq_layer_desc(96, 128, 64, 0), hq.hq_layer_desc(256, 128, 48, 0)):
