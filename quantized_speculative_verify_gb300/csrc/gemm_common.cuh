@@ -27,7 +27,10 @@
 // sums), each copied by its own producer warp with one bulk copy per run:
 // a bulk copy holds up the warp that issues it, and the weight stream must
 // not wait behind the activation copies.  A stage's `full` barrier completes
-// once both producers' bytes have landed.
+// once both producers' bytes have landed.  An SM serves its bulk copies in the
+// order they are issued, so while the ring first fills, unit u's weights go
+// out only after unit u - 1's activations: the first units land first
+// instead of behind the whole ring's weights.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -68,14 +71,22 @@ constexpr int MAX_STAGES = 32;
 constexpr int RS_UNIT = 4;  // tiles per pipeline unit of the register-resident GEMM
 constexpr int GEMM_SMEM_LIMIT = 227 * 1024;   // opt-in maximum of dynamic shared memory per block
 
-__device__ __forceinline__ int tile_begin(int c, int T, int grid) { return (int)(((long long)c * T) / grid); }
+// floor(x * y / z) for 0 <= x <= MAX_CTAS (or a tile index), y, z > 0: in
+// 32-bit arithmetic while the product fits (every layer below 2^23 tiles),
+// the 64-bit division (a long instruction sequence) otherwise.
+__device__ __forceinline__ int muldiv(int x, int y, int z) {
+    const long long p = (long long)x * y;
+    return p < (1LL << 31) ? (int)((unsigned)p / (unsigned)z) : (int)(p / z);
+}
+__device__ __forceinline__ int tile_begin(int c, int T, int grid) { return muldiv(c, T, grid); }
 // first tile of thread block c (c = grid: one past the last tile)
 __device__ __forceinline__ int range_begin(const GemmArgs &a, int c) {
-    return a.nb_align ? (int)(((long long)c * a.NB) / a.grid) * a.KTILES : tile_begin(c, a.T, a.grid);
+    return a.nb_align ? muldiv(c, a.NB, a.grid) * a.KTILES : tile_begin(c, a.T, a.grid);
 }
 // thread block whose range contains tile t
 __device__ __forceinline__ int cta_of_tile(int t, int T, int grid) {
-    return (int)((((long long)t + 1) * grid - 1) / T);
+    const long long p = ((long long)t + 1) * grid - 1;
+    return p < (1LL << 31) ? (int)((unsigned)p / (unsigned)T) : (int)(p / T);
 }
 
 // Position in a ring of n slots: slot index and the parity of its current
@@ -102,6 +113,7 @@ struct GemmBlock {
     uint8_t *ring;
     uint64_t *full, *empty;
     int *sflag;   // accumulating mode: the block's two segment flags
+    int *acts_issued;  // units whose activation copies have been issued (initial fill)
     __device__ __forceinline__ int unit_tiles(int u) const { return ntl - u * U < U ? ntl - u * U : U; }
 };
 
@@ -126,6 +138,7 @@ __device__ __forceinline__ GemmBlock make_gemm_block(const GemmArgs &a, uint8_t 
     b.full = full;
     b.empty = empty;
     b.sflag = sflag;
+    b.acts_issued = sflag + 2;
     return b;
 }
 
@@ -143,8 +156,13 @@ __device__ __forceinline__ void gemm_weight_producer(const GemmArgs &a, const Ge
                       a.blob + (size_t)(b.t0 + u * b.U) * (size_t)a.tile_bytes, (uint32_t)(nt * a.tile_bytes), fb, pol_w);
     };
     int u = 0;
-    for (; u < b.nunits && u < S; ++u) copy_weights(u, u);
+    if (b.nunits > 0) copy_weights(u++, 0);
     pdl_wait();
+    // the rest of the initial fill: unit u's weights after unit u - 1's activations
+    for (; u < b.nunits && u < S; ++u) {
+        if (!wait_count_shared_bounded(smem_addr(b.acts_issued), u, b.err)) break;
+        copy_weights(u, u);
+    }
     RingPos ps{u % S, (uint32_t)((u / S) & 1)};
     for (; u < b.nunits; ++u) {
         const int st = ps.slot;
@@ -207,6 +225,7 @@ __device__ __forceinline__ void gemm_act_producer(const GemmArgs &a, const GemmB
         const int st = ps.slot;
         if (!mbar_wait_bounded(smem_addr(&b.empty[st]), ps.phase ^ 1u, b.err)) break;
         copy_acts(u, st);
+        if (u < b.S) st_release_cta_shared(smem_addr(b.acts_issued), u + 1);
         if (!b.det)
             for (int j = 0; j < b.unit_tiles(u); ++j) check(u * b.U + j);
         ps.next(b.S);

@@ -322,6 +322,22 @@ __device__ __forceinline__ int ld_acquire_cta_shared(uint32_t addr) {
     return v;
 }
 
+// Wait until the shared-memory word at addr is at least target (acquire, CTA
+// scope), for at most WAIT_LIMIT_NS.  On time-out records DEV_ERR_TIMEOUT in
+// *err and returns false.
+__device__ __forceinline__ bool wait_count_shared_bounded(uint32_t addr, int target, int *err) {
+    if (ld_acquire_cta_shared(addr) >= target) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_cta_shared(addr) >= target) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (err) atomicExch(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Wait until the shared-memory word at addr is non-zero (acquire, CTA scope),
 // for at most WAIT_LIMIT_NS.  On time-out records DEV_ERR_TIMEOUT in *err and
 // returns false.

@@ -141,8 +141,9 @@ __global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmA
     uint64_t *d_full = a_empty + MAX_NA;
     uint64_t *d_empty = d_full + MAX_ND;
     uint64_t *done_bar = d_empty + MAX_ND;
-    int *sflag = reinterpret_cast<int *>(done_bar + 1);  // accumulating mode: two segment flags
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sflag + 2);
+    // accumulating mode: two segment flags; then the initial fill's counter
+    int *sflag = reinterpret_cast<int *>(done_bar + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sflag + 4);
     uint8_t *ring = smem_raw + 2048;
 
     // warp index made visibly warp-uniform (tensor-memory addresses derive from it)
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmA
             mbar_init(smem_addr(&d_empty[i]), NEPI);
         }
         mbar_init(smem_addr(done_bar), 1);
-        sflag[0] = sflag[1] = 0;
+        sflag[0] = sflag[1] = sflag[2] = 0;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);

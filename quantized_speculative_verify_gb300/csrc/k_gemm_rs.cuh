@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
     uint64_t *empty = full + MAX_STAGES;
-    int *sflag = reinterpret_cast<int *>(empty + MAX_STAGES);  // accumulating mode: two segment flags
+    // accumulating mode: two segment flags; then the initial fill's counter
+    int *sflag = reinterpret_cast<int *>(empty + MAX_STAGES);
     uint8_t *ring = smem_raw + 1024;
     const int S = a.stages;
 
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
             mbar_init(smem_addr(&full[i]), 2);             // the two producers' arrivals
             mbar_init(smem_addr(&empty[i]), RS_CONSUMERS);  // one per consumer warp
         }
-        sflag[0] = sflag[1] = 0;
+        sflag[0] = sflag[1] = sflag[2] = 0;
         fence_mbar_init();
     }
     __syncthreads();
