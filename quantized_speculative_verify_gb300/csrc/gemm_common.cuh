@@ -68,7 +68,13 @@ struct GemmArgs {
 constexpr int ZERO_MARK = 1 << 24;
 
 constexpr int MAX_STAGES = 32;
-constexpr int RS_UNIT = 4;  // tiles per pipeline unit of the register-resident GEMM
+// register-resident GEMM: tiles per pipeline unit, MMA row tiles (16
+// channels) per consumer warp, thread blocks per SM
+// (two blocks of 32-channel warps: an SM frees half its room for the next
+// kernel of the stream as soon as one of its blocks ends)
+constexpr int RS_UNIT = 2;
+constexpr int RS_RT = 2;
+constexpr int RS_BPS = 2;
 constexpr int GEMM_SMEM_LIMIT = 227 * 1024;   // opt-in maximum of dynamic shared memory per block
 
 // floor(x * y / z) for 0 <= x <= MAX_CTAS (or a tile index), y, z > 0: in

@@ -76,7 +76,9 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     // Small layers get fewer blocks so that every block streams at least
     // MIN_TILES tiles and an n-block is split between few blocks.
     constexpr int MIN_TILES = 4;
-    int grid = sms;
+    // the register-resident GEMM (4-bit weights, up to 32 rows) runs RS_BPS blocks per SM
+    const bool rs = g.fmt == HQ_W4_ASYM && act_rows(M) <= 32;
+    int grid = rs ? sms * RS_BPS : sms;
     if (exact) {
         // whole n-blocks per block: every output is summed by one block
         if (grid > g.NB) grid = g.NB;
@@ -95,23 +97,24 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.act_bytes = act_tile_code_bytes(M, g.G);
     a.s_bytes = act_tile_sum_bytes(M, g.G, g.fmt);
     a.act_tile_bytes = act_tile_bytes(M, g.G, g.fmt);
-    auto stage_layout = [&](int U, int header) {
+    auto stage_layout = [&](int U, int header, int budget) {
         a.U = U;
         a.act_off = (U * g.tile_bytes + 127) / 128 * 128;
         a.stage_bytes = (a.act_off + U * a.act_tile_bytes + 127) / 128 * 128;
-        // Stage ring: as many units as fit in shared memory beside the barriers.
-        int stages = (GEMM_SMEM_LIMIT - header) / a.stage_bytes;
+        // Stage ring: as many units as fit in the block's shared memory beside the barriers.
+        int stages = (budget - header) / a.stage_bytes;
         if (stages > MAX_STAGES) stages = MAX_STAGES;
         if (stages < 2) stages = 2;
         a.stages = stages;
-        return header + (size_t)stages * a.stage_bytes <= (size_t)GEMM_SMEM_LIMIT;
+        return header + (size_t)stages * a.stage_bytes <= (size_t)budget;
     };
-    if (g.fmt == HQ_W4_ASYM && MT <= 32) {
+    if (rs) {
         // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows of
         // 4-bit weights, where the per-group fold of every output is a few
         // register operations.  Units of four tiles.
         a.V = a.na = a.nd = 0;
-        if (!stage_layout(RS_UNIT, 1024)) return cudaErrorInvalidConfiguration;
+        // the SM's 228 KB of shared memory, less 1 KB per block, shared by RS_BPS blocks
+        if (!stage_layout(RS_UNIT, 1024, 228 * 1024 / RS_BPS - 1024)) return cudaErrorInvalidConfiguration;
         return launch_gemm_w4_rs(a, pdl, s);
     }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
@@ -138,7 +141,7 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     a.V = V;
     a.na = na;
     a.nd = nd;
-    if (!stage_layout(U, 2048) || nd < 2 || na * U * acols + nd * V * dc > TMEM_COLS)
+    if (!stage_layout(U, 2048, GEMM_SMEM_LIMIT) || nd < 2 || na * U * acols + nd * V * dc > TMEM_COLS)
         return cudaErrorInvalidConfiguration;
     return g.fmt == HQ_W4_ASYM ? launch_gemm_w4(a, pdl, s) : launch_gemm_w8(a, pdl, s);
 }

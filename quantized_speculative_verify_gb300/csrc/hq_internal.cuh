@@ -38,7 +38,7 @@ namespace hq {
 // N and K are padded up to whole tiles with zero codes and zero scales.
 // ---------------------------------------------------------------------------
 constexpr int BN = 128;           // output channels per tile (= TMEM lanes)
-constexpr int MAX_CTAS = 160;     // upper bound on GEMM thread blocks (one per SM; workspace sizing)
+constexpr int MAX_CTAS = 320;     // upper bound on GEMM thread blocks (up to two per SM; workspace sizing)
 constexpr int MAX_M = HQ_MAX_M;
 
 struct Geom {

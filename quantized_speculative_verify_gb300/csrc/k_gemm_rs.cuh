@@ -50,7 +50,7 @@
 namespace hq {
 
 
-constexpr int RS_CONSUMERS = 8;                      // consumer warps, 16 channels each
+constexpr int RS_CONSUMERS = 8 / RS_RT;              // consumer warps: the tile's 128 channels
 constexpr int RS_THREADS = (2 + RS_CONSUMERS) * 32;  // + the two producers
 
 // D (+)= A (16 x 16 fp16, row-major) x B (16 x 8 fp16, column-major).  A
@@ -92,7 +92,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
 // MT: token rows (16 or 32); G: quantization group (16 .. 256), fixed at
 // compile time so that a tile's K steps and groups unroll completely.
 template <int MT, int G, bool EXACT>
-__global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs a) {
+__global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const GemmArgs a) {
     constexpr int NT = MT / 8;             // MMA column tiles of tokens
     constexpr int KT = G > 128 ? G : 128;  // features per tile
     constexpr int GPT = KT / G;            // groups per tile
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
 
     // ------------------------------------------------------------ consumers ---
     pdl_wait();
-    const int cw = warp - 2;                  // consumer warp: channels 16 cw .. 16 cw + 15
+    const int cw = warp - 2;                  // consumer warp: channels 16 RT cw .. 16 RT (cw + 1) - 1
     const int ctid = threadIdx.x - 64;        // consumer thread 0 .. RS_CONSUMERS * 32 - 1
     const int g = lane >> 2, tig = lane & 3;  // MMA lane coordinates
     const int M = a.M, KTILES = a.KTILES;
@@ -149,10 +149,11 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
     const int first_b = blk.t0 / KTILES;
     const int mark_old = gemm_zero_outputs(a, blk, ctid, RS_CONSUMERS * 32, 1);
 
-    // y[n][e]: channel 16 cw + g + 8 (e >> 1), token 8 n + 2 tig + (e & 1)
-    float y[NT][4];
+    constexpr int RT = RS_RT;
+    // y[r][n][e]: channel 16 (RT cw + r) + g + 8 (e >> 1), token 8 n + 2 tig + (e & 1)
+    float y[RT][NT][4];
     int eb = blk.t0 / KTILES, ekt = blk.t0 - eb * KTILES, seg_k0 = ekt;
-    const int ch0 = 16 * cw + g;  // the lane's channels: ch0, ch0 + 8
+    const int chw = 16 * RT * cw + g;  // the lane's channels: chw + 16 r, + 8
 
     // lane's ldmatrix row within a 4-matrix load: matrix (lane >> 3) holds
     // features +0..7 / +8..15 (bit 0) of tokens +0..7 / +8..15 (bit 1)
@@ -172,82 +173,93 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
             if (i == 0 || ekt == 0) {
                 seg_k0 = ekt;
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int r = 0; r < RT; ++r)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) y[n][e] = 0.0f;
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) y[r][n][e] = 0.0f;
             }
             const uint8_t *tile = stage + (size_t)j * a.tile_bytes;
             const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);  // scales [channel][GPT]
             const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;                // zero nibbles [channel * GPT + g]
             const uint32_t act_s = smem_addr(stage + a.act_off + (size_t)j * a.act_tile_bytes);
-            // the lane's two channels' 32-feature chunks: [KT / 32][BN][16 B]
-            const uint4 *wc0 = reinterpret_cast<const uint4 *>(tile) + ch0;
+            // the lane's channels' 32-feature chunks: [KT / 32][BN][16 B]
+            const uint4 *wc0 = reinterpret_cast<const uint4 *>(tile) + chw;
             // the current 32-feature chunk of each channel (two 16-feature steps,
             // which may belong to two groups)
-            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+            uint4 wq[RT][2];
 #pragma unroll
             for (int gl = 0; gl < GPT; ++gl) {
                 // zero points -> the widening's additive constants; scales
-                uint32_t zadd[2];
-                float sc[2];
+                uint32_t zadd[RT][2];
+                float sc[RT][2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int zi = (ch0 + 8 * h) * GPT + gl;
-                    const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
-                    zadd[h] = (zbase + z * zmul) * 0x10001u;
-                    sc[h] = tsc[zi];
-                }
-                float acc[NT][4];
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int zi = (chw + 16 * r + 8 * h) * GPT + gl;
+                        const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
+                        zadd[r][h] = (zbase + z * zmul) * 0x10001u;
+                        sc[r][h] = tsc[zi];
+                    }
+                float acc[RT][NT][4];
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int s = gl * KS + ks;  // 16-feature step of the tile
-                    if ((s & 1) == 0) {
-                        w0 = wc0[(s >> 1) * BN];
-                        w1 = wc0[(s >> 1) * BN + 8];
-                    }
-                    // A: rows g, g + 8 (channels ch0, ch0 + 8), features 2 tig.. and 2 tig + 8..
-                    const uint32_t lo0 = (s & 1) ? w0.z : w0.x, hi0 = (s & 1) ? w0.w : w0.y;
-                    const uint32_t lo1 = (s & 1) ? w1.z : w1.x, hi1 = (s & 1) ? w1.w : w1.y;
-                    uint32_t A[4];
-                    A[0] = widen2(lo0, wsel, wmask, wmul, zadd[0]);
-                    A[1] = widen2(lo1, wsel, wmask, wmul, zadd[1]);
-                    A[2] = widen2(hi0, wsel, wmask, wmul, zadd[0]);
-                    A[3] = widen2(hi1, wsel, wmask, wmul, zadd[1]);
                     // B: tokens' fp16 codes, features 16 s ..: block s / 8, chunks 2 (s % 8), + 1
                     const uint32_t b_s = act_s + (uint32_t)((s >> 3) * (MT * 256) + ((s & 7) * 2) * (MT * 16));
+                    uint32_t bq[NT / 2][4];
 #pragma unroll
-                    for (int n2 = 0; n2 < NT; n2 += 2) {
-                        uint32_t bq[4];
-                        ldmatrix_x4(bq, b_s + lrow_off + (uint32_t)(n2 * 8 * 16));
-                        if (ks == 0) {
-                            mma_f16_zero(acc[n2], A, bq[0], bq[1]);
-                            mma_f16_zero(acc[n2 + 1], A, bq[2], bq[3]);
-                        } else {
-                            mma_f16_acc(acc[n2], A, bq[0], bq[1]);
-                            mma_f16_acc(acc[n2 + 1], A, bq[2], bq[3]);
+                    for (int n2 = 0; n2 < NT; n2 += 2) ldmatrix_x4(bq[n2 / 2], b_s + lrow_off + (uint32_t)(n2 * 8 * 16));
+#pragma unroll
+                    for (int r = 0; r < RT; ++r) {
+                        if ((s & 1) == 0) {
+                            wq[r][0] = wc0[(s >> 1) * BN + 16 * r];
+                            wq[r][1] = wc0[(s >> 1) * BN + 16 * r + 8];
+                        }
+                        // A: rows g, g + 8 (channels chw + 16 r, + 8), features 2 tig.. and 2 tig + 8..
+                        const uint4 &w0 = wq[r][0], &w1 = wq[r][1];
+                        const uint32_t lo0 = (s & 1) ? w0.z : w0.x, hi0 = (s & 1) ? w0.w : w0.y;
+                        const uint32_t lo1 = (s & 1) ? w1.z : w1.x, hi1 = (s & 1) ? w1.w : w1.y;
+                        uint32_t A[4];
+                        A[0] = widen2(lo0, wsel, wmask, wmul, zadd[r][0]);
+                        A[1] = widen2(lo1, wsel, wmask, wmul, zadd[r][1]);
+                        A[2] = widen2(hi0, wsel, wmask, wmul, zadd[r][0]);
+                        A[3] = widen2(hi1, wsel, wmask, wmul, zadd[r][1]);
+#pragma unroll
+                        for (int n2 = 0; n2 < NT; n2 += 2) {
+                            if (ks == 0) {
+                                mma_f16_zero(acc[r][n2], A, bq[n2 / 2][0], bq[n2 / 2][1]);
+                                mma_f16_zero(acc[r][n2 + 1], A, bq[n2 / 2][2], bq[n2 / 2][3]);
+                            } else {
+                                mma_f16_acc(acc[r][n2], A, bq[n2 / 2][0], bq[n2 / 2][1]);
+                                mma_f16_acc(acc[r][n2 + 1], A, bq[n2 / 2][2], bq[n2 / 2][3]);
+                            }
                         }
                     }
                 }
                 // fold the group: y += scale * P (P exact in acc)
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int r = 0; r < RT; ++r)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float s_ch = sc[e >> 1];
-                        if constexpr (EXACT) {
-                            if (a.partials) {
-                                const int tok = 8 * n + 2 * tig + (e & 1);
-                                const int nn = eb * BN + ch0 + 8 * (e >> 1);
-                                const int gq = ekt * GPT + gl;
-                                if (tok < M && nn < a.N && gq < a.NGK)
-                                    a.partials[((size_t)tok * a.N + nn) * a.NGK + gq] = __float2int_rn(acc[n][e]);
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float s_ch = sc[r][e >> 1];
+                            if constexpr (EXACT) {
+                                if (a.partials) {
+                                    const int tok = 8 * n + 2 * tig + (e & 1);
+                                    const int nn = eb * BN + chw + 16 * r + 8 * (e >> 1);
+                                    const int gq = ekt * GPT + gl;
+                                    if (tok < M && nn < a.N && gq < a.NGK)
+                                        a.partials[((size_t)tok * a.N + nn) * a.NGK + gq] = __float2int_rn(acc[r][n][e]);
+                                }
+                                // y += scale * P: product rounded, then sum rounded
+                                y[r][n][e] = __fadd_rn(y[r][n][e], __fmul_rn(s_ch, acc[r][n][e]));
+                            } else {
+                                y[r][n][e] = fmaf(s_ch, acc[r][n][e], y[r][n][e]);
                             }
-                            // y += scale * P: product rounded, then sum rounded
-                            y[n][e] = __fadd_rn(y[n][e], __fmul_rn(s_ch, acc[n][e]));
-                        } else {
-                            y[n][e] = fmaf(s_ch, acc[n][e], y[n][e]);
                         }
-                    }
             }
             // end of an n-block segment?
             if (ekt == KTILES - 1 || i == blk.ntl - 1) {
@@ -269,12 +281,15 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_verify_gemm_rs(const GemmArgs
                     ++nsplit;
                 }
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int r = 0; r < RT; ++r)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int nl = ch0 + 8 * (e >> 1);
-                        gemm_segment_out(a, kind, slot_base, 8 * n + 2 * tig + (e & 1), nl, eb * BN + nl, y[n][e]);
-                    }
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int nl = chw + 16 * r + 8 * (e >> 1);
+                            gemm_segment_out(a, kind, slot_base, 8 * n + 2 * tig + (e & 1), nl, eb * BN + nl,
+                                             y[r][n][e]);
+                        }
             }
             if (++ekt == KTILES) {
                 ekt = 0;
