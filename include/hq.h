@@ -119,7 +119,7 @@ size_t hq_packed_bytes(const hq_layer_desc *desc);
 /* Size in bytes of the workspace hq_verify_gemm needs for `desc` and M rows
  * (0 if the arguments are invalid).  The workspace holds the device error
  * word, the split-K partial sums (two slots of 128 channels x 128 rows per
- * thread block, up to 320 blocks: 40 MiB) and two counters per 128 output
+ * thread block, up to 480 blocks: 60 MiB) and two counters per 128 output
  * channels, at offsets
  * that depend on neither the layer nor M: one workspace of the largest size
  * serves calls of every layer and M in turn (calls that may overlap on the
@@ -255,7 +255,7 @@ int hq_workspace_status(void *workspace, void *stream);
  * synchronize the device.  The pages have no counterpart of this call.
  *
  * The scratch lives in one file-scope device array of
- * HQ_NOALLOC_SCRATCH_BYTES (40 MiB + 128 KiB) that every GPU which loads the
+ * HQ_NOALLOC_SCRATCH_BYTES (60 MiB + 128 KiB) that every GPU which loads the
  * library holds until the process exits.  A call is accepted when
  * hq_workspace_bytes(desc, M) fits in it (any M, for N up to about two
  * million outputs); larger calls return HQ_ERR_UNSUPPORTED and launch
@@ -273,7 +273,7 @@ int hq_workspace_status(void *workspace, void *stream);
  * race and must be serialized by the caller.  Arguments, outputs and flags
  * are those of hq_verify_gemm; HQ_LAUNCH_PDL works as there (nothing runs
  * between the previous kernel and the GEMM). */
-#define HQ_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u + 128u * 1024u)
+#define HQ_NOALLOC_SCRATCH_BYTES (60u * 1024u * 1024u + 128u * 1024u)
 int hq_verify_gemm_noalloc(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx,
                            int32_t M, float *Y, int32_t *partials, uint32_t flags, void *stream);
 

@@ -69,12 +69,15 @@ constexpr int ZERO_MARK = 1 << 24;
 
 constexpr int MAX_STAGES = 32;
 // register-resident GEMM: tiles per pipeline unit, MMA row tiles (16
-// channels) per consumer warp, thread blocks per SM
-// (two blocks of 32-channel warps: an SM frees half its room for the next
-// kernel of the stream as soon as one of its blocks ends)
+// channels) per consumer warp, thread blocks per SM for MT token rows.
+// Three blocks of one producer and four 32-channel consumer warps at 16 rows:
+// twelve consumer warps per SM hide the MMA and shared-memory latencies, and
+// an SM frees a third of its room for the next kernel of the stream as soon
+// as one of its blocks ends.  At 32 rows the sums of a warp need more than
+// the 128 registers a thread has at three blocks: two blocks.
 constexpr int RS_UNIT = 2;
 constexpr int RS_RT = 2;
-constexpr int RS_BPS = 2;
+__host__ __device__ constexpr int rs_bps(int MT) { return MT <= 16 ? 3 : 2; }
 constexpr int GEMM_SMEM_LIMIT = 227 * 1024;   // opt-in maximum of dynamic shared memory per block
 
 // floor(x * y / z) for 0 <= x <= MAX_CTAS (or a tile index), y, z > 0: in
@@ -236,6 +239,72 @@ __device__ __forceinline__ void gemm_act_producer(const GemmArgs &a, const GemmB
             for (int j = 0; j < b.unit_tiles(u); ++j) check(u * b.U + j);
         ps.next(b.S);
     }
+}
+
+// Both streams from one lane: the weight copies of the first `prefetch` units
+// before waiting for the previous kernel of the stream, their activation
+// copies after it, then unit by unit as stages free up: the unit's weights,
+// then its activations (one copy per run of consecutive K tiles).  Split
+// segments are counted as in gemm_act_producer.
+__device__ __forceinline__ void gemm_producer(const GemmArgs &a, const GemmBlock &b, int prefetch) {
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    const int S = b.S, KTILES = b.KTILES;
+    auto copy_weights = [&](int u, int st) {
+        const uint32_t fb = smem_addr(&b.full[st]);
+        const int nt = b.unit_tiles(u);
+        mbar_arrive_expect_tx(fb, (uint32_t)(nt * a.tile_bytes));
+        bulk_copy_g2s(smem_addr(b.ring + (size_t)st * a.stage_bytes),
+                      a.blob + (size_t)(b.t0 + u * b.U) * (size_t)a.tile_bytes, (uint32_t)(nt * a.tile_bytes), fb, pol_w);
+    };
+    auto copy_acts = [&](int u, int st) {
+        uint8_t *dst = b.ring + (size_t)st * a.stage_bytes + a.act_off;
+        const uint32_t fb = smem_addr(&b.full[st]);
+        const int nt = b.unit_tiles(u);
+        mbar_arrive_expect_tx(fb, (uint32_t)(nt * a.act_tile_bytes));
+        for (int j = 0; j < nt;) {
+            const int kt = (b.t0 + u * b.U + j) % KTILES;
+            const int run = nt - j < KTILES - kt ? nt - j : KTILES - kt;
+            bulk_copy_g2s(smem_addr(dst + (size_t)j * a.act_tile_bytes), a.qop + (size_t)kt * a.act_tile_bytes,
+                          (uint32_t)(run * a.act_tile_bytes), fb, pol_a);
+            j += run;
+        }
+    };
+    int nsplit = 0;
+    auto check = [&](int j) {
+        const int t = b.t0 + j, bb = t / KTILES, kb = t - bb * KTILES;
+        if (!((kb == KTILES - 1 || j == b.ntl - 1) && !(bb * KTILES >= b.t0 && kb == KTILES - 1))) return;
+        if (!(b.zeroer && bb == b.zb)) {
+            const int nc = cta_of_tile(bb * KTILES + KTILES - 1, a.T, a.grid) - cta_of_tile(bb * KTILES, a.T, a.grid) + 1;
+            const int v = atom_add_acquire_gpu(&b.ctr[bb], 1);
+            if (v < ZERO_MARK) wait_mark_bounded(&b.ctr[bb], ZERO_MARK, v + 1, b.err, a.wait_ns);
+            if (v == ZERO_MARK + nc - 1) atomicExch(&b.ctr[bb], 0);
+        }
+        st_release_cta_shared(smem_addr(&b.sflag[nsplit]), 1);
+        ++nsplit;
+    };
+    int u = 0;
+    for (; u < b.nunits && u < S && u < prefetch; ++u) copy_weights(u, u);
+    pdl_wait();
+    for (int v = 0; v < u; ++v) {
+        copy_acts(v, v);
+        if (!b.det)
+            for (int j = 0; j < b.unit_tiles(v); ++j) check(v * b.U + j);
+    }
+    RingPos ps{u % S, (uint32_t)((u / S) & 1)};
+    for (; u < b.nunits; ++u) {
+        const int st = ps.slot;
+        if (!mbar_wait_bounded(smem_addr(&b.empty[st]), ps.phase ^ 1u, b.err)) break;
+        copy_weights(u, st);
+        copy_acts(u, st);
+        if (!b.det)
+            for (int j = 0; j < b.unit_tiles(u); ++j) check(u * b.U + j);
+        ps.next(S);
+    }
+    // no copy may still be landing in shared memory when the block exits
+    const int issued = u;
+    for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+        mbar_wait_bounded(smem_addr(&b.full[j % S]), (uint32_t)((j / S) & 1), b.err);
 }
 
 // Accumulating mode, zeroing block: its consumer threads (tid of nthr, named

@@ -76,9 +76,11 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     // Small layers get fewer blocks so that every block streams at least
     // MIN_TILES tiles and an n-block is split between few blocks.
     constexpr int MIN_TILES = 4;
-    // the register-resident GEMM (4-bit weights, up to 32 rows) runs RS_BPS blocks per SM
+    // the register-resident GEMM (4-bit weights, up to 32 rows) runs
+    // rs_bps(rows) blocks per SM
     const bool rs = g.fmt == HQ_W4_ASYM && act_rows(M) <= 32;
-    int grid = rs ? sms * RS_BPS : sms;
+    const int bps = rs ? rs_bps(act_rows(M)) : 1;
+    int grid = sms * bps;
     if (exact) {
         // whole n-blocks per block: every output is summed by one block
         if (grid > g.NB) grid = g.NB;
@@ -111,10 +113,12 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     if (rs) {
         // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows of
         // 4-bit weights, where the per-group fold of every output is a few
-        // register operations.  Units of four tiles.
+        // register operations.  Units of RS_UNIT tiles, or of one tile where
+        // two stages of those do not fit.
         a.V = a.na = a.nd = 0;
-        // the SM's 228 KB of shared memory, less 1 KB per block, shared by RS_BPS blocks
-        if (!stage_layout(RS_UNIT, 1024, 228 * 1024 / RS_BPS - 1024)) return cudaErrorInvalidConfiguration;
+        // the SM's 228 KB of shared memory, less 1 KB per block, shared by its blocks
+        const int budget = 228 * 1024 / bps - 1024;
+        if (!stage_layout(RS_UNIT, 1024, budget) && !stage_layout(1, 1024, budget)) return cudaErrorInvalidConfiguration;
         return launch_gemm_w4_rs(a, pdl, s);
     }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator

@@ -21,14 +21,17 @@ namespace hq {
 //
 //   codes   4-bit: [c][quarter p 0..1][n][16 bytes]: the 32 features
 //           64c + 32p .. +31 of channel n as four 32-bit words of eight
-//           nibbles; byte b of word j holds feature 8j + b in its low nibble
-//           and feature 8j + 4 + b in its high nibble (so that one mask gives
-//           the four codes 8j..8j+3 as bytes, and a shift and a mask the next
-//           four).
+//           nibbles; nibble i of word t (bits 4i..4i+3) holds feature
+//           2t + 8i and nibble i + 4 feature 2t + 8i + 1, i = 0..3.  Word t
+//           is then exactly what lane t of a quad needs for two 16-feature
+//           MMA steps of one channel (feature pairs 2t, 2t+1 and 2t+8, 2t+9
+//           of each step), and one mask (after a shift by 8 for the second
+//           step) lifts each pair into the two halves of a 32-bit register.
 //           8-bit: [c][quarter p 0..3][n][16 bytes]: features 64c + 16p + e,
 //           e = 0..15, in order.
-//           A GEMM thread owns one channel: it reads 16 contiguous bytes per
-//           quarter and the 32 lanes of a warp read 512 contiguous bytes.
+//           A tcgen05 widening thread owns one channel and reads 16 contiguous
+//           bytes per quarter (the 32 lanes of a warp: 512 contiguous bytes);
+//           an MMA lane reads the one word of its quad position.
 //   scales  [n][group in tile] fp32
 //   zeros   4-bit only: nibble n * GPT + g (low nibble first), uint4
 //
@@ -38,7 +41,7 @@ namespace hq {
 // N and K are padded up to whole tiles with zero codes and zero scales.
 // ---------------------------------------------------------------------------
 constexpr int BN = 128;           // output channels per tile (= TMEM lanes)
-constexpr int MAX_CTAS = 320;     // upper bound on GEMM thread blocks (up to two per SM; workspace sizing)
+constexpr int MAX_CTAS = 480;     // upper bound on GEMM thread blocks (up to three per SM; workspace sizing)
 constexpr int MAX_M = HQ_MAX_M;
 
 struct Geom {

@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     auto op_off = [&](int idx) -> size_t {
         const int f = idx * 4;
         const int kb = f / ACT_BLOCK, fb = f % ACT_BLOCK;
-        const size_t blk = (size_t)(kb / bpt) * tb + (size_t)(kb % bpt) * MT * 256;
+        const int kt = bpt == 1 ? kb : kb >> 1, kbi = bpt == 1 ? 0 : kb & 1;  // bpt is 1 or 2
+        const size_t blk = (size_t)kt * tb + (size_t)kbi * MT * 256;
         if (e4) return blk + ((size_t)(fb / 16) * 2 * MT + row) * 16 + (size_t)(fb % 16);
         return blk + ((size_t)(fb / 8) * MT + row) * 16 + (size_t)(fb % 8) * 2;
     };

@@ -80,25 +80,29 @@ constexpr int MAX_ND = 16;                    // accumulator slots in TMEM
 // blocks of the kernel share an SM (each takes all of its TMEM).
 constexpr int MIN_GEMM_SMEM = 120 * 1024;
 
-// Eight 4-bit codes (byte b: features b and b + 4) -> the e4m3 bytes of
-// features 0..3 and 4..7.
-__device__ __forceinline__ void widen_w4_e4(uint32_t w, uint32_t *o) {
-    o[0] = w & 0x0F0F0F0Fu;
-    o[1] = (w >> 4) & 0x0F0F0F0Fu;
+// Words t and t + 1 (t even) of a 32-feature run (nibble i of word t: feature
+// 2t + 8i, nibble i + 4: feature 2t + 8i + 1) -> the e4m3 bytes of features
+// 2t + 8i .. 2t + 8i + 3 in o[t / 2 + 2i], i = 0..3.  A byte permute gathers
+// the four bytes holding each feature quad's low (then high) nibbles.
+__device__ __forceinline__ void widen_w4_e4(uint32_t w0, uint32_t w1, int t, uint32_t *o) {
+    uint32_t p, q;
+    asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(p) : "r"(w0), "r"(w1));  // bytes 0, 2 of each
+    asm("prmt.b32 %0, %1, %2, 0x7531;" : "=r"(q) : "r"(w0), "r"(w1));  // bytes 1, 3 of each
+    o[t / 2 + 0] = p & 0x0F0F0F0Fu;
+    o[t / 2 + 2] = (p >> 4) & 0x0F0F0F0Fu;
+    o[t / 2 + 4] = q & 0x0F0F0F0Fu;
+    o[t / 2 + 6] = (q >> 4) & 0x0F0F0F0Fu;
 }
 
-// Eight 4-bit codes (byte b: features b and b + 4) -> four fp16x2 (64 + q),
-// features (0,1) (2,3) (4,5) (6,7): a code at bits 4..7 of a 16-bit half
+// Word t of a 32-feature run -> four fp16x2 (64 + q) of the feature pairs
+// (2t + 8i, 2t + 8i + 1) in o[t + 4i]: a code at bits 4..7 of a 16-bit half
 // under the exponent bits 0x5400 (fp16 64, ulp 1/16) reads 64 + q.
-__device__ __forceinline__ void widen_w4_f16(uint32_t w, uint32_t *o) {
+__device__ __forceinline__ void widen_w4_f16(uint32_t w, int t, uint32_t *o) {
     constexpr uint32_t M4 = 0x00F000F0u, E64 = 0x54005400u;
-    uint32_t y01, y23;  // bytes (0, -, 1, -) and (2, -, 3, -)
-    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(y01) : "r"(w));
-    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(y23) : "r"(w));
-    o[0] = ((y01 << 4) & M4) | E64;  // features 0, 1
-    o[1] = ((y23 << 4) & M4) | E64;  // 2, 3
-    o[2] = (y01 & M4) | E64;         // 4, 5
-    o[3] = (y23 & M4) | E64;         // 6, 7
+    o[t + 0] = ((w << 4) & M4) | E64;
+    o[t + 4] = (w & M4) | E64;
+    o[t + 8] = ((w >> 4) & M4) | E64;
+    o[t + 12] = ((w >> 8) & M4) | E64;
 }
 
 // Four int8 codes -> two fp16x2 q: bias to unsigned, place under the fp16
@@ -288,10 +292,8 @@ __global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmA
 #pragma unroll
                             for (int p = 0; p < 2; ++p) {
                                 uint32_t *o = v + 16 * cc + 8 * p;
-                                widen_w4_e4(uu[p].x, o + 0);
-                                widen_w4_e4(uu[p].y, o + 2);
-                                widen_w4_e4(uu[p].z, o + 4);
-                                widen_w4_e4(uu[p].w, o + 6);
+                                widen_w4_e4(uu[p].x, uu[p].y, 0, o);
+                                widen_w4_e4(uu[p].z, uu[p].w, 2, o);
                             }
                         }
                         tmem_st32(tbase + lane_field + a_col + (uint32_t)(c * 16), v);
@@ -306,10 +308,10 @@ __global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmA
                                 uu[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 2 + p) * BN + n) * 16);
 #pragma unroll
                             for (int p = 0; p < 2; ++p) {
-                                widen_w4_f16(uu[p].x, v + 16 * p + 0);
-                                widen_w4_f16(uu[p].y, v + 16 * p + 4);
-                                widen_w4_f16(uu[p].z, v + 16 * p + 8);
-                                widen_w4_f16(uu[p].w, v + 16 * p + 12);
+                                widen_w4_f16(uu[p].x, 0, v + 16 * p);
+                                widen_w4_f16(uu[p].y, 1, v + 16 * p);
+                                widen_w4_f16(uu[p].z, 2, v + 16 * p);
+                                widen_w4_f16(uu[p].w, 3, v + 16 * p);
                             }
                         } else {
                             uint4 uu[4];

@@ -20,14 +20,15 @@
 // the activation codes, where the e4m3 forms on this GPU take several.
 //
 // Channels are the MMA's M (16 per warp), tokens its N (8 per MMA), so the
-// weights are the A operand.  A lane widens its four codes of one MMA step
-// and one channel in three instructions: a byte permute picks the two bytes
-// holding them (the packed layout puts features 8w .. 8w + 3 in the low
-// nibbles of word w, 8w + 4 .. 8w + 7 in its high nibbles), a mask under the
-// fp16 exponent bits of 1024 makes 1024 + q (low nibbles) or 1024 + 16 q
-// (high nibbles), and one fused multiply-add by 1 or 1/16 subtracts 1024 + z
-// or 64 + z, exactly.  The activation codes come from the operand's fp16
-// blocks through ldmatrix.
+// weights are the A operand.  The packed layout gives lane t of a quad one
+// 32-bit word per channel and 32 features: the feature pairs (2t, 2t + 1)
+// and (2t + 8, 2t + 9) of two 16-feature MMA steps, one pair per nibble
+// column.  A mask lifts a pair into the two halves of a register under the
+// fp16 exponent bits of 1024, which reads 1024 + q (low nibbles) or
+// 1024 + 16 q (high nibbles); one fp16 add of -(1024 + z), or a multiply-add
+// by 1/16 and -(64 + z), leaves q - z exactly.  Eight codes cost nine
+// instructions (four masks, a shift for the second step, four adds).  The
+// activation codes come from the operand's fp16 blocks through ldmatrix.
 //
 // Fold of a group into the running sums, in the oracle's ascending group
 // order: y += scale * P.  Exact-order and check modes round the multiply and
@@ -35,10 +36,11 @@
 // check mode); otherwise one fused multiply-add, within the fp32 tolerance of
 // the oracle.
 //
-// Thread block: warp 0 streams the weight tiles, warp 1 the activation K
-// tiles (gemm_common.cuh), warps 2..9 compute.  Consumer warp w owns channels
-// 16 w .. 16 w + 15 of every tile and every token; it needs no other warp
-// between a stage's arrival and its release.
+// Thread block: one lane of warp 0 streams the weight tiles and the
+// activation K tiles (gemm_common.cuh), warps 1..4 compute, three blocks per
+// SM.  Consumer warp w owns channels 32 w .. 32 w + 31 of every tile (two MMA
+// row tiles) and every token; it needs no other warp between a stage's
+// arrival and its release.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -51,7 +53,7 @@ namespace hq {
 
 
 constexpr int RS_CONSUMERS = 8 / RS_RT;              // consumer warps: the tile's 128 channels
-constexpr int RS_THREADS = (2 + RS_CONSUMERS) * 32;  // + the two producers
+constexpr int RS_THREADS = (1 + RS_CONSUMERS) * 32;  // + the producer
 
 // D (+)= A (16 x 16 fp16, row-major) x B (16 x 8 fp16, column-major).  A
 // function of its registers alone (not volatile): the compiler may move the
@@ -70,14 +72,19 @@ __device__ __forceinline__ void mma_f16_zero(float (&d)[4], const uint32_t (&A)[
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(b0), "r"(b1), "f"(z));
 }
-// Two 4-bit codes -> fp16x2 (q - z): the selected bytes' nibbles under the
-// exponent bits of 1024, then x * mul + add with (mul, add) = (1, -(1024 + z))
-// for low nibbles or (1/16, -(64 + z)) for high ones.
-__device__ __forceinline__ uint32_t widen2(uint32_t w, uint32_t sel, uint32_t mask, uint32_t mul, uint32_t add) {
-    uint32_t x, r;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
-    x = (x & mask) | 0x64006400u;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(mul), "r"(add));
+// The pair in nibbles (0, 4) of each half-word (bits 0..3, 16..19) ->
+// fp16x2 (q - z), zlo = fp16x2(-(1024 + z)).
+__device__ __forceinline__ uint32_t widen_lo(uint32_t w, uint32_t zlo) {
+    const uint32_t x = (w & 0x000F000Fu) | 0x64006400u;
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(zlo));
+    return r;
+}
+// The pair at bits 4..7, 20..23 -> fp16x2 (q - z), zhi = fp16x2(-(64 + z)).
+__device__ __forceinline__ uint32_t widen_hi(uint32_t w, uint32_t zhi) {
+    const uint32_t x = (w & 0x00F000F0u) | 0x64006400u;
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(zhi));  // x / 16 - (64 + z)
     return r;
 }
 // four 8 x 16-byte row blocks of shared memory, one row address per lane
@@ -92,7 +99,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
 // MT: token rows (16 or 32); G: quantization group (16 .. 256), fixed at
 // compile time so that a tile's K steps and groups unroll completely.
 template <int MT, int G, bool EXACT>
-__global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const GemmArgs a) {
+__global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const GemmArgs a) {
     constexpr int NT = MT / 8;             // MMA column tiles of tokens
     constexpr int KT = G > 128 ? G : 128;  // features per tile
     constexpr int GPT = KT / G;            // groups per tile
@@ -119,31 +126,18 @@ __global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const Gem
     pdl_launch_dependents();
 
     if (warp == 0) {
-        if (lane == 0) gemm_weight_producer(a, blk);
-        return;
-    }
-    if (warp == 1) {
-        if (lane == 0) gemm_act_producer(a, blk);
+        // two stages of weights before the dependency wait
+        if (lane == 0) gemm_producer(a, blk, 2);
         return;
     }
 
     // ------------------------------------------------------------ consumers ---
     pdl_wait();
-    const int cw = warp - 2;                  // consumer warp: channels 16 RT cw .. 16 RT (cw + 1) - 1
-    const int ctid = threadIdx.x - 64;        // consumer thread 0 .. RS_CONSUMERS * 32 - 1
+    const int cw = warp - 1;                  // consumer warp: channels 16 RT cw .. 16 RT (cw + 1) - 1
+    const int ctid = threadIdx.x - 32;        // consumer thread 0 .. RS_CONSUMERS * 32 - 1
     const int g = lane >> 2, tig = lane & 3;  // MMA lane coordinates
     const int M = a.M, KTILES = a.KTILES;
     float *wsp = reinterpret_cast<float *>(a.ws + ws_partial_offset());
-    // widening constants of this lane: features 2 tig, 2 tig + 1 of a word
-    // are bytes 2 (tig & 1), + 1, low nibbles for tig < 2, high for tig >= 2
-    const uint32_t b0 = 2u * (uint32_t)(tig & 1);
-    const uint32_t wsel = b0 | (4u << 4) | ((b0 + 1u) << 8) | (4u << 12);
-    const bool hi_nib = tig >= 2;
-    const uint32_t wmask = hi_nib ? 0x00F000F0u : 0x000F000Fu;
-    const uint32_t wmul = hi_nib ? 0x2C002C00u : 0x3C003C00u;  // fp16x2 1/16 or 1
-    // fp16 bits of -(64 + z) = 0xD400 + 16 z, of -(1024 + z) = 0xE400 + z
-    const uint32_t zbase = hi_nib ? 0xD400u : 0xE400u, zmul = hi_nib ? 16u : 1u;
-
     bool ok = true;
     int pend0 = -1, pend1 = -1, nsplit = 0;
     const int first_b = blk.t0 / KTILES;
@@ -183,15 +177,16 @@ __global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const Gem
             const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);  // scales [channel][GPT]
             const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;                // zero nibbles [channel * GPT + g]
             const uint32_t act_s = smem_addr(stage + a.act_off + (size_t)j * a.act_tile_bytes);
-            // the lane's channels' 32-feature chunks: [KT / 32][BN][16 B]
-            const uint4 *wc0 = reinterpret_cast<const uint4 *>(tile) + chw;
-            // the current 32-feature chunk of each channel (two 16-feature steps,
+            // the lane's word of its channels' 32-feature runs: [KT / 32][BN][4 words]
+            const uint32_t *wc0 = reinterpret_cast<const uint32_t *>(tile) + 4 * chw + tig;
+            // the current run's word of each channel (two 16-feature steps,
             // which may belong to two groups)
-            uint4 wq[RT][2];
+            uint32_t wq[RT][2];
 #pragma unroll
             for (int gl = 0; gl < GPT; ++gl) {
-                // zero points -> the widening's additive constants; scales
-                uint32_t zadd[RT][2];
+                // zero points -> the widening's additive constants (fp16 bits of
+                // -(1024 + z) = 0xE400 + z, of -(64 + z) = 0xD400 + 16 z); scales
+                uint32_t zlo[RT][2], zhi[RT][2];
                 float sc[RT][2];
 #pragma unroll
                 for (int r = 0; r < RT; ++r)
@@ -199,7 +194,8 @@ __global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const Gem
                     for (int h = 0; h < 2; ++h) {
                         const int zi = (chw + 16 * r + 8 * h) * GPT + gl;
                         const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
-                        zadd[r][h] = (zbase + z * zmul) * 0x10001u;
+                        zlo[r][h] = z * 0x00010001u + 0xE400E400u;
+                        zhi[r][h] = z * 0x00100010u + 0xD400D400u;
                         sc[r][h] = tsc[zi];
                     }
                 float acc[RT][NT][4];
@@ -214,18 +210,20 @@ __global__ void __launch_bounds__(RS_THREADS, RS_BPS) k_verify_gemm_rs(const Gem
 #pragma unroll
                     for (int r = 0; r < RT; ++r) {
                         if ((s & 1) == 0) {
-                            wq[r][0] = wc0[(s >> 1) * BN + 16 * r];
-                            wq[r][1] = wc0[(s >> 1) * BN + 16 * r + 8];
+                            wq[r][0] = wc0[4 * ((s >> 1) * BN + 16 * r)];
+                            wq[r][1] = wc0[4 * ((s >> 1) * BN + 16 * r + 8)];
                         }
-                        // A: rows g, g + 8 (channels chw + 16 r, + 8), features 2 tig.. and 2 tig + 8..
-                        const uint4 &w0 = wq[r][0], &w1 = wq[r][1];
-                        const uint32_t lo0 = (s & 1) ? w0.z : w0.x, hi0 = (s & 1) ? w0.w : w0.y;
-                        const uint32_t lo1 = (s & 1) ? w1.z : w1.x, hi1 = (s & 1) ? w1.w : w1.y;
+                        // A: rows g, g + 8 (channels chw + 16 r, + 8), features
+                        // 2 tig, + 1 (nibbles 0, 4 of the step's half-words) and
+                        // 2 tig + 8, + 9 (nibbles 1, 5); the odd step's pairs sit
+                        // 8 bits higher
+                        const uint32_t v0 = (s & 1) ? wq[r][0] >> 8 : wq[r][0];
+                        const uint32_t v1 = (s & 1) ? wq[r][1] >> 8 : wq[r][1];
                         uint32_t A[4];
-                        A[0] = widen2(lo0, wsel, wmask, wmul, zadd[r][0]);
-                        A[1] = widen2(lo1, wsel, wmask, wmul, zadd[r][1]);
-                        A[2] = widen2(hi0, wsel, wmask, wmul, zadd[r][0]);
-                        A[3] = widen2(hi1, wsel, wmask, wmul, zadd[r][1]);
+                        A[0] = widen_lo(v0, zlo[r][0]);
+                        A[1] = widen_lo(v1, zlo[r][1]);
+                        A[2] = widen_hi(v0, zhi[r][0]);
+                        A[3] = widen_hi(v1, zhi[r][1]);
 #pragma unroll
                         for (int n2 = 0; n2 < NT; n2 += 2) {
                             if (ks == 0) {

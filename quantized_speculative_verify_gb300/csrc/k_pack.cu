@@ -137,14 +137,15 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
         const uint8_t *src = codes_s + r * KT;
         uint32_t wv[4];
         if (w4) {
-            // word j: features 32 cp + 8 j + e; byte b = feature b | feature b + 4 << 4
+            // word t: nibble i = feature 2 t + 8 i, nibble i + 4 = feature 2 t + 8 i + 1 (i = 0..3)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint8_t *p8 = src + cp * 32 + j * 8;
+            for (int t = 0; t < 4; ++t) {
+                const uint8_t *p8 = src + cp * 32 + 2 * t;
                 uint32_t word = 0;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) word |= ((uint32_t)(p8[b] & 15u) | ((uint32_t)(p8[b + 4] & 15u) << 4)) << (8 * b);
-                wv[j] = word;
+                for (int i = 0; i < 4; ++i)
+                    word |= ((uint32_t)(p8[8 * i] & 15u) << (4 * i)) | ((uint32_t)(p8[8 * i + 1] & 15u) << (4 * i + 16));
+                wv[t] = word;
             }
         } else {
             // features 16 cp + e, e = 0..15, in order
@@ -179,8 +180,8 @@ __global__ void __launch_bounds__(256) k_unpack(Geom g, const uint8_t *__restric
         if (n >= g.N) continue;
         for (int j = 0; j < 4; ++j) {
             if (w4) {
-                for (int i = 0; i < 8; ++i) {  // nibble i: byte i / 2, feature (i / 2) + 4 (i % 2)
-                    const int k = kt * g.KT + cp * 32 + j * 8 + (i >> 1) + 4 * (i & 1);
+                for (int i = 0; i < 8; ++i) {  // nibble i of word j: feature 2 j + 8 (i % 4) + i / 4
+                    const int k = kt * g.KT + cp * 32 + 2 * j + 8 * (i & 3) + (i >> 2);
                     if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
                 }
             } else {

@@ -207,7 +207,7 @@ def hq_selftest_gemm_wait_timeout(desc, blob, qop, sx, M: int, Y, workspace, lim
            "hq_selftest_gemm_wait_timeout")
 
 
-HQ_NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024 + 128 * 1024
+HQ_NOALLOC_SCRATCH_BYTES = 60 * 1024 * 1024 + 128 * 1024
 
 
 def hq_verify_gemm_noalloc(desc, blob, qop, sx, M: int, Y, partials=None, flags: int = 0, stream=None) -> None:

@@ -127,8 +127,8 @@ def test_pack_bit_exact(fmt, K, N, G):
 
 
 # ---------------------------------------------------------------- GEMM ---
-# workspace: 16-byte error word, 320 blocks x 2 slots x 128 x 128 fp32 partial sums, counters
-COUNTER_OFFSET = 16 + 320 * 2 * 128 * 128 * 4
+# workspace: 16-byte error word, 480 blocks x 2 slots x 128 x 128 fp32 partial sums, counters
+COUNTER_OFFSET = 16 + 480 * 2 * 128 * 128 * 4
 
 
 def run_layer(X, W, G, fmt, s_host, check=False, flags=0, layer=None):
