@@ -96,7 +96,7 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     const int MT = act_rows(M);
     const bool e4 = act_e4(g.fmt, M, g.G);
     // stage: U weight tiles, then the U activation K tiles (codes, group sums)
-    a.act_bytes = act_tile_code_bytes(M, g.G);
+    a.act_bytes = act_tile_code_bytes(M, g.G, g.fmt);
     a.s_bytes = act_tile_sum_bytes(M, g.G, g.fmt);
     a.act_tile_bytes = act_tile_bytes(M, g.G, g.fmt);
     auto stage_layout = [&](int U, int header, int budget) {
@@ -245,7 +245,7 @@ int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, co
         (gsum && !aligned(gsum, 4)) || (qop && !aligned(qop, 16)))
         return HQ_ERR_INVALID_ARG;
     const int K = desc->K, G = desc->group;
-    return cuda_status(hq::launch_rotate_quant_act(X, M, K, G, hq::act_e4(desc->format, M, G), hq::act_sums(desc->format, M), signs, qx, gsum,
+    return cuda_status(hq::launch_rotate_quant_act(X, M, K, G, hq::act_rs(desc->format, M), hq::act_e4(desc->format, M, G), hq::act_sums(desc->format, M), signs, qx, gsum,
                                                    static_cast<uint8_t *>(qop), sx, (flags & HQ_LAUNCH_PDL) != 0,
                                                    static_cast<cudaStream_t>(stream)));
 }

@@ -125,16 +125,21 @@ __host__ __device__ inline size_t ws_bytes(const Geom &g) { return ws_counter_of
 // are zero.  It is a sequence of K tiles of KT = max(G, 128) features (the
 // weight blob's K tiles), each holding what one weight tile's MMAs and
 // epilogue read, so that a run of consecutive K tiles is one contiguous copy:
-//   codes, KT / 128 blocks of 128 features, in one of two encodings chosen
-//   by the layers that read the operand (act_e4):
+//   codes, KT / 128 blocks of 128 features, in one of three encodings
+//   chosen by the GEMM that reads the operand (act_rs, act_e4):
+//     fp16 rows (act_rs: the register-resident GEMM, 4-bit weights, up to
+//             32 rows): [MT rows][128 fp16 + 16 bytes of padding]: a row of
+//             272 bytes puts the 16-byte chunk c of the 8 rows of an
+//             ldmatrix in 8 distinct bank quads (272 = 256 + 16), and the
+//             activation kernel writes each row's 256 bytes in one run;
 //     fp16:   [16 chunks of 8 features][MT rows][8 fp16] (exact for
 //             |q| <= 127), the B operand of kind::f16 MMAs;
 //     digits: [8 chunks of 16 features][2 MT rows][16 e4m3]: q = 16 h + l
 //             with l in [-8, 7], h in [-8, 8], both exact in e4m3; row r < MT
 //             holds the l of token r, row MT + r its h: the B operand of
 //             kind::f8f6f4 MMAs whose N covers both digits;
-//   either way a block is the B operand of a tile's MMAs as 8-row x 16-byte
-//   core matrices (K-major, no swizzle), MT * 256 bytes; then, where the
+//   the last two are the B operand of a tile's tcgen05 MMAs as 8-row x
+//   16-byte core matrices (K-major, no swizzle), MT * 256 bytes; then, where the
 //   consuming GEMM needs them (act_sums),
 //   group sums [KT / G groups][MT] fp32: S[g][m] = sum of the int8 codes of
 //   row m over the tile's group g (zero past K).
@@ -155,13 +160,18 @@ __host__ __device__ inline int act_ktiles(int K, int G) { return (K + act_kt(G) 
 // rows).  Up to 32 rows the register-resident GEMM subtracts the zero point
 // while widening the weights; 8-bit weights have none.
 __host__ __device__ inline bool act_sums(int fmt, int M) { return fmt == HQ_W4_ASYM && act_rows(M) > 32; }
-// bytes of one K tile's codes, of its group sums, and of the whole K tile
-__host__ __device__ inline int act_tile_code_bytes(int M, int G) { return (act_kt(G) / ACT_BLOCK) * act_rows(M) * 256; }
+// The row encoding: the operand of the register-resident GEMM.
+__host__ __device__ inline bool act_rs(int fmt, int M) { return fmt == HQ_W4_ASYM && act_rows(M) <= 32; }
+constexpr int ACT_RS_PITCH = 272;  // bytes per row of a 128-feature block in the row encoding
+// bytes of one 128-feature block's codes, of one K tile's codes, of its group
+// sums, and of the whole K tile
+__host__ __device__ inline int act_block_bytes(int M, int fmt) { return act_rows(M) * (act_rs(fmt, M) ? ACT_RS_PITCH : 256); }
+__host__ __device__ inline int act_tile_code_bytes(int M, int G, int fmt) { return (act_kt(G) / ACT_BLOCK) * act_block_bytes(M, fmt); }
 __host__ __device__ inline int act_tile_sum_bytes(int M, int G, int fmt) {
     return act_sums(fmt, M) ? (act_kt(G) / G) * act_rows(M) * 4 : 0;
 }
 __host__ __device__ inline int act_tile_bytes(int M, int G, int fmt) {
-    return act_tile_code_bytes(M, G) + act_tile_sum_bytes(M, G, fmt);
+    return act_tile_code_bytes(M, G, fmt) + act_tile_sum_bytes(M, G, fmt);
 }
 __host__ __device__ inline size_t act_operand_bytes(int M, int K, int G, int fmt) {
     return (size_t)act_ktiles(K, G) * (size_t)act_tile_bytes(M, G, fmt);
@@ -384,7 +394,7 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 
 // Launchers (defined in the kernel translation units).
 namespace hq {
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, bool sums, const uint32_t *signs, int8_t *qx,
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool rs, bool e4, bool sums, const uint32_t *signs, int8_t *qx,
                                     int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s);
 // rows of W -> n-blocks nb0.. of the blob of layer g
 cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,

@@ -60,7 +60,7 @@ __device__ __forceinline__ void digits4(int q0, int q1, int q2, int q3, uint32_t
 }
 
 template <int V, int T>
-__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G, int e4, int sums,
+__global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict__ X, int M, int K, int G, int rs, int e4, int sums,
                                                         const uint32_t *__restrict__ signs, int8_t *__restrict__ qx,
                                                         int32_t *__restrict__ gsum, uint8_t *__restrict__ qop,
                                                         float *__restrict__ sx) {
@@ -79,11 +79,13 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     const int bpt = act_kt(G) / ACT_BLOCK;  // code blocks per K tile
     const int gpt = act_kt(G) / G;          // groups per K tile
     const int ngp = act_ktiles(K, G) * gpt; // groups of the operand, padding included
-    // bytes per K tile: codes, then (where the GEMM reads them) group sums
-    const size_t tb = (size_t)bpt * MT * 256 + (sums ? (size_t)gpt * MT * 4 : 0);
+    // bytes per 128-feature block and per K tile: codes, then (where the GEMM
+    // reads them) group sums
+    const int cb = MT * (rs ? ACT_RS_PITCH : 256);
+    const size_t tb = (size_t)bpt * cb + (sums ? (size_t)gpt * MT * 4 : 0);
     // operand position of group sum g of this row
     auto op_s = [&](int g) -> float * {
-        return reinterpret_cast<float *>(qop + (size_t)(g / gpt) * tb + (size_t)bpt * MT * 256) + (size_t)(g % gpt) * MT + row;
+        return reinterpret_cast<float *>(qop + (size_t)(g / gpt) * tb + (size_t)bpt * cb) + (size_t)(g % gpt) * MT + row;
     };
     // byte offset of the 4 features 4*idx .. 4*idx+3 of this row in the
     // operand: fp16, 8 bytes; digits, 4 bytes of low digits (the high digits
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
         const int f = idx * 4;
         const int kb = f / ACT_BLOCK, fb = f % ACT_BLOCK;
         const int kt = bpt == 1 ? kb : kb >> 1, kbi = bpt == 1 ? 0 : kb & 1;  // bpt is 1 or 2
-        const size_t blk = (size_t)kt * tb + (size_t)kbi * MT * 256;
+        const size_t blk = (size_t)kt * tb + (size_t)kbi * cb;
+        if (rs) return blk + (size_t)row * ACT_RS_PITCH + (size_t)fb * 2;
         if (e4) return blk + ((size_t)(fb / 16) * 2 * MT + row) * 16 + (size_t)(fb % 16);
         return blk + ((size_t)(fb / 8) * MT + row) * 16 + (size_t)(fb % 8) * 2;
     };
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
 }
 
 template <int V, int T>
-cudaError_t launch_act_t(const float *X, int M, int K, int G, bool e4, const uint32_t *signs, int8_t *qx,
+cudaError_t launch_act_t(const float *X, int M, int K, int G, bool rs, bool e4, const uint32_t *signs, int8_t *qx,
                          int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s, bool sums) {
     cudaLaunchConfig_t cfg = {};
     // one block per operand row (rows past M write the operand's zero padding)
@@ -239,26 +242,26 @@ cudaError_t launch_act_t(const float *X, int M, int K, int G, bool e4, const uin
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, e4 ? 1 : 0, sums ? 1 : 0, signs, qx, gsum, qop,
+    return cudaLaunchKernelEx(&cfg, k_rotate_quant_act<V, T>, X, M, K, G, rs ? 1 : 0, e4 ? 1 : 0, sums ? 1 : 0, signs, qx, gsum, qop,
                               sx);
 }
 
 }  // namespace
 
-cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool e4, bool sums, const uint32_t *signs,
+cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool rs, bool e4, bool sums, const uint32_t *signs,
                                     int8_t *qx, int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s) {
     // As many threads per row as the row has float4s, up to 1024: the kernel
     // is latency-bound (one block per row), so the shortest chain per thread
     // wins (256 threads x 4 float4s at K = 4096 made the pass 4% slower).
     const int n4 = K / 4;
-    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
-    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 256 * 1) return launch_act_t<1, 256>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 512 * 1) return launch_act_t<1, 512>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 1) return launch_act_t<1, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 2) return launch_act_t<2, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 3) return launch_act_t<3, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 4) return launch_act_t<4, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
+    if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
     return cudaErrorInvalidValue;
 }
 

@@ -28,7 +28,7 @@
 // 1024 + 16 q (high nibbles); one fp16 add of -(1024 + z), or a multiply-add
 // by 1/16 and -(64 + z), leaves q - z exactly.  Eight codes cost nine
 // instructions (four masks, a shift for the second step, four adds).  The
-// activation codes come from the operand's fp16 blocks through ldmatrix.
+// activation codes come from the operand's fp16 rows through ldmatrix.
 //
 // Fold of a group into the running sums, in the oracle's ascending group
 // order: y += scale * P.  Exact-order and check modes round the multiply and
@@ -150,9 +150,10 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
     const int chw = 16 * RT * cw + g;  // the lane's channels: chw + 16 r, + 8
 
     // lane's ldmatrix row within a 4-matrix load: matrix (lane >> 3) holds
-    // features +0..7 / +8..15 (bit 0) of tokens +0..7 / +8..15 (bit 1)
+    // features +0..7 / +8..15 (bit 0) of tokens +0..7 / +8..15 (bit 1); the
+    // operand's blocks are [MT rows][272 bytes]
     const int lm = lane >> 3, lr = lane & 7;
-    const uint32_t lrow_off = (uint32_t)(((lm & 1) * MT + (lm >> 1) * 8 + lr) * 16);
+    const uint32_t lrow_off = (uint32_t)(((lm >> 1) * 8 + lr) * ACT_RS_PITCH + (lm & 1) * 16);
 
     RingPos ps{0, 0u};
     for (int u = 0; u < blk.nunits; ++u) {
@@ -203,10 +204,11 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
                 for (int ks = 0; ks < KS; ++ks) {
                     const int s = gl * KS + ks;  // 16-feature step of the tile
                     // B: tokens' fp16 codes, features 16 s ..: block s / 8, chunks 2 (s % 8), + 1
-                    const uint32_t b_s = act_s + (uint32_t)((s >> 3) * (MT * 256) + ((s & 7) * 2) * (MT * 16));
+                    const uint32_t b_s = act_s + (uint32_t)((s >> 3) * (MT * ACT_RS_PITCH) + (s & 7) * 32);
                     uint32_t bq[NT / 2][4];
 #pragma unroll
-                    for (int n2 = 0; n2 < NT; n2 += 2) ldmatrix_x4(bq[n2 / 2], b_s + lrow_off + (uint32_t)(n2 * 8 * 16));
+                    for (int n2 = 0; n2 < NT; n2 += 2)
+                        ldmatrix_x4(bq[n2 / 2], b_s + lrow_off + (uint32_t)(n2 * 8 * ACT_RS_PITCH));
 #pragma unroll
                     for (int r = 0; r < RT; ++r) {
                         if ((s & 1) == 0) {
