@@ -70,12 +70,15 @@ constexpr int ZERO_MARK = 1 << 24;
 constexpr int MAX_STAGES = 32;
 // register-resident GEMM: tiles per pipeline unit, MMA row tiles (16
 // channels) per consumer warp, thread blocks per SM for MT token rows.
+// Units of one tile: a block's consumers start on its first tile as soon as
+// that tile is in, and the ring holds more, smaller stages (verify pass 2.204
+// -> 2.145 ms against units of two).
 // Three blocks of one producer and four 32-channel consumer warps at 16 rows:
 // twelve consumer warps per SM hide the MMA and shared-memory latencies, and
 // an SM frees a third of its room for the next kernel of the stream as soon
 // as one of its blocks ends.  At 32 rows the sums of a warp need more than
 // the 128 registers a thread has at three blocks: two blocks.
-constexpr int RS_UNIT = 2;
+constexpr int RS_UNIT = 1;
 constexpr int RS_RT = 2;
 __host__ __device__ constexpr int rs_bps(int MT) { return MT <= 16 ? 3 : 2; }
 constexpr int GEMM_SMEM_LIMIT = 227 * 1024;   // opt-in maximum of dynamic shared memory per block

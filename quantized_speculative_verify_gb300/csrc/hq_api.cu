@@ -113,12 +113,11 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     if (rs) {
         // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows of
         // 4-bit weights, where the per-group fold of every output is a few
-        // register operations.  Units of RS_UNIT tiles, or of one tile where
-        // two stages of those do not fit.
+        // register operations.  Units of RS_UNIT tiles.
         a.V = a.na = a.nd = 0;
         // the SM's 228 KB of shared memory, less 1 KB per block, shared by its blocks
         const int budget = 228 * 1024 / bps - 1024;
-        if (!stage_layout(RS_UNIT, 1024, budget) && !stage_layout(1, 1024, budget)) return cudaErrorInvalidConfiguration;
+        if (!stage_layout(RS_UNIT, 1024, budget)) return cudaErrorInvalidConfiguration;
         return launch_gemm_w4_rs(a, pdl, s);
     }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
