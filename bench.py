@@ -272,7 +272,8 @@ def gemm_source_parts(csrc: str) -> list:
     def read(f):
         with open(os.path.join(csrc, f)) as fh:
             return fh.read()
-    parts = [read("k_gemm.cuh"), read("k_gemm_w4.cu"), read("k_gemm_w8.cu")]
+    parts = [read("k_gemm.cuh"), read("k_gemm_w4.cu"), read("k_gemm_w8.cu"), read("gemm_common.cuh"),
+             read("k_gemm_rs.cuh"), read("k_gemm_rs.cu")]
     internal = read("hq_internal.cuh")
     parts.append(internal.split("// Launchers (defined in the kernel translation units).")[0])
     api = read("hq_api.cu")
@@ -286,6 +287,13 @@ def kernel_source_hash() -> str:
     for part in gemm_source_parts(os.path.join(ROOT, "quantized_speculative_verify_gb300", "csrc")):
         h.update(part.encode())
     return h.hexdigest()[:16]
+
+
+def gemm_kernel_name(fmt: str, M: int) -> str:
+    """The GEMM kernel the library runs for a format and row count: the
+    register-resident kernel for 4-bit weights up to 32 rows, else the
+    tensor-memory kernel."""
+    return "k_verify_gemm_rs" if fmt == "w4" and M <= 32 else "k_verify_gemm"
 
 
 def gemm_traffic_record():
@@ -481,7 +489,7 @@ def run_gpu(args, ranks: Ranks):
     roofline = {"bound": "hbm", "achieved": gemm_achieved, "peak": peak, "unit": "GB/s",
                 "frac": gemm_achieved / peak, "peak_kind": f"{peak_kind} (HBM copy bandwidth)",
                 "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
-                "kernel": "k_verify_gemm", "launches_per_pass": vp.n_gemm,
+                "kernel": gemm_kernel_name(vp.fmt, vp.M), "launches_per_pass": vp.n_gemm,
                 "avg_launch_us": gemm_ms_per_pass * 1e3 / vp.n_gemm,
                 "algorithmic_bytes_per_launch": vp.algo_weight_bytes / vp.n_gemm}
 
@@ -848,7 +856,7 @@ def summarize_ncu(args) -> int:
     if gemm and any("dram__bytes_read.sum" in per[n] for n in gemm):
         n_l = sum(len(launches[n]) for n in gemm)
         dram = sum(per[n].get("dram__bytes_read.sum", 0) + per[n].get("dram__bytes_write.sum", 0) for n in gemm)
-        rec = {"kernel": "k_verify_gemm", "workload": args.ncu_name, "launches": n_l,
+        rec = {"kernel": ", ".join(sorted(gemm)), "workload": args.ncu_name, "launches": n_l,
                "dram_bytes_total": dram, "dram_bytes_per_launch": dram / n_l,
                "kernel_source_hash": kernel_source_hash(), "command": args.ncu_command}
         js = os.path.join(ROOT, "profiles", f"k_verify_gemm_{args.ncu_name}_traffic.json")

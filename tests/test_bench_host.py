@@ -149,7 +149,19 @@ def test_kernel_source_hash_follows_the_gemm_sources(tmp_path, monkeypatch):
     api = (csrc / "hq_api.cu").read_text()
     i = api.index("cudaError_t launch_verify_gemm(")
     (csrc / "hq_api.cu").write_text(api[:i] + api[i:].replace("MIN_TILES = 4", "MIN_TILES = 5", 1))
-    assert bench.kernel_source_hash() != h0
+    h1 = bench.kernel_source_hash()
+    assert h1 != h0
+    # so does the register-resident kernel and the code both GEMMs share
+    for f in ("k_gemm_rs.cuh", "gemm_common.cuh"):
+        with open(csrc / f, "a") as fh:
+            fh.write("\n// changed\n")
+        assert bench.kernel_source_hash() != h1
+        h1 = bench.kernel_source_hash()
+
+
+def test_gemm_kernel_name_follows_the_library_dispatch():
+    assert bench.gemm_kernel_name("w4", 16) == bench.gemm_kernel_name("w4", 32) == "k_verify_gemm_rs"
+    assert bench.gemm_kernel_name("w4", 33) == bench.gemm_kernel_name("w8", 16) == "k_verify_gemm"
 
 
 # ------------------------------------------------------ reference arm ---
