@@ -233,6 +233,28 @@ int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, co
 int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop, const float *sx, int32_t M, float *Y,
                    int32_t *partials, void *workspace, uint32_t flags, void *stream);
 
+/* The verify GEMM on int8 activation codes, the boundary's form with qx, sx
+ * and the group sums (page "Karpathy's Trick for Faster Local LLMs Finally
+ * Has Proper Tooling", section "How Uzu optimizes bytes and tokens per pass":
+ * both matmul operands are integers).  The result is that of
+ * hq_verify_gemm on the operand hq_rotate_quant_act would write for these
+ * codes (same Y, same modes and flags, same errors).
+ *   qx        int8 [M][K] (4-byte aligned): clamp(rint(x' / sx), -127, 127)
+ *             from hq_rotate_quant_act or any other producer of the codes
+ *   sx        fp32 [M]
+ *   gsum      int32 [M][K/group] or NULL: not read (the group sums the
+ *             Medium zero point needs are formed from qx, exactly)
+ *   workspace hq_workspace_q8_bytes(desc, M) bytes, 16-byte aligned: the
+ *             hq_workspace_bytes(desc, M) bytes of hq_verify_gemm (zero-filled
+ *             before first use, as there), then room for the operand
+ * One launch converts qx into the operand inside the workspace, the GEMM
+ * follows on the same stream (with programmatic dependent launch: its weight
+ * stream starts while the conversion runs). */
+size_t hq_workspace_q8_bytes(const hq_layer_desc *desc, int32_t M);
+int hq_verify_gemm_q8(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
+                      const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
+                      void *stream);
+
 /* Canonical view of a blob (for verification and for saving in a portable
  * form): codes uint8 [N][K] (Medium: 0..15; Large: the int8 code's byte),
  * scales fp32 [N][K/group], zeros uint8 [N][K/group] (Medium only; may be

@@ -264,6 +264,39 @@ int hq_verify_gemm(const hq_layer_desc *desc, const void *blob, const void *qop,
                                               flags, static_cast<cudaStream_t>(stream)));
 }
 
+static size_t q8_operand_offset(const hq_layer_desc *desc, int32_t M) {
+    return (hq_workspace_bytes(desc, M) + 255) / 256 * 256;
+}
+
+size_t hq_workspace_q8_bytes(const hq_layer_desc *desc, int32_t M) {
+    if (!desc_ok(desc) || M < 0 || M > HQ_MAX_M) return 0;
+    return q8_operand_offset(desc, M) + (M > 0 ? hq::act_operand_bytes(M, desc->K, desc->group, desc->format) : 0);
+}
+
+int hq_verify_gemm_q8(const hq_layer_desc *desc, const void *blob, const int8_t *qx, const float *sx,
+                      const int32_t *gsum, int32_t M, float *Y, int32_t *partials, void *workspace, uint32_t flags,
+                      void *stream) {
+    (void)gsum;  // the group sums are formed from qx itself
+    if (!desc_ok(desc)) return HQ_ERR_INVALID_ARG;
+    if (M < 0 || M > HQ_MAX_M) return HQ_ERR_INVALID_ARG;
+    if ((flags & ~(HQ_LAUNCH_PDL | HQ_LAUNCH_DETERMINISTIC | HQ_LAUNCH_EXACT_ORDER)) != 0) return HQ_ERR_INVALID_ARG;
+    if (M == 0) return HQ_OK;
+    if (!blob || !qx || !sx || !Y || !workspace) return HQ_ERR_INVALID_ARG;
+    if (!aligned(blob, 16) || !aligned(qx, 4) || !aligned(sx, 4) || !aligned(Y, 4) || !aligned(workspace, 16) ||
+        (partials && !aligned(partials, 4)))
+        return HQ_ERR_INVALID_ARG;
+    const int fmt = desc->format, K = desc->K, G = desc->group;
+    uint8_t *qop = static_cast<uint8_t *>(workspace) + q8_operand_offset(desc, M);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = hq::launch_codes_to_operand(qx, M, K, G, hq::act_rs(fmt, M), hq::act_e4(fmt, M, G),
+                                                hq::act_sums(fmt, M), qop, (flags & HQ_LAUNCH_PDL) != 0, s);
+    if (e != cudaSuccess) return HQ_ERR_CUDA;
+    // the GEMM follows the conversion on the stream (programmatic launch: its
+    // weight stream starts before the operand is complete)
+    const Geom g = geom_of(desc);
+    return cuda_status(hq::launch_verify_gemm(g, blob, qop, sx, M, Y, partials, workspace, flags | HQ_LAUNCH_PDL, s));
+}
+
 int hq_unpack_codes(const hq_layer_desc *desc, const void *blob, uint8_t *codes, float *scales, uint8_t *zeros,
                     void *stream) {
     if (!desc_ok(desc) || !blob || !codes || !scales) return HQ_ERR_INVALID_ARG;

@@ -396,6 +396,8 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 namespace hq {
 cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool rs, bool e4, bool sums, const uint32_t *signs, int8_t *qx,
                                     int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s);
+cudaError_t launch_codes_to_operand(const int8_t *qx, int M, int K, int G, bool rs, bool e4, bool sums, uint8_t *qop,
+                                    bool pdl, cudaStream_t s);
 // rows of W -> n-blocks nb0.. of the blob of layer g
 cudaError_t launch_pack(const Geom &g, const float *W, int rows, int nb0, const uint32_t *signs, void *blob,
                         cudaStream_t s);

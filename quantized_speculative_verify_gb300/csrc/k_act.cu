@@ -228,6 +228,61 @@ __global__ void __launch_bounds__(T) k_rotate_quant_act(const float *__restrict_
     }
 }
 
+// int8 codes [M][K] -> the GEMM's operand (the same layout and values as
+// k_rotate_quant_act writes for these codes): one block per operand row,
+// rows past M and features past K zero; group sums formed from the codes.
+__global__ void __launch_bounds__(256) k_codes_to_operand(const int8_t *__restrict__ qx, int M, int K, int G, int rs,
+                                                          int e4, int sums, uint8_t *__restrict__ qop) {
+    constexpr int T = 256;
+    pdl_wait();
+    // the dependent GEMM may start streaming its weights; its reads of the
+    // operand wait for this grid's completion
+    pdl_launch_dependents();
+    const int row = blockIdx.x, MT = gridDim.x, tid = threadIdx.x;
+    const int n4 = K >> 2, n4pad = act_blocks(K) * (ACT_BLOCK / 4);
+    const int bpt = act_kt(G) / ACT_BLOCK, gpt = act_kt(G) / G;
+    const int cb = MT * (rs ? ACT_RS_PITCH : 256);
+    const size_t tb = (size_t)bpt * cb + (sums ? (size_t)gpt * MT * 4 : 0);
+    const bool live = row < M;
+    for (int idx = tid; idx < n4pad; idx += T) {
+        int q[4] = {0, 0, 0, 0};
+        if (live && idx < n4) {
+            const char4 c = reinterpret_cast<const char4 *>(qx + (size_t)row * K)[idx];
+            q[0] = c.x;
+            q[1] = c.y;
+            q[2] = c.z;
+            q[3] = c.w;
+        }
+        const int f = idx * 4, kb = f / ACT_BLOCK, fb = f % ACT_BLOCK;
+        const int kt = bpt == 1 ? kb : kb >> 1, kbi = bpt == 1 ? 0 : kb & 1;
+        const size_t blk = (size_t)kt * tb + (size_t)kbi * cb;
+        if (e4) {
+            uint32_t lo, hi;
+            digits4(q[0], q[1], q[2], q[3], lo, hi);
+            const size_t o = blk + ((size_t)(fb / 16) * 2 * MT + row) * 16 + (size_t)(fb % 16);
+            *reinterpret_cast<uint32_t *>(qop + o) = lo;
+            *reinterpret_cast<uint32_t *>(qop + o + (size_t)MT * 16) = hi;
+        } else {
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = __half_as_ushort(__int2half_rn(q[i]));
+            const size_t o = rs ? blk + (size_t)row * ACT_RS_PITCH + (size_t)fb * 2
+                                : blk + ((size_t)(fb / 8) * MT + row) * 16 + (size_t)(fb % 8) * 2;
+            *reinterpret_cast<uint2 *>(qop + o) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        }
+    }
+    if (sums) {
+        const int ngp = act_ktiles(K, G) * gpt;
+        for (int g = tid; g < ngp; g += T) {
+            int acc = 0;
+            if (live)
+                for (int k = g * G; k < (g + 1) * G && k < K; ++k) acc += qx[(size_t)row * K + k];
+            float *d = reinterpret_cast<float *>(qop + (size_t)(g / gpt) * tb + (size_t)bpt * cb) + (size_t)(g % gpt) * MT + row;
+            *d = (float)acc;
+        }
+    }
+}
+
 template <int V, int T>
 cudaError_t launch_act_t(const float *X, int M, int K, int G, bool rs, bool e4, const uint32_t *signs, int8_t *qx,
                          int32_t *gsum, uint8_t *qop, float *sx, bool pdl, cudaStream_t s, bool sums) {
@@ -263,6 +318,21 @@ cudaError_t launch_rotate_quant_act(const float *X, int M, int K, int G, bool rs
     if (n4 <= 1024 * 8) return launch_act_t<8, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
     if (n4 <= 1024 * 16) return launch_act_t<16, 1024>(X, M, K, G, rs, e4, signs, qx, gsum, qop, sx, pdl, s, sums);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_codes_to_operand(const int8_t *qx, int M, int K, int G, bool rs, bool e4, bool sums, uint8_t *qop,
+                                    bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)act_rows(M));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_codes_to_operand, qx, M, K, G, rs ? 1 : 0, e4 ? 1 : 0, sums ? 1 : 0, qop);
 }
 
 }  // namespace hq

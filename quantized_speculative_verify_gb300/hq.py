@@ -34,7 +34,8 @@ FORMATS = {"w4": HQ_W4_ASYM, "w8": HQ_W8_SYM}
 # Every symbol include/hq.h declares.
 EXPORTS = ("hq_tree_accept_workspace_bytes", "hq_tree_accept", "hq_status_string", "hq_version", "hq_packed_bytes", "hq_workspace_bytes", "hq_act_operand_bytes",
            "hq_make_signs",
-           "hq_pack_weights", "hq_pack_weights_at", "hq_rotate_quant_act", "hq_verify_gemm", "hq_unpack_codes", "hq_workspace_status",
+           "hq_pack_weights", "hq_pack_weights_at", "hq_rotate_quant_act", "hq_verify_gemm", "hq_workspace_q8_bytes",
+           "hq_verify_gemm_q8", "hq_unpack_codes", "hq_workspace_status",
            "hq_selftest_wait_timeout", "hq_selftest_gemm_wait_timeout", "hq_verify_gemm_noalloc", "hq_noalloc_status",
            "hq_tree_attention_workspace_bytes",
            "hq_tree_attention", "hq_tree_commit_kv", "hq_delta_tree", "hq_delta_commit")
@@ -83,6 +84,8 @@ def load() -> ctypes.CDLL:
         "hq_pack_weights_at": (ctypes.c_int, [D, I32, I32, P, P, P, P]),
         "hq_rotate_quant_act": (ctypes.c_int, [D, P, I32, P, P, P, P, P, U32, P]),
         "hq_verify_gemm": (ctypes.c_int, [D, P, P, P, I32, P, P, P, U32, P]),
+        "hq_workspace_q8_bytes": (SZ, [D, I32]),
+        "hq_verify_gemm_q8": (ctypes.c_int, [D, P, P, P, P, I32, P, P, P, U32, P]),
         "hq_unpack_codes": (ctypes.c_int, [D, P, P, P, P, P]),
         "hq_workspace_status": (ctypes.c_int, [P, P]),
         "hq_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_int64, P]),
@@ -185,6 +188,15 @@ def hq_rotate_quant_act(desc, X, M: int, signs, qx, gsum, qop, sx, flags: int = 
 def hq_verify_gemm(desc, blob, qop, sx, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
     _check(load().hq_verify_gemm(ctypes.byref(desc), _ptr(blob), _ptr(qop), _ptr(sx), int(M), _ptr(Y),
                                  _ptr(partials), _ptr(workspace), int(flags), _stream(stream)), "hq_verify_gemm")
+
+
+def hq_workspace_q8_bytes(desc: hq_layer_desc, M: int) -> int:
+    return int(load().hq_workspace_q8_bytes(ctypes.byref(desc), int(M)))
+
+
+def hq_verify_gemm_q8(desc, blob, qx, sx, gsum, M: int, Y, partials, workspace, flags: int = 0, stream=None) -> None:
+    _check(load().hq_verify_gemm_q8(ctypes.byref(desc), _ptr(blob), _ptr(qx), _ptr(sx), _ptr(gsum), int(M), _ptr(Y),
+                                    _ptr(partials), _ptr(workspace), int(flags), _stream(stream)), "hq_verify_gemm_q8")
 
 
 def hq_unpack_codes(desc, blob, codes, scales, zeros, stream=None) -> None:

@@ -113,6 +113,25 @@ def test_K_above_the_activation_limit_is_invalid(K):
         hq.HQ_ERR_INVALID_ARG
 
 
+def test_q8_workspace_and_argument_checks():
+    d = hq.make_desc(4096, 384, 64, "w4")
+    for M in (1, 16, 40, 128):
+        assert hq.hq_workspace_q8_bytes(d, M) >= hq.hq_workspace_bytes(d, M) + hq.hq_act_operand_bytes(d, M)
+        assert hq.hq_workspace_q8_bytes(d, M) % 16 == 0
+    assert hq.hq_workspace_q8_bytes(d, 129) == 0 and hq.hq_workspace_q8_bytes(d, -1) == 0
+    lib = hq.load()
+    FAKE = ctypes.c_void_p(0x10000)
+    E = hq.HQ_ERR_INVALID_ARG
+    D = ctypes.byref(d)
+    # null pointers, bad M, unknown flags, misaligned workspace: refused before any launch
+    assert lib.hq_verify_gemm_q8(D, None, FAKE, FAKE, None, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm_q8(D, FAKE, None, FAKE, None, 4, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm_q8(D, FAKE, FAKE, FAKE, None, 129, FAKE, None, FAKE, 0, None) == E
+    assert lib.hq_verify_gemm_q8(D, FAKE, FAKE, FAKE, None, 4, FAKE, None, FAKE, 1 << 9, None) == E
+    assert lib.hq_verify_gemm_q8(D, FAKE, FAKE, FAKE, None, 4, FAKE, None, ctypes.c_void_p(0x10008), 0, None) == E
+    assert lib.hq_verify_gemm_q8(D, FAKE, FAKE, FAKE, None, 0, FAKE, None, FAKE, 0, None) == hq.HQ_OK
+
+
 def test_act_operand_bytes():
     # opaque, but its size follows from the rows padded to the MMA's N (16, 32,
     # 64, 128), 128-feature blocks of 2 bytes per code (fp16, or two e4m3

@@ -198,6 +198,44 @@ def test_gemm_exact_order_is_bit_exact(fmt, M, K, N, G):
     assert np.array_equal(r["Y"].view(np.uint32), ref["Y"].view(np.uint32))
 
 
+Q8_CASES = [("w4", 16, 4096, 384, 64), ("w4", 1, 256, 256, 32), ("w4", 40, 2048, 1000, 128), ("w4", 100, 512, 256, 64),
+            ("w8", 16, 1024, 512, 128), ("w4", 32, 1024, 1024, 16), ("w4", 7, 4096, 256, 256)]
+
+
+@pytest.mark.parametrize("flags", [hq.HQ_LAUNCH_EXACT_ORDER, hq.HQ_LAUNCH_DEFAULT])
+@pytest.mark.parametrize("fmt,M,K,N,G", Q8_CASES)
+def test_gemm_on_int8_codes(fmt, M, K, N, G, flags):
+    # the boundary's int8 form: the oracle's own codes qx and scales sx go in
+    # (hq_verify_gemm_q8 converts them inside its workspace); the outputs are
+    # the oracle's (bit for bit in exact-order mode), the partials exact
+    X = synth.activations(M, K, seed=M + K + 21, outlier_channels=2)
+    W = synth.weights(N, K, seed=N + K + 22, outlier_frac=0.005)
+    s_host, _ = signs_pair(M * N + K + 23, K)
+    ref = oracle.verify_linear(X.numpy(), W.numpy(), G, fmt, s_host)
+    layer = hq.pack_layer(W.to(DEV), G, fmt, s_host)
+    ws = torch.zeros(hq.hq_workspace_q8_bytes(layer.desc, M), dtype=torch.uint8, device=DEV)
+    assert ws.numel() > hq.hq_workspace_bytes(layer.desc, M) + hq.hq_act_operand_bytes(layer.desc, M) - 256
+    qx = torch.from_numpy(ref["qx"]).to(DEV)
+    sx = torch.from_numpy(ref["sx"]).to(DEV)
+    Y = Guarded((M, N), torch.float32, DEV, fill=float("nan"))
+    P = Guarded((M, N, K // G), torch.int32, DEV)
+    hq.hq_verify_gemm_q8(layer.desc, layer.blob, qx, sx, None, M, Y.t, P.t, ws, flags | hq.HQ_LAUNCH_PDL)
+    assert hq.hq_workspace_status(ws) == hq.HQ_OK
+    torch.cuda.synchronize()
+    Y.check("Y")
+    P.check("partials")
+    assert np.array_equal(P.t.cpu().numpy(), ref["P"])
+    y = Y.t.cpu().numpy()
+    if flags & hq.HQ_LAUNCH_EXACT_ORDER:
+        assert np.array_equal(y.view(np.uint32), ref["Y"].view(np.uint32))
+    else:
+        assert_close(y, ref)
+    # the same codes through the two-call path give the same outputs
+    r = run_layer(X, None, G, fmt, s_host, flags=hq.HQ_LAUNCH_EXACT_ORDER, layer=layer)
+    if flags & hq.HQ_LAUNCH_EXACT_ORDER:
+        assert np.array_equal(r["Y"].view(np.uint32), y.view(np.uint32))
+
+
 def test_gemm_wait_timeout_selftest_reports_error_and_recovers():
     # a GEMM whose waits between thread blocks ask for one arrival too many:
     # each runs out after 1 ms, the call reports HQ_ERR_TIMEOUT, no hang
