@@ -96,10 +96,13 @@ typedef struct {
 #define HQ_LAUNCH_DETERMINISTIC 2u
 /* hq_verify_gemm only: no output's K range is split between thread blocks:
  * each thread block takes whole blocks of 128 output channels, so every
- * output is summed over its groups in ascending order by one thread block and
- * is bit-identical to the sequential fp32 sum of the definition (see
- * hq_verify_gemm).  Slower on layers with few 128-channel blocks (fewer thread
- * blocks than SMs); implies HQ_LAUNCH_DETERMINISTIC. */
+ * output is summed over its groups in ascending order by one thread block,
+ * each product scale * P rounded and then added (the definition's
+ * arithmetic), and is bit-identical to the sequential fp32 sum of the
+ * definition (see hq_verify_gemm).  Without this flag (and without check-mode
+ * partials) a group is folded with one fused multiply-add, one rounding
+ * fewer per group.  Slower on layers with few 128-channel blocks (fewer
+ * thread blocks than SMs); implies HQ_LAUNCH_DETERMINISTIC. */
 #define HQ_LAUNCH_EXACT_ORDER 4u
 
 /* Maximum number of token rows per call. */
@@ -212,10 +215,11 @@ int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, co
  *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
  *             before its first use
  * The integer sums P are exact: the codes are multiplied on the tensor cores
- * (tcgen05, e4m3 or fp16 operands) with fp32 accumulation, exact for these
- * ranges, and the Medium zero point enters through the group sums.  The fp32
- * sum
- * over groups is taken in ascending group order.  An output whose K range is
+ * with fp32 accumulation, exact for these ranges (4-bit weights up to 32
+ * rows: warp-level fp16 MMAs on the weights widened to q - z; otherwise
+ * tcgen05 MMAs with e4m3 or fp16 operands, the Medium zero point entering
+ * through the group sums).  The fp32 sum over groups is taken in ascending
+ * group order.  An output whose K range is
  * split across thread blocks is the sum of the blocks' partial sums: by
  * default each block adds sx[m] * (its partial sum) into Y with an fp32
  * atomic add when it finishes (Y is zeroed first by the kernel itself), so

@@ -15,7 +15,8 @@
 // widened weights as the A operand in TMEM (128 channels = 128 TMEM lanes),
 // the activation codes as the B operand in shared memory, each quantization
 // group's integer sum in its own TMEM accumulator slot:
-//  - 4-bit weights, up to 64 rows, groups of 32 or more: kind::f8f6f4.  A
+//  - 4-bit weights, 33 to 64 rows (fewer rows run on the register-resident
+//    kernel, k_gemm_rs.cuh), groups of 32 or more: kind::f8f6f4.  A
 //    4-bit code q in a byte is the e4m3 number q * 2^-9 (subnormal up to 7,
 //    then exponent 1), so the codes need only be spread to bytes; an
 //    activation code is split into two exact e4m3 digits, q = 16 h + l, which
@@ -37,23 +38,25 @@
 // packed fused multiply-add (two tokens per instruction): one rounding per
 // group instead of two, within the fp32 tolerance of the oracle.
 //
-// Thread block (one per SM, 14 warps, each role running ahead of the next
+// Thread block (one per SM, 11 or 15 warps, each role running ahead of the next
 // through rings of shared-memory stages, A buffers and accumulator slots).
-// The unit of the rings is U consecutive tiles of the block's range (U = 2
-// where tensor memory allows): every barrier wait, which costs about a
-// hundred cycles beside running MMAs, serves U tiles.
-//  - warp 0, one lane: producer.  Per tile, one bulk copy of the weight tile,
-//    one of the activation blocks and one of their group sums into a stage
-//    (mbarrier transaction counts).  The weight copies of the first stages go
-//    out before waiting for the previous kernel of the stream; the activation
-//    copies after.
+// The unit of the rings is U consecutive tiles of the block's range (up to 32
+// rows U = 4 where tensor memory allows, else 2 or 1; above 32 rows U = 1):
+// every barrier wait, which costs about a hundred cycles beside running MMAs,
+// serves U tiles.
+//  - warp 0, one lane: weight producer, and the last warp, one lane:
+//    activation producer (gemm_common.cuh).  Per unit, one bulk copy of its
+//    weight tiles and one per run of activation K tiles (codes and group
+//    sums) into a stage (mbarrier transaction counts).  The weight copies of
+//    the first stage go out before waiting for the previous kernel of the
+//    stream; the activation copies after.
 //  - warp 1: tensor-memory owner and MMA issuer (one elected lane).  Per
 //    group: wait for a free accumulator slot, issue group/16 MMAs (K = 16
 //    each) from one unrolled sequence, commit to the slot's "full" barrier.
 //  - warps 2..5: widening.  Warp w owns TMEM lanes 32 (w % 4) .. + 31 (= the
 //    tile's channels); each thread widens its channel's codes of the whole
 //    tile into the tile's A buffer (tcgen05.st).
-//  - warps 6..13: epilogue.  Same lanes, and half h = (w - 6) / 4 of the
+//  - warps 6..9 (up to 32 rows) or 6..13: epilogue.  Same lanes, and half h = (w - 6) / 4 of the
 //    tokens: fold each group out of its accumulator slot (tcgen05.ld) into the
 //    running fp32 sums, and write, add or publish them at the end of a
 //    128-channel block's segment.
