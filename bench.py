@@ -273,7 +273,7 @@ def gemm_source_parts(csrc: str) -> list:
         with open(os.path.join(csrc, f)) as fh:
             return fh.read()
     parts = [read("k_gemm.cuh"), read("k_gemm_w4.cu"), read("k_gemm_w8.cu"), read("gemm_common.cuh"),
-             read("k_gemm_rs.cuh"), read("k_gemm_rs.cu")]
+             read("k_gemm_rs.cuh"), read("k_gemm_rs.cu"), read("k_gemm_rs_w8.cu")]
     internal = read("hq_internal.cuh")
     parts.append(internal.split("// Launchers (defined in the kernel translation units).")[0])
     api = read("hq_api.cu")
@@ -291,9 +291,8 @@ def kernel_source_hash() -> str:
 
 def gemm_kernel_name(fmt: str, M: int) -> str:
     """The GEMM kernel the library runs for a format and row count: the
-    register-resident kernel for 4-bit weights up to 32 rows, else the
-    tensor-memory kernel."""
-    return "k_verify_gemm_rs" if fmt == "w4" and M <= 32 else "k_verify_gemm"
+    register-resident kernel up to 32 rows, else the tensor-memory kernel."""
+    return "k_verify_gemm_rs" if M <= 32 else "k_verify_gemm"
 
 
 def gemm_traffic_record():

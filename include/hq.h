@@ -215,10 +215,10 @@ int hq_rotate_quant_act(const hq_layer_desc *desc, const float *X, int32_t M, co
  *   workspace hq_workspace_bytes(desc, M) bytes, 16-byte aligned, zero-filled
  *             before its first use
  * The integer sums P are exact: the codes are multiplied on the tensor cores
- * with fp32 accumulation, exact for these ranges (4-bit weights up to 32
- * rows: warp-level fp16 MMAs on the weights widened to q - z; otherwise
- * tcgen05 MMAs with e4m3 or fp16 operands, the Medium zero point entering
- * through the group sums).  The fp32 sum over groups is taken in ascending
+ * with fp32 accumulation, exact for these ranges (up to 32 rows: warp-level
+ * fp16 MMAs on the weight codes widened in registers, 4-bit codes to
+ * q - z; above: tcgen05 MMAs with e4m3 or fp16 operands, the Medium zero
+ * point entering through the group sums).  The fp32 sum over groups is taken in ascending
  * group order.  An output whose K range is
  * split across thread blocks is the sum of the blocks' partial sums: by
  * default each block adds sx[m] * (its partial sum) into Y with an fp32

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libhq.so")
-SOURCES = ["hq_api.cu", "k_act.cu", "k_pack.cu", "k_gemm_w4.cu", "k_gemm_w8.cu", "k_gemm_rs.cu", "hq_noalloc.cu", "k_accept.cu",
+SOURCES = ["hq_api.cu", "k_act.cu", "k_pack.cu", "k_gemm_w4.cu", "k_gemm_w8.cu", "k_gemm_rs.cu", "k_gemm_rs_w8.cu", "hq_noalloc.cu", "k_accept.cu",
            "k_attn.cu", "k_delta.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

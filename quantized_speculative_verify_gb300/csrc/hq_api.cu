@@ -76,10 +76,17 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
     // Small layers get fewer blocks so that every block streams at least
     // MIN_TILES tiles and an n-block is split between few blocks.
     constexpr int MIN_TILES = 4;
-    // the register-resident GEMM (4-bit weights, up to 32 rows) runs
-    // rs_bps(rows) blocks per SM
-    const bool rs = g.fmt == HQ_W4_ASYM && act_rows(M) <= 32;
-    const int bps = rs ? rs_bps(act_rows(M)) : 1;
+    // the register-resident GEMM (up to 32 rows) runs rs_bps(rows) blocks per SM
+    const bool rs = act_rs(g.fmt, M);
+    int bps = 1;
+    if (rs) {
+        // rs_bps(rows), fewer where two stages of a unit do not fit in a
+        // block's share of the SM's 228 KB (less 1 KB per block)
+        const int stage = ((RS_UNIT * g.tile_bytes + 127) / 128 * 128 + RS_UNIT * act_tile_bytes(M, g.G, g.fmt) + 127) /
+                          128 * 128;
+        bps = rs_bps(act_rows(M));
+        while (bps > 1 && 1024 + 2 * stage > 228 * 1024 / bps - 1024) --bps;
+    }
     int grid = sms * bps;
     if (exact) {
         // whole n-blocks per block: every output is summed by one block
@@ -111,14 +118,13 @@ cudaError_t launch_verify_gemm(const Geom &g, const void *blob, const uint8_t *q
         return header + (size_t)stages * a.stage_bytes <= (size_t)budget;
     };
     if (rs) {
-        // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows of
-        // 4-bit weights, where the per-group fold of every output is a few
-        // register operations.  Units of RS_UNIT tiles.
+        // Register-resident kernel (warp-level fp16 MMAs): up to 32 rows, where
+        // the per-group fold of every output is a few register operations.  Units of RS_UNIT tiles.
         a.V = a.na = a.nd = 0;
         // the SM's 228 KB of shared memory, less 1 KB per block, shared by its blocks
         const int budget = 228 * 1024 / bps - 1024;
         if (!stage_layout(RS_UNIT, 1024, budget)) return cudaErrorInvalidConfiguration;
-        return launch_gemm_w4_rs(a, pdl, s);
+        return g.fmt == HQ_W4_ASYM ? launch_gemm_w4_rs(a, pdl, s) : launch_gemm_w8_rs(a, pdl, s);
     }
     const int dc = e4 ? 2 * MT : MT;             // TMEM columns of one group's accumulator
     const int acols = e4 ? g.KT / 4 : g.KT / 2;  // TMEM columns of one tile's widened weights

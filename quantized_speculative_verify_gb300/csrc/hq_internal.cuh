@@ -27,8 +27,10 @@ namespace hq {
 //           MMA steps of one channel (feature pairs 2t, 2t+1 and 2t+8, 2t+9
 //           of each step), and one mask (after a shift by 8 for the second
 //           step) lifts each pair into the two halves of a 32-bit register.
-//           8-bit: [c][quarter p 0..3][n][16 bytes]: features 64c + 16p + e,
-//           e = 0..15, in order.
+//           8-bit: [c][quarter p 0..3][n][16 bytes]: the 16 features
+//           64c + 16p .. of channel n as four words, word t holding features
+//           2t, 2t+1, 2t+8, 2t+9 (bytes 0..3): lane t of a quad's A operand
+//           for one 16-feature MMA step.
 //           A tcgen05 widening thread owns one channel and reads 16 contiguous
 //           bytes per quarter (the 32 lanes of a warp: 512 contiguous bytes);
 //           an MMA lane reads the one word of its quad position.
@@ -160,8 +162,9 @@ __host__ __device__ inline int act_ktiles(int K, int G) { return (K + act_kt(G) 
 // rows).  Up to 32 rows the register-resident GEMM subtracts the zero point
 // while widening the weights; 8-bit weights have none.
 __host__ __device__ inline bool act_sums(int fmt, int M) { return fmt == HQ_W4_ASYM && act_rows(M) > 32; }
-// The row encoding: the operand of the register-resident GEMM.
-__host__ __device__ inline bool act_rs(int fmt, int M) { return fmt == HQ_W4_ASYM && act_rows(M) <= 32; }
+// The row encoding: the operand of the register-resident GEMM (every
+// format, up to 32 rows).
+__host__ __device__ inline bool act_rs(int fmt, int M) { return (fmt == HQ_W4_ASYM || fmt == HQ_W8_SYM) && act_rows(M) <= 32; }
 constexpr int ACT_RS_PITCH = 272;  // bytes per row of a 128-feature block in the row encoding
 // bytes of one 128-feature block's codes, of one K tile's codes, of its group
 // sums, and of the whole K tile

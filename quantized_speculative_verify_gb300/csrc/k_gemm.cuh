@@ -108,15 +108,17 @@ __device__ __forceinline__ void widen_w4_f16(uint32_t w, int t, uint32_t *o) {
     o[t + 12] = ((w >> 8) & M4) | E64;
 }
 
-// Four int8 codes -> two fp16x2 q: bias to unsigned, place under the fp16
-// exponent bits 0x64 (1024 + 128 + q), subtract 1152.
-__device__ __forceinline__ void widen_i8(uint32_t w, uint32_t *o) {
+// Four int8 codes (word t of a 16-feature run: features 2t, 2t+1, 2t+8,
+// 2t+9) -> the fp16x2 q of the pairs (2t, 2t+1) in lo and (2t+8, 2t+9) in
+// hi: bias to unsigned, place under the fp16 exponent bits 0x64
+// (1024 + 128 + q), subtract 1152.
+__device__ __forceinline__ void widen_i8(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const uint32_t u = w ^ 0x80808080u;
     uint32_t l, h;
     asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(l) : "r"(u), "r"(0x64646464u));
     asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(h) : "r"(u), "r"(0x64646464u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(l), "r"(0x64806480u));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(h), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
 }
 
 // E4: the kind::f8f6f4 path (4-bit weights, digit-encoded operand).  EXACT:
@@ -323,10 +325,10 @@ __global__ void __launch_bounds__(gemm_threads(MT), 1) k_verify_gemm(const GemmA
                                 uu[p] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(c * 4 + p) * BN + n) * 16);
 #pragma unroll
                             for (int p = 0; p < 4; ++p) {
-                                widen_i8(uu[p].x, v + 8 * p + 0);
-                                widen_i8(uu[p].y, v + 8 * p + 2);
-                                widen_i8(uu[p].z, v + 8 * p + 4);
-                                widen_i8(uu[p].w, v + 8 * p + 6);
+                                widen_i8(uu[p].x, v[8 * p + 0], v[8 * p + 4]);
+                                widen_i8(uu[p].y, v[8 * p + 1], v[8 * p + 5]);
+                                widen_i8(uu[p].z, v[8 * p + 2], v[8 * p + 6]);
+                                widen_i8(uu[p].w, v[8 * p + 3], v[8 * p + 7]);
                             }
                         }
                         tmem_st32(tbase + lane_field + a_col + (uint32_t)(c * 32), v);
@@ -664,5 +666,6 @@ cudaError_t launch_gemm_w4(const GemmArgs &a, bool pdl, cudaStream_t s);
 cudaError_t launch_gemm_w8(const GemmArgs &a, bool pdl, cudaStream_t s);
 // register-resident kernel: 4-bit weights, fp16-encoded operand, up to 32 rows
 cudaError_t launch_gemm_w4_rs(const GemmArgs &a, bool pdl, cudaStream_t s);
+cudaError_t launch_gemm_w8_rs(const GemmArgs &a, bool pdl, cudaStream_t s);
 
 }  // namespace hq

@@ -1,17 +1,18 @@
-// k_gemm_rs.cuh -- the verify GEMM for 4-bit weights and up to 32 token rows,
-// with every partial sum in registers: warp-level fp16 MMAs on the weights
+// k_gemm_rs.cuh -- the verify GEMM for up to 32 token rows, with every
+// partial sum in registers: warp-level fp16 MMAs on the weights
 // widened straight from the packed tile, the per-group dequantization folded
 // into the fp32 sums as each group ends.
 //
 // Page "Karpathy's Trick for Faster Local LLMs Finally Has Proper Tooling":
 // section "How Uzu optimizes bytes and tokens per pass" (both operands of the
-// verify matmul are integers; Medium weights are 4-bit asymmetric, grouped
-// along K) and section "Producing several tokens from one model pass" (the
+// verify matmul are integers; Medium weights are 4-bit asymmetric, Large
+// 8-bit symmetric, grouped along K) and section "Producing several tokens from one model pass" (the
 // verify batch: a draft tree of up to 32 tokens shares one weight stream).
 //
 // Exact integer contraction on fp16 MMAs (mma.sync m16n8k16, fp32
-// accumulate): weight codes minus the zero point (|q - z| <= 15) and
-// activation codes (|q| <= 127) are exact in fp16, their products exact in
+// accumulate): 4-bit weight codes minus the zero point (|q - z| <= 15),
+// 8-bit weight codes and activation codes (|q| <= 127) are exact in fp16,
+// their products exact in
 // fp32, and a group's sum stays below 2^24, so each group's accumulator holds
 // the integer partial sum P of the Medium identity exactly (with the zero
 // point applied to the weights, no group-sum correction is needed).  With at
@@ -27,7 +28,10 @@
 // fp16 exponent bits of 1024, which reads 1024 + q (low nibbles) or
 // 1024 + 16 q (high nibbles); one fp16 add of -(1024 + z), or a multiply-add
 // by 1/16 and -(64 + z), leaves q - z exactly.  Eight codes cost nine
-// instructions (four masks, a shift for the second step, four adds).  The
+// instructions (four masks, a shift for the second step, four adds).  8-bit
+// codes: lane t's word of a 16-feature run holds the same four features as
+// bytes; a bias to unsigned, two byte permutes under the exponent bits of
+// 1024 and two fp16 subtractions of 1152 give the two pairs.  The
 // activation codes come from the operand's fp16 rows through ldmatrix.
 //
 // Fold of a group into the running sums, in the oracle's ascending group
@@ -87,6 +91,17 @@ __device__ __forceinline__ uint32_t widen_hi(uint32_t w, uint32_t zhi) {
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(zhi));  // x / 16 - (64 + z)
     return r;
 }
+// Four int8 codes (bytes 0..3 of w) -> the fp16x2 q of bytes (0, 1) in lo
+// and (2, 3) in hi: biased to unsigned under the fp16 exponent bits 0x64
+// (1024 + 128 + q), then 1152 subtracted, exactly.
+__device__ __forceinline__ void widen_i8_pairs(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t l, h;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(l) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(h) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
+}
 // four 8 x 16-byte row blocks of shared memory, one row address per lane
 // (a memory read: it stays after the wait for the stage)
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -96,9 +111,10 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
         : "memory");
 }
 
-// MT: token rows (16 or 32); G: quantization group (16 .. 256), fixed at
-// compile time so that a tile's K steps and groups unroll completely.
-template <int MT, int G, bool EXACT>
+// FMT: weight format; MT: token rows (16 or 32); G: quantization group
+// (16 .. 256), fixed at compile time so that a tile's K steps and groups
+// unroll completely.
+template <int FMT, int MT, int G, bool EXACT>
 __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const GemmArgs a) {
     constexpr int NT = MT / 8;             // MMA column tiles of tokens
     constexpr int KT = G > 128 ? G : 128;  // features per tile
@@ -178,7 +194,8 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
             const float *tsc = reinterpret_cast<const float *>(tile + a.code_bytes);  // scales [channel][GPT]
             const uint8_t *tzp = tile + a.code_bytes + a.scale_bytes;                // zero nibbles [channel * GPT + g]
             const uint32_t act_s = smem_addr(stage + a.act_off + (size_t)j * a.act_tile_bytes);
-            // the lane's word of its channels' 32-feature runs: [KT / 32][BN][4 words]
+            // the lane's word of its channels' runs: [KT / 32 (4-bit) or KT / 16
+            // (8-bit) runs][BN][4 words]
             const uint32_t *wc0 = reinterpret_cast<const uint32_t *>(tile) + 4 * chw + tig;
             // the current run's word of each channel (two 16-feature steps,
             // which may belong to two groups)
@@ -194,9 +211,11 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int zi = (chw + 16 * r + 8 * h) * GPT + gl;
-                        const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
-                        zlo[r][h] = z * 0x00010001u + 0xE400E400u;
-                        zhi[r][h] = z * 0x00100010u + 0xD400D400u;
+                        if (FMT == HQ_W4_ASYM) {
+                            const uint32_t z = (tzp[zi >> 1] >> ((zi & 1) * 4)) & 15u;
+                            zlo[r][h] = z * 0x00010001u + 0xE400E400u;
+                            zhi[r][h] = z * 0x00100010u + 0xD400D400u;
+                        }
                         sc[r][h] = tsc[zi];
                     }
                 float acc[RT][NT][4];
@@ -211,21 +230,27 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
                         ldmatrix_x4(bq[n2 / 2], b_s + lrow_off + (uint32_t)(n2 * 8 * ACT_RS_PITCH));
 #pragma unroll
                     for (int r = 0; r < RT; ++r) {
-                        if ((s & 1) == 0) {
-                            wq[r][0] = wc0[4 * ((s >> 1) * BN + 16 * r)];
-                            wq[r][1] = wc0[4 * ((s >> 1) * BN + 16 * r + 8)];
-                        }
                         // A: rows g, g + 8 (channels chw + 16 r, + 8), features
-                        // 2 tig, + 1 (nibbles 0, 4 of the step's half-words) and
-                        // 2 tig + 8, + 9 (nibbles 1, 5); the odd step's pairs sit
-                        // 8 bits higher
-                        const uint32_t v0 = (s & 1) ? wq[r][0] >> 8 : wq[r][0];
-                        const uint32_t v1 = (s & 1) ? wq[r][1] >> 8 : wq[r][1];
+                        // 2 tig, + 1 and 2 tig + 8, + 9 of the step
                         uint32_t A[4];
-                        A[0] = widen_lo(v0, zlo[r][0]);
-                        A[1] = widen_lo(v1, zlo[r][1]);
-                        A[2] = widen_hi(v0, zhi[r][0]);
-                        A[3] = widen_hi(v1, zhi[r][1]);
+                        if (FMT == HQ_W4_ASYM) {
+                            if ((s & 1) == 0) {
+                                wq[r][0] = wc0[4 * ((s >> 1) * BN + 16 * r)];
+                                wq[r][1] = wc0[4 * ((s >> 1) * BN + 16 * r + 8)];
+                            }
+                            // nibbles 0, 4 and 1, 5 of the step's half-words;
+                            // the odd step's pairs sit 8 bits higher
+                            const uint32_t v0 = (s & 1) ? wq[r][0] >> 8 : wq[r][0];
+                            const uint32_t v1 = (s & 1) ? wq[r][1] >> 8 : wq[r][1];
+                            A[0] = widen_lo(v0, zlo[r][0]);
+                            A[1] = widen_lo(v1, zlo[r][1]);
+                            A[2] = widen_hi(v0, zhi[r][0]);
+                            A[3] = widen_hi(v1, zhi[r][1]);
+                        } else {
+                            // one word per channel and step: bytes (0, 1), (2, 3)
+                            widen_i8_pairs(wc0[4 * (s * BN + 16 * r)], A[0], A[2]);
+                            widen_i8_pairs(wc0[4 * (s * BN + 16 * r + 8)], A[1], A[3]);
+                        }
 #pragma unroll
                         for (int n2 = 0; n2 < NT; n2 += 2) {
                             if (ks == 0) {
@@ -305,9 +330,9 @@ __global__ void __launch_bounds__(RS_THREADS, rs_bps(MT)) k_verify_gemm_rs(const
     gemm_finish(a, blk, ok, pend0, pend1, mark_old, ctid, RS_CONSUMERS * 32, 1);
 }
 
-template <int MT, int G, bool EXACT>
+template <int FMT, int MT, int G, bool EXACT>
 cudaError_t launch_gemm_rs_instance(const GemmArgs &a, bool pdl, cudaStream_t s) {
-    auto kern = k_verify_gemm_rs<MT, G, EXACT>;
+    auto kern = k_verify_gemm_rs<FMT, MT, G, EXACT>;
     const size_t smem = 1024 + (size_t)a.stages * (size_t)a.stage_bytes;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -332,23 +357,25 @@ cudaError_t launch_gemm_rs_instance(const GemmArgs &a, bool pdl, cudaStream_t s)
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int MT, bool EXACT>
+template <int FMT, int MT, bool EXACT>
 cudaError_t launch_gemm_rs_g(const GemmArgs &a, bool pdl, cudaStream_t s) {
     switch (a.G) {
-        case 16: return launch_gemm_rs_instance<MT, 16, EXACT>(a, pdl, s);
-        case 32: return launch_gemm_rs_instance<MT, 32, EXACT>(a, pdl, s);
-        case 64: return launch_gemm_rs_instance<MT, 64, EXACT>(a, pdl, s);
-        case 128: return launch_gemm_rs_instance<MT, 128, EXACT>(a, pdl, s);
-        case 256: return launch_gemm_rs_instance<MT, 256, EXACT>(a, pdl, s);
+        case 16: return launch_gemm_rs_instance<FMT, MT, 16, EXACT>(a, pdl, s);
+        case 32: return launch_gemm_rs_instance<FMT, MT, 32, EXACT>(a, pdl, s);
+        case 64: return launch_gemm_rs_instance<FMT, MT, 64, EXACT>(a, pdl, s);
+        case 128: return launch_gemm_rs_instance<FMT, MT, 128, EXACT>(a, pdl, s);
+        case 256: return launch_gemm_rs_instance<FMT, MT, 256, EXACT>(a, pdl, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-// 4-bit weights, the fp16-encoded operand, up to 32 rows.
-inline cudaError_t launch_gemm_rs(const GemmArgs &a, bool pdl, cudaStream_t s) {
+// Weights of format FMT, the fp16 row operand, up to 32 rows.
+template <int FMT>
+cudaError_t launch_gemm_rs(const GemmArgs &a, bool pdl, cudaStream_t s) {
     const bool exact = a.partials != nullptr || a.nb_align != 0;
-    if (act_rows(a.M) <= 16) return exact ? launch_gemm_rs_g<16, true>(a, pdl, s) : launch_gemm_rs_g<16, false>(a, pdl, s);
-    return exact ? launch_gemm_rs_g<32, true>(a, pdl, s) : launch_gemm_rs_g<32, false>(a, pdl, s);
+    if (act_rows(a.M) <= 16)
+        return exact ? launch_gemm_rs_g<FMT, 16, true>(a, pdl, s) : launch_gemm_rs_g<FMT, 16, false>(a, pdl, s);
+    return exact ? launch_gemm_rs_g<FMT, 32, true>(a, pdl, s) : launch_gemm_rs_g<FMT, 32, false>(a, pdl, s);
 }
 
 }  // namespace hq

@@ -148,12 +148,12 @@ __global__ void __launch_bounds__(256) k_pack(Geom g, const float *__restrict__ 
                 wv[t] = word;
             }
         } else {
-            // features 16 cp + e, e = 0..15, in order
+            // word t: features 2 t, 2 t + 1, 2 t + 8, 2 t + 9 of the run 16 cp ..
             const uint8_t *p8 = src + cp * 16;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                wv[j] = (uint32_t)p8[4 * j] | ((uint32_t)p8[4 * j + 1] << 8) | ((uint32_t)p8[4 * j + 2] << 16) |
-                        ((uint32_t)p8[4 * j + 3] << 24);
+            for (int t = 0; t < 4; ++t)
+                wv[t] = (uint32_t)p8[2 * t] | ((uint32_t)p8[2 * t + 1] << 8) | ((uint32_t)p8[2 * t + 8] << 16) |
+                        ((uint32_t)p8[2 * t + 9] << 24);
         }
         reinterpret_cast<uint4 *>(tile)[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(256) k_unpack(Geom g, const uint8_t *__restric
                     if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
                 }
             } else {
-                for (int e = 0; e < 4; ++e) {
-                    const int k = kt * g.KT + cp * 16 + j * 4 + e;
+                for (int e = 0; e < 4; ++e) {  // byte e of word j: feature 2 j + (e & 1) + 8 (e >> 1)
+                    const int k = kt * g.KT + cp * 16 + 2 * j + (e & 1) + 8 * (e >> 1);
                     if (k < g.K) codes[(size_t)n * g.K + k] = (uint8_t)(wv[j] >> (8 * e));
                 }
             }

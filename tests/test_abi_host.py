@@ -135,13 +135,14 @@ def test_q8_workspace_and_argument_checks():
 def test_act_operand_bytes():
     # opaque, but its size follows from the rows padded to the MMA's N (16, 32,
     # 64, 128), 128-feature blocks of 2 bytes per code (fp16, or two e4m3
-    # digits; rows of 272 bytes for the register-resident GEMM of 4-bit
-    # weights up to 32 rows), and one fp32 sum per group and row where the
+    # digits; rows of 272 bytes for the register-resident GEMM up to 32
+    # rows), and one fp32 sum per group and row where the
     # GEMM applies a 4-bit zero point through them (above 32 rows)
     def size(M, K, G, fmt="w4"):
         return hq.hq_act_operand_bytes(hq.make_desc(K, 128, G, fmt), M)
     assert size(16, 4096, 64) == 32 * 16 * 272  # the zero point is applied to the weights
-    assert size(16, 4096, 64, "w8") == 32 * 16 * 256
+    assert size(16, 4096, 64, "w8") == 32 * 16 * 272
+    assert size(33, 4096, 64, "w8") == 32 * 64 * 256  # the tensor-memory GEMM's encoding
     assert size(3, 96, 32) == 1 * 16 * 272  # one padded block
     assert size(32, 4096, 256) == 32 * 32 * 272
     assert size(33, 512, 256) == 4 * 64 * 256 + 2 * 64 * 4  # group sums for the 4-bit zero point

@@ -160,8 +160,8 @@ def test_kernel_source_hash_follows_the_gemm_sources(tmp_path, monkeypatch):
 
 
 def test_gemm_kernel_name_follows_the_library_dispatch():
-    assert bench.gemm_kernel_name("w4", 16) == bench.gemm_kernel_name("w4", 32) == "k_verify_gemm_rs"
-    assert bench.gemm_kernel_name("w4", 33) == bench.gemm_kernel_name("w8", 16) == "k_verify_gemm"
+    assert bench.gemm_kernel_name("w4", 16) == bench.gemm_kernel_name("w8", 32) == "k_verify_gemm_rs"
+    assert bench.gemm_kernel_name("w4", 33) == bench.gemm_kernel_name("w8", 128) == "k_verify_gemm"
 
 
 # ------------------------------------------------------ reference arm ---
